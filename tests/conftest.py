@@ -1,0 +1,28 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: full-size workloads (minutes)")
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests fail loudly rather than skip when no device is present; the
+    # "-m 'not gpu'" selection is what keeps them off CPU-only machines.
+    pass
+
+
+@pytest.fixture(scope="session")
+def oracle_mod():
+    import oracle
+    return oracle.default()

@@ -1,0 +1,438 @@
+"""Pins for the float64 CPU oracle: checks against things other than the oracle.
+
+Each ``pin_*`` function takes a loaded :class:`oracle.Oracle` and raises
+``AssertionError`` when the oracle disagrees with what the pages or the
+mathematics fix: values the pages print, hand-derived cases from the pages'
+definitions (``tests/golden/``), closed forms, library routines (scipy), and
+central finite differences.  ``test_oracle_pins.py`` runs them against the
+real oracle; ``test_oracle_mutants.py`` runs them against builds with planted
+mistakes and requires each mistake to fail at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+from vocab_wide_logprob_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(fname):
+    with open(os.path.join(GOLDEN, fname)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                yield line
+
+
+# --------------------------------------------------------------------------
+# "The completion mask"
+# --------------------------------------------------------------------------
+
+def mask_cases():
+    cases = []
+    for line in _rows("mask_cases.txt"):
+        eos, prompt, comp, exp_mask, exp_len = [s.split() for s in line.split("|")]
+        cases.append((int(eos[0]), [int(x) for x in prompt], [int(x) for x in comp],
+                      [int(x) for x in exp_mask], int(exp_len[0])))
+    return cases
+
+
+def pin_mask_golden(o):
+    for eos, prompt, comp, exp_mask, exp_len in mask_cases():
+        ids = np.array([prompt + comp], np.int64)
+        m, ln = o.mask(ids, len(prompt), len(comp), eos)
+        assert m[0].tolist() == exp_mask, (prompt, comp, m[0].tolist(), exp_mask)
+        assert int(ln[0]) == exp_len, (prompt, comp, int(ln[0]), exp_len)
+
+
+def pin_mask_batch_matches_rows(o):
+    """All golden cases with equal shapes stacked into one batch give the
+    same rows as one at a time (no cross-row leakage)."""
+    cases = [c for c in mask_cases() if len(c[1]) == 2 and len(c[2]) == 6 and c[0] == 2]
+    ids = np.array([c[1] + c[2] for c in cases], np.int64)
+    m, ln = o.mask(ids, 2, 6, 2)
+    assert m.tolist() == [c[3] for c in cases]
+    assert ln.tolist() == [c[4] for c in cases]
+
+
+# --------------------------------------------------------------------------
+# "Dr. GRPO" advantage: A_i = R_i - mean of the group, no sigma
+# --------------------------------------------------------------------------
+
+def pin_advantage_examples(o):
+    # hand-derived: one success among four -> mean 1/4
+    assert o.advantage(np.array([1, 0, 0, 0.]), 4).tolist() == [0.75, -0.25, -0.25, -0.25]
+    # two groups of four: (1,1,0,0) mean 1/2; (0,0,0,1) mean 1/4
+    assert o.advantage(np.array([1, 1, 0, 0, 0, 0, 0, 1.]), 4).tolist() == \
+        [0.5, 0.5, -0.5, -0.5, -0.25, -0.25, -0.25, 0.75]
+    # uniform groups carry no contrast: every advantage is exactly zero
+    assert o.advantage(np.ones(8), 8).tolist() == [0.0] * 8
+    assert o.advantage(np.zeros(16), 16).tolist() == [0.0] * 16
+    # no division by the group's standard deviation: scaling rewards by 3
+    # scales advantages by 3 (a sigma-normalised advantage would not change)
+    a1 = o.advantage(np.array([1, 0, 0, 0.]), 4)
+    a3 = o.advantage(np.array([3, 0, 0, 0.]), 4)
+    assert np.allclose(a3, 3 * a1, rtol=0, atol=1e-15)
+    # G = 3, real rewards: mean 0.5 -> (0.5, -0.25, -0.25)
+    assert np.allclose(o.advantage(np.array([1.0, 0.25, 0.25]), 3), [0.5, -0.25, -0.25],
+                       rtol=0, atol=1e-15)
+    # G = 1: a single completion is its own baseline
+    assert o.advantage(np.array([1.0, 0.0]), 1).tolist() == [0.0, 0.0]
+
+
+def no_contrast_golden():
+    out = []
+    for line in _rows("no_contrast.txt"):
+        q, p, G, printed, dec = line.split()
+        out.append((q, float(p), int(G), float(printed), int(dec)))
+    return out
+
+
+def pin_printed_probabilities():
+    """The closed forms reproduce the digits the pages print."""
+    for q, p, G, printed, dec in no_contrast_golden():
+        val = (1 - p) ** G if q == "all_fail" else (1 - p) ** G + p ** G
+        assert round(val, dec) == printed, (q, p, G, val, printed)
+
+
+def pin_advantage_monte_carlo(o, groups=1_000_000):
+    """Rewards from the generator's Bernoulli draw, advantages from the
+    oracle: the fraction of groups whose advantages are all zero matches the
+    pages' closed form (1-p)^G + p^G within 4 standard errors, and the mixture
+    p ~ U(0, 1/2) used by the batched workload matches its closed form 2/9."""
+    cases = [(0.05, 8, 0.95 ** 8 + 0.05 ** 8), (0.05, 16, 0.95 ** 16 + 0.05 ** 16)]
+    for p, G, exact in cases:
+        w = wl.Workload("mc", B=groups, G=G, P=1, C=1, V=2, dtype="f32", logit_std=1.0,
+                        eos_id=0, reward_p=p, seed=777 + G)
+        A = o.advantage(wl.make_rewards(w), G).reshape(groups, G)
+        frac = float(np.mean(np.all(A == 0.0, axis=1)))
+        se = math.sqrt(exact * (1 - exact) / groups)
+        assert abs(frac - exact) < 4 * se, (p, G, frac, exact, se)
+    # int_0^{1/2} [(1-p)^8 + p^8] dp / (1/2) = 2 * (1/9) = 2/9 for G = 8
+    w = wl.Workload("mc_mix", B=groups, G=8, P=1, C=1, V=2, dtype="f32", logit_std=1.0,
+                    eos_id=0, reward_p_range=(0.0, 0.5), seed=4242)
+    A = o.advantage(wl.make_rewards(w), 8).reshape(groups, 8)
+    frac = float(np.mean(np.all(A == 0.0, axis=1)))
+    exact = 2.0 / 9.0
+    se = math.sqrt(exact * (1 - exact) / groups)
+    assert abs(frac - exact) < 4 * se, (frac, exact, se)
+
+
+# --------------------------------------------------------------------------
+# "compute_logprobs": shift by one, log_softmax, gather
+# --------------------------------------------------------------------------
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest even) and return the bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def _bf16_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_logp_constant_row(o):
+    """A constant row is the uniform distribution: logp = -ln V exactly."""
+    for V in (1, 7, 1024, 151936):
+        for c in (0.0, 3.7, -120.5):
+            row = np.full((1, V), c, np.float64)
+            lp, ls = o.logp_rows(row, "f64", np.array([V // 2]))
+            assert abs(lp[0] + math.log(V)) <= 1e-12 * max(1.0, math.log(V)), (V, c, lp)
+            assert abs(ls[0] - (c + math.log(V))) <= 1e-12 * max(1.0, abs(c) + 12), (V, c, ls)
+
+
+def pin_logp_two_level(o):
+    """k entries equal to a, the rest equal to b: closed-form logsumexp
+    a + ln(k + (V-k) e^(b-a))."""
+    for V, k, a, b in [(1024, 1, 9.0, 0.0), (151936, 5, 2.5, -1.0), (33, 32, 0.0, 4.0)]:
+        row = np.full(V, b, np.float64)
+        row[:k] = a
+        lse = a + math.log(k + (V - k) * math.exp(b - a))
+        lp, ls = o.logp_rows(row[None, :], "f64", np.array([0]))
+        assert abs(ls[0] - lse) < 1e-12 * max(1, abs(lse)), (V, k, ls[0], lse)
+        assert abs(lp[0] - (a - lse)) < 1e-12 * max(1, abs(lse)), (V, k, lp[0], a - lse)
+        lp2, _ = o.logp_rows(row[None, :], "f64", np.array([V - 1]))
+        assert abs(lp2[0] - (b - lse)) < 1e-12 * max(1, abs(lse))
+
+
+def pin_logp_library(o):
+    """Random rows in f64, f32 and bf16 against scipy.special.log_softmax."""
+    from scipy.special import log_softmax
+    rng = np.random.default_rng(5)
+    for V in (2, 1000, 1003, 151936):
+        x = rng.normal(0.0, 3.0, size=(4, V))
+        y = rng.integers(0, V, size=4)
+        ref = log_softmax(x, axis=1)[np.arange(4), y]
+        lp, _ = o.logp_rows(x, "f64", y)
+        assert np.max(np.abs(lp - ref)) < 1e-11, (V, np.max(np.abs(lp - ref)))
+        x32 = x.astype(np.float32)
+        ref32 = log_softmax(x32.astype(np.float64), axis=1)[np.arange(4), y]
+        lp32, _ = o.logp_rows(x32, "f32", y)
+        assert np.max(np.abs(lp32 - ref32)) < 1e-11
+        xb = _bf16_bits(x32)
+        refb = log_softmax(_bf16_to_f64(xb), axis=1)[np.arange(4), y]
+        lpb, _ = o.logp_rows(xb, "bf16", y)
+        assert np.max(np.abs(lpb - refb)) < 1e-11
+    # rows with -inf entries (a masked vocabulary) and a huge spread
+    x = np.array([[-np.inf, 0.0, 1.0, -np.inf, 80.0, -80.0]])
+    ref = log_softmax(x, axis=1)
+    for y in (1, 2, 4, 5):
+        lp, _ = o.logp_rows(x, "f64", np.array([y]))
+        assert abs(lp[0] - ref[0, y]) < 1e-12, (y, lp[0], ref[0, y])
+    lp, _ = o.logp_rows(x, "f64", np.array([0]))
+    assert lp[0] == -np.inf
+
+
+def pin_logp_token_range(o):
+    """A sampled id outside [0, V) is refused."""
+    for bad in (-1, 8):
+        try:
+            o.logp_rows(np.zeros((1, 8)), "f64", np.array([bad]))
+        except ValueError:
+            continue
+        raise AssertionError(f"token id {bad} accepted")
+
+
+def pin_logp_shift(o):
+    """"logits at position t predict the token at t+1": completion token t is
+    scored by logits row P-1+t.  Plant a large logit at (row P-1+t, column
+    y_t) for even t only; rows of odd t stay all-zero.  Then logp is ~0 at
+    even t and exactly -ln V at odd t; a shift by one swaps the pattern."""
+    N, P, C, V, big = 3, 5, 8, 64, 60.0
+    rng = np.random.default_rng(11)
+    ids = rng.integers(3, V, size=(N, P + C))
+    lens = np.array([C, 5, 1], np.int32)
+    z = np.zeros((N, P + C, V))
+    for i in range(N):
+        for t in range(0, C, 2):
+            z[i, P - 1 + t, ids[i, P + t]] = big
+    lp, ls = o.logp(z, "f64", P, C, ids, lens)
+    for i in range(N):
+        for t in range(C):
+            if t >= lens[i]:
+                assert lp[i, t] == 0.0 and ls[i, t] == 0.0
+            elif t % 2 == 0:
+                assert -1e-20 < lp[i, t] <= 0.0 and lp[i, t] > -(V) * math.exp(-big) * 1.01
+            else:
+                assert abs(lp[i, t] + math.log(V)) < 1e-12, (i, t, lp[i, t])
+
+
+# --------------------------------------------------------------------------
+# "The loss": clipped surrogate, KL, token-sum / constant
+# --------------------------------------------------------------------------
+
+def surrogate_cases():
+    return [tuple(float(x) for x in line.split()) for line in _rows("surrogate_cases.txt")]
+
+
+def kl_cases():
+    return [tuple(float(x) for x in line.split()) for line in _rows("kl_cases.txt")]
+
+
+def pin_surrogate_golden(o):
+    """One token per completion, norm 1, beta 0: ell = -s, w = -ds."""
+    for A, r, eps, s, ds in surrogate_cases():
+        lp = np.array([[-2.0]])
+        old = lp - math.log(r)   # exp(lp - old) = r
+        loss, w, ell = o.loss(lp, old, None, np.array([A]), np.array([1], np.int32),
+                              eps, 0.0, 1.0)
+        assert abs(ell[0, 0] + s) < 1e-12, (A, r, eps, ell[0, 0], -s)
+        assert abs(loss + s) < 1e-12
+        assert abs(w[0, 0] + ds) < 1e-12, (A, r, eps, w[0, 0], -ds)
+
+
+def pin_kl_golden(o):
+    """Zero advantage, beta 0.5, norm 2: ell = beta*k3, w = beta*dk3/norm."""
+    beta, norm = 0.5, 2.0
+    for d, k3, dk3 in kl_cases():
+        lp = np.array([[-1.25]])
+        ref = lp + d
+        loss, w, ell = o.loss(lp, None, ref, np.array([0.0]), np.array([1], np.int32),
+                              0.2, beta, norm)
+        assert abs(ell[0, 0] - beta * k3) < 1e-14, (d, ell[0, 0], beta * k3)
+        assert abs(loss - beta * k3 / norm) < 1e-14
+        assert abs(w[0, 0] - beta * dk3 / norm) < 1e-14, (d, w[0, 0], beta * dk3 / norm)
+
+
+def _tiny_inputs(o):
+    w = wl.TINY
+    ids = wl.make_ids(w)
+    z, dt = wl.logits_as_numpy(wl.make_logits_cpu(w))
+    m, lens = o.mask(ids, w.P, w.C, w.eos_id)
+    A = o.advantage(wl.make_rewards(w), w.G)
+    lp, ls = o.logp(z, dt, w.P, w.C, ids, lens)
+    return w, ids, z, dt, m, lens, A, lp, ls
+
+
+def pin_step0_identity(o):
+    """"On inner step 0 ... ratio is exactly 1 everywhere and the loss reduces
+    to -(advantages * mask).sum(dim=1).mean()": with the constant N*C the same
+    identity reads loss = -sum_i A_i len_i / (N*C); with norm = N it is the
+    page's own expression."""
+    w, ids, z, dt, m, lens, A, lp, ls = _tiny_inputs(o)
+    N, C = w.N, w.C
+    page_value = -float(np.mean(np.sum(A[:, None] * m, axis=1)))
+    for old in (None, lp.copy()):
+        loss, wt, ell = o.loss(lp, old, None, A, lens, w.eps, 0.0)
+        assert abs(loss - page_value * N / (N * C)) < 1e-14, (loss, page_value / C)
+        loss_n, _, _ = o.loss(lp, old, None, A, lens, w.eps, 0.0, float(N))
+        assert abs(loss_n - page_value) < 1e-13, (loss_n, page_value)
+        assert np.allclose(wt, -(A[:, None] * m) / (N * C), rtol=0, atol=1e-17)
+    # zero advantages and no KL: no loss and no gradient at all
+    loss, wt, _ = o.loss(lp, None, None, np.zeros(N), lens, w.eps, 0.0)
+    assert loss == 0.0 and not np.any(wt)
+
+
+def pin_ratio_closed_form(o):
+    """old = logp - ln r0 on every token gives r = r0; for r0 = 1.5, eps 0.2 the
+    surrogate is 1.2*A for A > 0 and 1.5*A for A < 0."""
+    w, ids, z, dt, m, lens, A, lp, ls = _tiny_inputs(o)
+    N, C = w.N, w.C
+    old = lp - math.log(1.5)
+    s = np.where(A > 0, 1.2 * A, 1.5 * A)
+    expect = -float(np.sum(s * lens)) / (N * C)
+    loss, wt, ell = o.loss(lp, old, None, A, lens, 0.2, 0.0)
+    assert abs(loss - expect) < 1e-13, (loss, expect)
+    ds = np.where(A > 0, 0.0, 1.5 * A)
+    assert np.allclose(wt, -(ds[:, None] * m) / (N * C), rtol=0, atol=1e-15)
+
+
+def pin_kl_closed_form(o):
+    """Uniform rewards (A = 0), ref = logp + ln 2: every valid token adds
+    beta*(1 - ln 2), and w = -beta/(N*C) on valid tokens."""
+    w, ids, z, dt, m, lens, A, lp, ls = _tiny_inputs(o)
+    N, C = w.N, w.C
+    beta = 0.04
+    ref = lp + math.log(2.0)
+    loss, wt, _ = o.loss(lp, None, ref, np.zeros(N), lens, 0.2, beta)
+    expect = beta * (1 - math.log(2.0)) * float(lens.sum()) / (N * C)
+    assert abs(loss - expect) < 1e-15, (loss, expect)
+    assert np.allclose(wt, -beta * m / (N * C), rtol=0, atol=1e-17)
+
+
+def pin_masked_never_read(o):
+    """Old and reference log-probs past the first EOS are padding: NaN there
+    changes nothing ("the mask multiplies per_token_loss, not ratio")."""
+    w, ids, z, dt, m, lens, A, lp, ls = _tiny_inputs(o)
+    rng = np.random.default_rng(3)
+    old = lp + rng.normal(0, 0.1, lp.shape)
+    ref = lp + rng.normal(0, 0.1, lp.shape)
+    l1, w1, e1 = o.loss(lp, old, ref, A, lens, 0.2, 0.04)
+    old[m == 0] = np.nan
+    ref[m == 0] = np.nan
+    l2, w2, e2 = o.loss(lp, old, ref, A, lens, 0.2, 0.04)
+    assert l1 == l2 and np.array_equal(w1, w2) and np.array_equal(e1, e2)
+    assert np.all(e2[m == 0] == 0.0) and np.all(w2[m == 0] == 0.0)
+
+
+# --------------------------------------------------------------------------
+# "loss.backward()": gradient with respect to the logits
+# --------------------------------------------------------------------------
+
+def _away_from_kinks(rng, shape, eps):
+    """Noise on log-probs whose ratio exp(-noise) stays >= 0.01 (in log space)
+    away from the clip boundaries 1-eps and 1+eps."""
+    kinks = np.array([-math.log(1 + eps), -math.log(1 - eps)])
+    x = rng.normal(0, 0.2, shape)
+    bad = np.min(np.abs(x[..., None] - kinks), axis=-1) < 0.01
+    x[bad] += 0.05
+    return x
+
+
+def _fd_setup(o, z, P, C, ids, lens, A, eps, beta, norm, seed):
+    lp, _ = o.logp(z, "f64", P, C, ids, lens)
+    rng = np.random.default_rng(seed)
+    old = lp + _away_from_kinks(rng, lp.shape, eps)
+    ref = lp + rng.normal(0, 0.3, lp.shape)
+
+    def f(zz):
+        lpz, _ = o.logp(zz, "f64", P, C, ids, lens)
+        return o.loss(lpz, old, ref, A, lens, eps, beta, norm)[0]
+
+    lp, ls = o.logp(z, "f64", P, C, ids, lens)
+    _, wt, _ = o.loss(lp, old, ref, A, lens, eps, beta, norm)
+    return f, ls, wt
+
+
+def _fd_check(o, z, P, C, ids, lens, A, eps, beta, norm, entries, seed, g=1.0):
+    f, ls, wt = _fd_setup(o, z, P, C, ids, lens, A, eps, beta, norm, seed)
+    an = o.dlogits(z, "f64", P, C, ids, lens, ls, wt, g)
+    h = 1e-5
+    for (i, r, v) in entries:
+        zp = z.copy()
+        zp[i, r, v] += h
+        zm = z.copy()
+        zm[i, r, v] -= h
+        fd = g * (f(zp) - f(zm)) / (2 * h)
+        a = an[i, r, v]
+        assert abs(fd - a) <= 1e-8 + 1e-5 * abs(a), ((i, r, v), fd, a)
+    return an
+
+
+def pin_dlogits_fd_micro(o):
+    """Every entry of a micro batch (B=2, G=2, P=2, C=4, V=8) against central
+    finite differences of the oracle's own loss (float64 logits, h = 1e-5),
+    with clipping, the KL term and masked rows all active."""
+    B, G, P, C, V = 2, 2, 2, 4, 8
+    rng = np.random.default_rng(21)
+    z = rng.normal(0, 2, size=(B * G, P + C, V))
+    ids = rng.integers(3, V, size=(B * G, P + C))
+    ids[1, P + 2] = 2          # EOS at index 2 -> length 3
+    ids[2, P + 0:] = 2         # EOS first -> length 1
+    _, lens = o.mask(ids, P, C, 2)
+    assert lens.tolist() == [4, 3, 1, 4]
+    A = o.advantage(np.array([1, 0, 0, 1.]), G)
+    entries = [(i, r, v) for i in range(B * G) for r in range(P + C) for v in range(V)]
+    an = _fd_check(o, z, P, C, ids, lens, A, 0.2, 0.1, 1.0, entries, seed=22)
+    # invariants: each scored row sums to zero; rows that score nothing are 0
+    for i in range(B * G):
+        for r in range(P + C):
+            t = r - (P - 1)
+            if 0 <= t < lens[i]:
+                assert abs(an[i, r].sum()) < 1e-14
+            else:
+                assert not np.any(an[i, r])
+
+
+def pin_dlogits_fd_tiny(o):
+    """200 random entries of the tiny workload (logits widened to float64),
+    half of them in scored rows, with old/ref noise, beta = 0.04, norm 1,
+    and an upstream gradient g = 2.5."""
+    w, ids, z, dt, m, lens, A, lp, ls = _tiny_inputs(o)
+    z = z.astype(np.float64)
+    rng = np.random.default_rng(23)
+    entries = []
+    for _ in range(100):
+        i = int(rng.integers(0, w.N))
+        t = int(rng.integers(0, lens[i]))
+        v = int(ids[i, w.P + t]) if rng.random() < 0.3 else int(rng.integers(0, w.V))
+        entries.append((i, w.P - 1 + t, v))
+    for _ in range(100):
+        entries.append((int(rng.integers(0, w.N)), int(rng.integers(0, w.T)),
+                        int(rng.integers(0, w.V))))
+    _fd_check(o, z, w.P, w.C, ids, lens, A, 0.2, 0.04, 1.0, entries, seed=24, g=2.5)
+
+
+def pin_dlogits_row_closed_form(o):
+    """Constant row (uniform softmax 1/V): out = gw*(onehot - 1/V)."""
+    V, y, gw = 16, 5, 0.3
+    row = np.zeros(V)
+    out = o.dlogits_row(row, "f64", y, math.log(V), gw)
+    expect = np.full(V, -gw / V)
+    expect[y] += gw
+    assert np.allclose(out, expect, rtol=0, atol=1e-16)
+
+
+ALL_CHEAP = [
+    pin_mask_golden, pin_mask_batch_matches_rows, pin_advantage_examples,
+    pin_logp_constant_row, pin_logp_two_level, pin_logp_library, pin_logp_token_range,
+    pin_logp_shift, pin_surrogate_golden, pin_kl_golden, pin_step0_identity,
+    pin_ratio_closed_form, pin_kl_closed_form, pin_masked_never_read,
+    pin_dlogits_row_closed_form, pin_dlogits_fd_micro, pin_dlogits_fd_tiny,
+]

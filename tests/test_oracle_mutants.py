@@ -1,0 +1,71 @@
+"""Planted mistakes in the oracle must fail its pins.
+
+Each mutant is a copy of ``oracle/grpo_oracle.c`` with one plausible mistake
+(a dropped term, a wrong sign or index, a transposed operand, the traps the
+page "Making Dr GRPO go brrr" warns about), compiled on the CPU into a
+temporary library.  The test requires at least one pin of
+``oracle_pins.ALL_CHEAP`` to reject it.  CPU only."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+MUTANTS = {
+    # "The completion mask"
+    "mask_drops_eos_itself": ("j <= first_eos : 1", "j < first_eos : 1"),
+    "mask_argmax_trap": ("int64_t first_eos = -1;", "int64_t first_eos = 0;"),
+    "mask_no_eos_all_zero": ("j <= first_eos : 1)", "j <= first_eos : 0)"),
+    "len_off_by_one": ("first_eos + 1 : C", "first_eos : C"),
+    # advantage
+    "advantage_divides_by_G_minus_1": ("sum / (double)G", "sum / (double)(G - 1)"),
+    "advantage_sign": ("R[b * G + g] - mu;", "mu - R[b * G + g];"),
+    # compute_logprobs
+    "shift_off_by_one": ("i * c->T + (c->P - 1 + t)", "i * c->T + (c->P + t)"),
+    "lse_drops_max": ("return mx + log(s);", "return log(s);"),
+    "bf16_wrong_shift": ("[v] << 16;", "[v] << 8;"),
+    "target_wrong_column": ("c->ids[i * c->T + c->P + t];\n    const void",
+                            "c->ids[i * c->T + c->P + t - 1];\n    const void"),
+    # the loss
+    "ratio_inverted": ("exp(lp - old[k])", "exp(old[k] - lp)"),
+    "clip_after_multiply": ("clamp_d(r, 1.0 - eps, 1.0 + eps) * a", "clamp_d(r * a, 1.0 - eps, 1.0 + eps)"),
+    "min_becomes_max": ("unclipped < clipped ? unclipped : clipped",
+                        "unclipped > clipped ? unclipped : clipped"),
+    "surrogate_sign": ("double l = -s + beta * k3;", "double l = s + beta * k3;"),
+    "kl_dropped": ("double l = -s + beta * k3;", "double l = -s;"),
+    "k3_sign": ("k3 = exp(d) - d - 1.0;", "k3 = exp(d) + d - 1.0;"),
+    "norm_per_response": ("norm = (double)N * (double)C;", "norm = (double)N;"),
+    "mask_off_by_one_in_loss": ("if (t >= len[i]) {\n                if (w)", "if (t > len[i]) {\n                if (w)"),
+    # the gradient
+    "grad_ignores_clip": ("unclipped <= clipped ? a * r : 0.0", "a * r"),
+    "grad_kl_sign": ("dk3 = 1.0 - exp(d);", "dk3 = exp(d) - 1.0;"),
+    "grad_drops_onehot": ("(v == y ? 1.0 : 0.0) - p", "-p"),
+    "grad_sign": ("out[v] = gw * ((v", "out[v] = -gw * ((v"),
+    "grad_row_shift": ("int64_t t = pos - (c->P - 1);", "int64_t t = pos - c->P;"),
+    "grad_ignores_upstream": ("c->g * c->w[k]", "c->w[k]"),
+}
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, source, tmp_path):
+    old, new = MUTANTS[name]
+    assert source.count(old) == 1, f"mutation site for {name} not unique/present"
+    src = tmp_path / f"{name}.c"
+    src.write_text(source.replace(old, new))
+    lib = oracle.compile_source(str(src), str(tmp_path / f"{name}.so"))
+    o = oracle.Oracle(lib)
+    failures = []
+    for pin in pins.ALL_CHEAP:
+        try:
+            pin(o)
+        except (AssertionError, ValueError) as e:
+            failures.append(pin.__name__)
+            break
+    assert failures, f"mutant {name} passed every pin"
