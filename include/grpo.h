@@ -1,0 +1,182 @@
+/*
+ * grpo.h -- C ABI of the GB300 (sm_103a) Dr. GRPO loss library.
+ *
+ * The library computes the data-parallel hot path of one Dr. GRPO update
+ * step over policy logits, forward and backward, as the page "Making Dr GRPO
+ * go brrr" (salahadawi.com, "i-made-a-kernel-22x-faster-it-made-my-training-
+ * loop-3x-slower") defines it:
+ *
+ *   grpo_mask       "The completion mask" (build_completion_mask)
+ *   grpo_advantage  "Dr. GRPO": A_i = R_i - mean of the group, no sigma
+ *   grpo_loss_fwd   "compute_logprobs" (shift, log_softmax, gather) and
+ *                   "The loss" (grpo_loss): clipped surrogate, optional k3 KL
+ *                   term, token-sum aggregation divided by a constant
+ *   grpo_loss_bwd   "loss.backward()": d loss / d logits
+ *
+ * Shapes: N = B*G completions (completions b*G .. b*G+G-1 answer prompt b),
+ * P prompt tokens, C completion tokens, T = P + C, vocabulary V.  Completion
+ * token t of sequence i is input_ids[i, P+t]; it is scored by logits row
+ * P-1+t of sequence i ("logits at position t predict the token at t+1").
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers to dense row-major arrays.  The
+ *    caller owns all memory; the library never allocates, frees or keeps a
+ *    pointer after a call returns.
+ *  - Calls only enqueue work on `stream` and return without synchronising,
+ *    except grpo_check_error.  Results are bitwise reproducible run to run
+ *    for the same inputs and shapes on the same GPU model.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    validation failure returns an error and enqueues nothing.  A failed
+ *    launch returns GRPO_ERR_CUDA.  No C++ exception crosses this boundary.
+ *  - Data-dependent problems (a scored token id outside [0, V), a length
+ *    outside [0, C]) cannot be seen on the host without a synchronisation;
+ *    the kernels record them in the workspace and grpo_check_error reports
+ *    them.  The kernels never trap.
+ *  - Inputs at positions the mask excludes (old_logp and ref_logp past the
+ *    first EOS) are never read; outputs there are 0.
+ *  - Index arithmetic is 64-bit; N*C must be below 2^31.
+ */
+#ifndef GRPO_H
+#define GRPO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *grpo_stream_t;
+
+typedef enum {
+    GRPO_OK = 0,
+    GRPO_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad eps/beta/G */
+    GRPO_ERR_UNSUPPORTED = 2,  /* dtype or size outside what the kernels take */
+    GRPO_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required  */
+    GRPO_ERR_MISALIGNED = 4,   /* pointer not aligned as documented           */
+    GRPO_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+    GRPO_ERR_TOKEN_RANGE = 6,  /* a scored token id was outside [0, V)        */
+    GRPO_ERR_LENGTH_RANGE = 7, /* a completion length was outside [0, C]      */
+    GRPO_ERR_TIMEOUT = 8       /* a bounded device-side wait gave up          */
+} grpo_status;
+
+typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1 } grpo_dtype;
+
+/* Static English description of a status code. */
+const char *grpo_status_string(grpo_status status);
+
+/*
+ * grpo_mask -- completion mask ("The completion mask", build_completion_mask).
+ *
+ * input_ids [N, P+C] int64, 8-byte aligned; only columns P .. P+C-1 (the
+ *           completion) are read.
+ * mask      [N, C] uint8 out, may be NULL: 1 at positions up to and including
+ *           the first id equal to eos_id, 0 after it; every position 1 when
+ *           the completion holds no EOS (the torch.where fallback that keeps
+ *           argmax's 0 on a row without EOS from masking the completion).
+ * len       [N] int32 out: the number of 1s of each mask row, i.e. the first
+ *           EOS index + 1, or C.  The loss calls take `len`: the mask is a
+ *           prefix of each row.
+ * N, P, C >= 0.  N == 0 enqueues nothing.
+ */
+grpo_status grpo_mask(const int64_t *input_ids, int64_t N, int64_t P, int64_t C,
+                      int64_t eos_id, uint8_t *mask, int32_t *len, grpo_stream_t stream);
+
+/*
+ * grpo_advantage -- Dr. GRPO group advantage (section "Dr. GRPO": both
+ * denominators removed, A_i = R_i - mu; code "rewards_grouped -
+ * rewards_grouped.mean(dim=1, keepdim=True)").
+ *
+ * rewards [B*G] float32, grouped as [B, G]; adv [B*G] float32 out:
+ * adv_i = R_i - (sum of the group's rewards) / G, in float32.  For binary
+ * rewards and power-of-two G every step is exact.  B >= 0, G >= 1.
+ */
+grpo_status grpo_advantage(const float *rewards, int64_t B, int64_t G, float *adv,
+                           grpo_stream_t stream);
+
+/*
+ * grpo_workspace_size -- bytes of device scratch grpo_loss_fwd needs for N
+ * completions of C tokens (a few bytes per completion).  The workspace needs
+ * no initialisation; grpo_loss_fwd resets what it uses.  It must be 256-byte
+ * aligned and must not be shared by calls that may run concurrently.
+ */
+grpo_status grpo_workspace_size(int64_t N, int64_t C, int64_t V, size_t *bytes);
+
+/*
+ * grpo_loss_fwd -- per-token log-probs and the Dr. GRPO loss.
+ *
+ * logits    [N, P+C, V] of `dtype` (float32 or bfloat16), aligned to its
+ *           element size, read-only.  Only the rows that score a valid token
+ *           (rows P-1 .. P-2+len_i of sequence i) are read.
+ * input_ids [N, P+C] int64; len [N] int32 (from grpo_mask); adv [N] float32.
+ * old_logp  [N, C] float32 or NULL.  NULL means the old policy equals the
+ *           current one (inner step 0): the ratio is exactly 1.
+ * ref_logp  [N, C] float32; may be NULL only when beta == 0.
+ * eps in [0, 1): clip range; beta >= 0: k3 KL weight.
+ * norm      the constant the token sum is divided by; norm <= 0 selects N*C
+ *           (the padded completion width times N).  P >= 1.
+ *
+ * Per valid token (t < len_i), with y = input_ids[i, P+t] and z the logits
+ * row P-1+t of sequence i:
+ *   lse   = log sum_v exp(z_v)                  (float32 accumulation)
+ *   logp  = z_y - lse
+ *   r     = exp(logp - old)                     (1 when old_logp == NULL)
+ *   s     = min(r*A_i, clamp(r, 1-eps, 1+eps)*A_i)
+ *   k3    = exp(ref - logp) - (ref - logp) - 1  (0 when beta == 0)
+ *   ell   = -s + beta*k3
+ *   w     = d loss / d logp = (-(r*A_i if min() selects r*A_i, else 0)
+ *                              + beta*(1 - exp(ref - logp))) / norm
+ *   loss  = (sum over valid tokens of ell) / norm   (float64 accumulation
+ *                                                    in a fixed order)
+ * Outputs: logp, lse, w [N, C] float32 (0 past each length); loss: one
+ * float32 in device memory.
+ * workspace: device scratch of at least grpo_workspace_size bytes.
+ */
+grpo_status grpo_loss_fwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t *input_ids, const int32_t *len,
+                          const float *adv, const float *old_logp, const float *ref_logp,
+                          float eps, float beta, float norm, float *logp, float *lse, float *w,
+                          float *loss, void *workspace, size_t workspace_bytes,
+                          grpo_stream_t stream);
+
+/*
+ * grpo_loss_bwd -- gradient of (grad_loss * loss) with respect to the logits.
+ *
+ * Inputs as for grpo_loss_fwd, plus lse and w from it; grad_loss is one
+ * float32 in device memory (the upstream gradient of the scalar loss) or NULL
+ * for 1.
+ * dlogits [N, P+C, V] of `dtype`, fully written:
+ *   a row that scores valid token t:  g*w_t*([v == y] - exp(z_v - lse_t)),
+ *   every other row (prompt rows 0..P-2, row P+C-1, rows past the first EOS):
+ *   0, as autograd through the slice and the mask gives.
+ * bfloat16 results are rounded to nearest even from float32.  dlogits must
+ * not overlap logits.  Lengths are clamped to [0, C].
+ */
+grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t *input_ids, const int32_t *len,
+                          const float *lse, const float *w, const float *grad_loss,
+                          void *dlogits, grpo_stream_t stream);
+
+/*
+ * grpo_check_error -- synchronises `stream`, then reports what the kernels of
+ * the most recent grpo_loss_fwd on `workspace` recorded: GRPO_OK,
+ * GRPO_ERR_TOKEN_RANGE (a scored id outside [0, V); its logp and lse are NaN),
+ * GRPO_ERR_LENGTH_RANGE (a length outside [0, C]; it was clamped), or
+ * GRPO_ERR_TIMEOUT.  GRPO_ERR_CUDA if the synchronisation itself failed.
+ */
+grpo_status grpo_check_error(const void *workspace, grpo_stream_t stream);
+
+/*
+ * grpo_copy -- dst[0 .. bytes) = src[0 .. bytes) with 16-byte vector loads and
+ * streaming stores: the device-to-device copy ceiling the HBM roofline of the
+ * other kernels is compared with.  Both pointers 16-byte aligned, bytes a
+ * multiple of 16, no overlap.
+ */
+grpo_status grpo_copy(void *dst, const void *src, size_t bytes, grpo_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_H */

@@ -1,0 +1,18 @@
+"""GB300 (sm_103a) Dr. GRPO loss over policy logits, forward and backward.
+
+The compute lives in ``libgrpo.so`` (hand-written CUDA kernels behind the C
+ABI in ``include/grpo.h``); :mod:`vocab_wide_logprob_gb300._native` is its
+thin ctypes binding and :mod:`vocab_wide_logprob_gb300.workloads` draws the
+seeded synthetic inputs.  The binding is imported lazily so that the input
+generators stay usable on machines without the built library.
+"""
+
+_NAMES = ("grpo_mask", "grpo_advantage", "grpo_workspace_size", "grpo_loss_fwd",
+          "grpo_loss_bwd", "grpo_check_error", "grpo_copy", "GrpoError")
+
+
+def __getattr__(name):
+    if name in _NAMES:
+        from . import _native
+        return getattr(_native, name)
+    raise AttributeError(name)

@@ -1,0 +1,198 @@
+"""ctypes binding of ``libgrpo.so`` (the C ABI declared in ``include/grpo.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind these calls.  Functions take PyTorch tensors for device
+memory, pass ``tensor.data_ptr()`` and the current CUDA stream, and raise
+:class:`GrpoError` on any status other than ``GRPO_OK``.  There is no CPU
+fallback: importing this module fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_PKG, "libgrpo.so")
+
+GRPO_OK = 0
+STATUS_NAMES = {
+    0: "GRPO_OK", 1: "GRPO_ERR_INVALID_ARG", 2: "GRPO_ERR_UNSUPPORTED",
+    3: "GRPO_ERR_WORKSPACE", 4: "GRPO_ERR_MISALIGNED", 5: "GRPO_ERR_CUDA",
+    6: "GRPO_ERR_TOKEN_RANGE", 7: "GRPO_ERR_LENGTH_RANGE", 8: "GRPO_ERR_TIMEOUT",
+}
+GRPO_F32, GRPO_BF16 = 0, 1
+
+
+class GrpoError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{where}: {self.name} ({_lib.grpo_status_string(status).decode()})")
+
+
+def _load():
+    if not os.path.exists(LIBRARY):
+        raise ImportError(
+            f"{LIBRARY} is missing: build it with `python -m vocab_wide_logprob_gb300.build` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIBRARY)
+    P, I64, F, SZ, INT = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t,
+                          ctypes.c_int)
+    sig = {
+        "grpo_status_string": ([INT], ctypes.c_char_p),
+        "grpo_mask": ([P, I64, I64, I64, I64, P, P, P], INT),
+        "grpo_advantage": ([P, I64, I64, P, P], INT),
+        "grpo_workspace_size": ([I64, I64, I64, ctypes.POINTER(SZ)], INT),
+        "grpo_loss_fwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P, P, SZ,
+                           P], INT),
+        "grpo_loss_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, P], INT),
+        "grpo_check_error": ([P, P], INT),
+        "grpo_copy": ([P, P, SZ, P], INT),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, where: str):
+    if status != GRPO_OK:
+        raise GrpoError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GRPO_F32
+    if t.dtype == torch.bfloat16:
+        return GRPO_BF16
+    raise TypeError(f"logits dtype {t.dtype} is not supported (float32 or bfloat16)")
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def grpo_mask(input_ids: torch.Tensor, P: int, C: int, eos_id: int, mask=None, len_out=None,
+              stream=None):
+    """Completion mask of ``input_ids`` [N, P+C] int64 -> ``(mask u8 [N, C],
+    len int32 [N])``."""
+    _dev(input_ids, "input_ids", torch.int64)
+    N = input_ids.shape[0]
+    if mask is None:
+        mask = torch.empty((N, C), dtype=torch.uint8, device=input_ids.device)
+    if len_out is None:
+        len_out = torch.empty((N,), dtype=torch.int32, device=input_ids.device)
+    _check(_lib.grpo_mask(_ptr(input_ids), N, P, C, int(eos_id), _ptr(mask), _ptr(len_out),
+                          _stream(stream)), "grpo_mask")
+    return mask, len_out
+
+
+def grpo_advantage(rewards: torch.Tensor, G: int, adv=None, stream=None):
+    """Dr. GRPO advantage: R_i minus its group's mean, float32 [B*G]."""
+    _dev(rewards, "rewards", torch.float32)
+    if adv is None:
+        adv = torch.empty_like(rewards)
+    n = rewards.numel()
+    if G < 1 or n % G:
+        raise ValueError("len(rewards) must be a multiple of G >= 1")
+    _check(_lib.grpo_advantage(_ptr(rewards), n // G, G, _ptr(adv), _stream(stream)),
+           "grpo_advantage")
+    return adv
+
+
+def grpo_workspace_size(N: int, C: int, V: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.grpo_workspace_size(N, C, V, ctypes.byref(out)), "grpo_workspace_size")
+    return int(out.value)
+
+
+def grpo_loss_fwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
+                  beta=0.0, norm=0.0, out=None, workspace=None, stream=None):
+    """Per-token log-probs, gradient weights and the Dr. GRPO loss.
+
+    ``logits`` [N, P+C, V] float32/bfloat16.  Returns a dict with ``logp``,
+    ``lse``, ``w`` ([N, C] float32), ``loss`` (one-element float32 tensor on
+    the device) and ``workspace``.  Pass ``out``/``workspace`` (as returned
+    by an earlier call) to reuse buffers."""
+    _dev(logits, "logits")
+    N, T, V = logits.shape
+    C = T - P
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("adv", adv, torch.float32), ("old_logp", old_logp, torch.float32),
+                        ("ref_logp", ref_logp, torch.float32)):
+        _dev(t, name, dt)
+    dev = logits.device
+    if out is None:
+        out = {"logp": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "lse": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "w": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "loss": torch.empty((1,), dtype=torch.float32, device=dev)}
+    need = grpo_workspace_size(N, C, V)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    out["workspace"] = workspace
+    _check(_lib.grpo_loss_fwd(
+        _ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
+        _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(out["logp"]),
+        _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _ptr(workspace), workspace.numel(),
+        _stream(stream)), "grpo_loss_fwd")
+    return out
+
+
+def grpo_loss_bwd(logits, P, input_ids, lens, lse, w, grad_loss=None, dlogits=None,
+                  stream=None):
+    """d (grad_loss * loss) / d logits, same shape and dtype as ``logits``."""
+    _dev(logits, "logits")
+    N, T, V = logits.shape
+    C = T - P
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("lse", lse, torch.float32), ("w", w, torch.float32),
+                        ("grad_loss", grad_loss, torch.float32)):
+        _dev(t, name, dt)
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    _dev(dlogits, "dlogits", logits.dtype)
+    _check(_lib.grpo_loss_bwd(_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids),
+                              _ptr(lens), _ptr(lse), _ptr(w), _ptr(grad_loss), _ptr(dlogits),
+                              _stream(stream)), "grpo_loss_bwd")
+    return dlogits
+
+
+def grpo_check_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the status the last forward call
+    on ``workspace`` recorded (0 = GRPO_OK); does not raise."""
+    return int(_lib.grpo_check_error(_ptr(workspace), _stream(stream)))
+
+
+def grpo_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: int | None = None, stream=None):
+    """Vector device-to-device copy (the HBM copy ceiling)."""
+    nbytes = src.numel() * src.element_size() if nbytes is None else nbytes
+    _check(_lib.grpo_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "grpo_copy")
+    return dst

@@ -1,0 +1,243 @@
+// C ABI of the library (declared in include/grpo.h): argument validation on
+// the host, then the launches on the caller's stream.  Nothing here allocates
+// device memory or synchronises, except grpo_check_error.
+#include <math.h>
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "grpo.h"
+
+namespace grpo {
+
+int row_split(int64_t row_bytes, const char* env) {
+  if (env != nullptr) {
+    if (const char* s = getenv(env)) {
+      const int k = atoi(s);
+      if (k == 1 || k == 2 || k == 4 || k == 8) return k;
+    }
+  }
+  int k = 1;
+  while (k < 8 && row_bytes / (2 * k) >= 32768) k *= 2;
+  return k;
+}
+
+namespace {
+
+int g_sms[64] = {};  // SM count per device ordinal; benign race (same value)
+
+cudaError_t current_device(DeviceInfo* d) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  d->device = dev;
+  int& sms = g_sms[dev & 63];
+  if (sms == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms = n;
+  }
+  d->sms = sms;
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a*b*c without int64 overflow, or -1
+int64_t mul3(int64_t a, int64_t b, int64_t c) {
+  if (a < 0 || b < 0 || c < 0) return -1;
+  if (a == 0 || b == 0 || c == 0) return 0;
+  if (a > INT64_MAX / b) return -1;
+  const int64_t ab = a * b;
+  if (ab > INT64_MAX / c) return -1;
+  return ab * c;
+}
+
+grpo_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA; }
+
+// Shape checks shared by the loss calls.
+grpo_status check_shapes(grpo_dtype dtype, int64_t N, int64_t P, int64_t C, int64_t V) {
+  if (dtype != GRPO_F32 && dtype != GRPO_BF16) return GRPO_ERR_UNSUPPORTED;
+  if (N < 0 || P < 1 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;  // N*C < 2^31
+  const int64_t elems = mul3(N, P + C, V);
+  if (elems < 0 || elems > INT64_MAX / 4) return GRPO_ERR_UNSUPPORTED;
+  return GRPO_OK;
+}
+
+}  // namespace
+}  // namespace grpo
+
+using namespace grpo;
+
+extern "C" {
+
+const char* grpo_status_string(grpo_status s) {
+  switch (s) {
+    case GRPO_OK:
+      return "ok";
+    case GRPO_ERR_INVALID_ARG:
+      return "invalid argument";
+    case GRPO_ERR_UNSUPPORTED:
+      return "unsupported dtype or size";
+    case GRPO_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case GRPO_ERR_MISALIGNED:
+      return "pointer misaligned";
+    case GRPO_ERR_CUDA:
+      return "CUDA runtime error";
+    case GRPO_ERR_TOKEN_RANGE:
+      return "a scored token id is outside [0, V)";
+    case GRPO_ERR_LENGTH_RANGE:
+      return "a completion length is outside [0, C]";
+    case GRPO_ERR_TIMEOUT:
+      return "a device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+grpo_status grpo_mask(const int64_t* input_ids, int64_t N, int64_t P, int64_t C, int64_t eos_id,
+                      uint8_t* mask, int32_t* len, grpo_stream_t stream) {
+  if (N < 0 || P < 0 || C < 0) return GRPO_ERR_INVALID_ARG;
+  if (N == 0) return GRPO_OK;
+  if (len == nullptr || (C > 0 && input_ids == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (mul3(N, P + C, 8) < 0 || C > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
+  if (!aligned(input_ids, 8) || !aligned(len, 4)) return GRPO_ERR_MISALIGNED;
+  return from_cuda(launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream));
+}
+
+grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* adv,
+                           grpo_stream_t stream) {
+  if (B < 0 || G < 1) return GRPO_ERR_INVALID_ARG;
+  if (B == 0) return GRPO_OK;
+  if (rewards == nullptr || adv == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
+  if (!aligned(rewards, 4) || !aligned(adv, 4)) return GRPO_ERR_MISALIGNED;
+  return from_cuda(launch_advantage(rewards, B, G, adv, (cudaStream_t)stream));
+}
+
+grpo_status grpo_workspace_size(int64_t N, int64_t C, int64_t V, size_t* bytes) {
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
+  *bytes = ws_layout(N).total;
+  return GRPO_OK;
+}
+
+grpo_status grpo_loss_fwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t* input_ids, const int32_t* len,
+                          const float* adv, const float* old_logp, const float* ref_logp,
+                          float eps, float beta, float norm, float* logp, float* lse, float* w,
+                          float* loss, void* workspace, size_t workspace_bytes,
+                          grpo_stream_t stream) {
+  grpo_status s = check_shapes(dtype, N, P, C, V);
+  if (s != GRPO_OK) return s;
+  if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) || isinf(norm))
+    return GRPO_ERR_INVALID_ARG;
+  if (loss == nullptr || workspace == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && (len == nullptr || adv == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 &&
+      (logits == nullptr || input_ids == nullptr || logp == nullptr || lse == nullptr ||
+       w == nullptr))
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && ref_logp == nullptr && N > 0 && C > 0) return GRPO_ERR_INVALID_ARG;
+  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
+  if (!aligned(logits, esize) || !aligned(input_ids, 8) || !aligned(len, 4) ||
+      !aligned(adv, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(logp, 4) ||
+      !aligned(lse, 4) || !aligned(w, 4) || !aligned(loss, 4) || !aligned(workspace, 256))
+    return GRPO_ERR_MISALIGNED;
+  if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
+
+  FwdArgs a;
+  a.logits = logits;
+  a.dtype = dtype == GRPO_F32 ? 0 : 1;
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.ids = input_ids;
+  a.len = len;
+  a.adv = adv;
+  a.old_logp = old_logp;
+  a.ref_logp = beta != 0.f ? ref_logp : nullptr;
+  a.eps = eps;
+  a.beta = beta;
+  a.norm = norm;
+  a.logp = logp;
+  a.lse = lse;
+  a.w = w;
+  a.loss = loss;
+  a.ws = workspace;
+  const cudaStream_t st = (cudaStream_t)stream;
+  DeviceInfo d;
+  cudaError_t e = current_device(&d);
+  if (e != cudaSuccess) return GRPO_ERR_CUDA;
+  // the prep kernel also resets the error flags and the reduction ticket
+  if ((e = launch_prep(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (N == 0 || C == 0) return from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  if ((e = launch_lse_gather(a, d, st)) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_surrogate(a, st));
+}
+
+grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t* input_ids, const int32_t* len,
+                          const float* lse, const float* w, const float* grad_loss,
+                          void* dlogits, grpo_stream_t stream) {
+  grpo_status s = check_shapes(dtype, N, P, C, V);
+  if (s != GRPO_OK) return s;
+  if (N == 0) return GRPO_OK;
+  if (dlogits == nullptr || len == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (C > 0 && (logits == nullptr || input_ids == nullptr || lse == nullptr || w == nullptr))
+    return GRPO_ERR_INVALID_ARG;
+  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
+  if (!aligned(logits, esize) || !aligned(dlogits, esize) || !aligned(input_ids, 8) ||
+      !aligned(len, 4) || !aligned(lse, 4) || !aligned(w, 4) || !aligned(grad_loss, 4))
+    return GRPO_ERR_MISALIGNED;
+  const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
+  const char* lo = static_cast<const char*>(logits);
+  const char* dl = static_cast<const char*>(dlogits);
+  if (logits != nullptr && dl < lo + bytes && lo < dl + bytes) return GRPO_ERR_INVALID_ARG;
+
+  BwdArgs a;
+  a.logits = logits;
+  a.dtype = dtype == GRPO_F32 ? 0 : 1;
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.ids = input_ids;
+  a.len = len;
+  a.lse = lse;
+  a.w = w;
+  a.grad = grad_loss;
+  a.dlogits = dlogits;
+  DeviceInfo d;
+  if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_dlogits(a, d, (cudaStream_t)stream));
+}
+
+grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
+  if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
+  uint32_t flags = 0;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (flags & kFlagTokenRange) return GRPO_ERR_TOKEN_RANGE;
+  if (flags & kFlagLengthRange) return GRPO_ERR_LENGTH_RANGE;
+  if (flags & kFlagTimeout) return GRPO_ERR_TIMEOUT;
+  return GRPO_OK;
+}
+
+grpo_status grpo_copy(void* dst, const void* src, size_t bytes, grpo_stream_t stream) {
+  if (bytes == 0) return GRPO_OK;
+  if (dst == nullptr || src == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(dst, 16) || !aligned(src, 16) || bytes % 16 != 0) return GRPO_ERR_MISALIGNED;
+  const char* d8 = static_cast<const char*>(dst);
+  const char* s8 = static_cast<const char*>(src);
+  if (d8 < s8 + bytes && s8 < d8 + bytes) return GRPO_ERR_INVALID_ARG;
+  DeviceInfo d;
+  if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_copy(dst, src, bytes, d, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,263 @@
+// Internal header of the GB300 (sm_103a) Dr. GRPO loss library: device
+// helpers written as inline PTX, the workspace layout, and the launchers that
+// api.cu calls.  Not part of the public ABI (include/grpo.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace grpo {
+
+constexpr int kThreads = 256;  // threads per CTA of the streaming kernels
+constexpr int kWarps = kThreads / 32;
+
+// log2(e): exp(x) = 2^(x * log2(e)); the streaming kernels work in base 2 so
+// that one FFMA feeds one ex2.approx.
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Flag bits the kernels set in the workspace header (read by grpo_check_error).
+constexpr uint32_t kFlagTokenRange = 1u;
+constexpr uint32_t kFlagLengthRange = 2u;
+constexpr uint32_t kFlagTimeout = 4u;
+
+// Workspace: a 256-byte header, then the exclusive prefix sums of the
+// clamped lengths (offsets[i] = sum of len[0..i), offsets[N] = number of
+// valid tokens), the clamped lengths, and the per-block partial sums of the
+// loss reduction.
+struct WsHeader {
+  uint32_t flags;   // kFlag* bits of the most recent forward call
+  uint32_t ticket;  // arrival counter of the loss reduction's last-block step
+  uint32_t pad[2];
+};
+constexpr int kMaxLossBlocks = 1024;
+
+struct WsLayout {
+  size_t offsets;   // int32[N + 1]
+  size_t lens;      // int32[N]
+  size_t partials;  // double[kMaxLossBlocks]
+  size_t total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int64_t N) {
+  WsLayout l;
+  l.offsets = 256;
+  l.lens = align_up(l.offsets + sizeof(int32_t) * (size_t)(N + 1), 256);
+  l.partials = align_up(l.lens + sizeof(int32_t) * (size_t)N, 256);
+  l.total = align_up(l.partials + sizeof(double) * kMaxLossBlocks, 256);
+  return l;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+// 2^x on the SFU (MUFU.EX2); flushes subnormal results to zero.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte load through the read-only path, not allocated in L1: every logits
+// byte is read once per kernel.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// 16-byte streaming store (evict-first): dlogits is written once, not re-read.
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// bfloat16 -> float: the 16 stored bits are the high half of a binary32.
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
+  return __uint_as_float((uint32_t)u << 16);
+}
+
+// Two floats -> packed bfloat16x2 (round to nearest even), `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster; release/acquire orders the
+// shared::cluster stores before it with the loads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Merge of two partial (max m, sum of exp(x - m)) pairs; the sums are kept
+// relative to their own maximum, so merging rescales the smaller side.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) {  // both empty (or all -inf logits)
+    m = M;
+    s = 0.f;
+    return;
+  }
+  s = s * ex2((m - M) * kLog2e) + s2 * ex2((m2 - M) * kLog2e);
+  m = M;
+}
+
+// ---------------------------------------------------------------------------
+// element types: 16-byte vectors of float32 (4) or bfloat16 bit patterns (8)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct Elt;
+
+template <>
+struct Elt<float> {
+  static constexpr int kPerVec = 4;
+  static constexpr int kUnroll = 8;  // vectors in flight per thread
+  static constexpr uint32_t kNegInf = 0xff800000u;
+  __device__ static void unpack(const uint4& d, float* x) {
+    x[0] = __uint_as_float(d.x);
+    x[1] = __uint_as_float(d.y);
+    x[2] = __uint_as_float(d.z);
+    x[3] = __uint_as_float(d.w);
+  }
+  __device__ static float extract(const uint4& d, int e) {
+    const uint32_t w = e == 0 ? d.x : (e == 1 ? d.y : (e == 2 ? d.z : d.w));
+    return __uint_as_float(w);
+  }
+  __device__ static float load1(const float* p) { return __ldg(p); }
+  __device__ static uint4 pack(const float* o) {
+    return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                      __float_as_uint(o[3]));
+  }
+  __device__ static void store1(float* p, float v) { *p = v; }
+};
+
+template <>
+struct Elt<uint16_t> {  // bfloat16 bit patterns
+  static constexpr int kPerVec = 8;
+  static constexpr int kUnroll = 4;
+  static constexpr uint32_t kNegInf = 0xff80ff80u;
+  __device__ static void unpack(const uint4& d, float* x) {
+    x[0] = bf16_lo(d.x);
+    x[1] = bf16_hi(d.x);
+    x[2] = bf16_lo(d.y);
+    x[3] = bf16_hi(d.y);
+    x[4] = bf16_lo(d.z);
+    x[5] = bf16_hi(d.z);
+    x[6] = bf16_lo(d.w);
+    x[7] = bf16_hi(d.w);
+  }
+  __device__ static float extract(const uint4& d, int e) {
+    const int k = e >> 1;
+    const uint32_t w = k == 0 ? d.x : (k == 1 ? d.y : (k == 2 ? d.z : d.w));
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+  __device__ static float load1(const uint16_t* p) { return bf16_bits_to_float(__ldg(p)); }
+  __device__ static uint4 pack(const float* o) {
+    return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                      pack_bf16x2(o[6], o[7]));
+  }
+  __device__ static void store1(uint16_t* p, float v) {
+    *p = (uint16_t)(pack_bf16x2(v, 0.f) & 0xffffu);
+  }
+};
+
+// Number of CTAs a row of `row_bytes` is split over: the largest power of two
+// <= 8 that keeps at least 32 KiB of the row per CTA.  `env` names an
+// environment variable that may force 1, 2, 4 or 8.
+int row_split(int64_t row_bytes, const char* env);
+
+// ---------------------------------------------------------------------------
+// launchers (defined in the kernel files, called by api.cu)
+// ---------------------------------------------------------------------------
+
+struct DeviceInfo {
+  int device;
+  int sms;
+};
+
+cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int64_t eos,
+                        uint8_t* mask, int32_t* len, cudaStream_t st);
+cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, float* adv, cudaStream_t st);
+
+struct FwdArgs {
+  const void* logits;
+  int dtype;  // 0 f32, 1 bf16
+  int64_t N, P, C, V;
+  const int64_t* ids;
+  const int32_t* len;
+  const float* adv;
+  const float* old_logp;
+  const float* ref_logp;
+  float eps, beta, norm;
+  float* logp;
+  float* lse;
+  float* w;
+  float* loss;
+  void* ws;
+};
+cudaError_t launch_prep(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st);
+cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st);
+
+struct BwdArgs {
+  const void* logits;
+  int dtype;
+  int64_t N, P, C, V;
+  const int64_t* ids;
+  const int32_t* len;
+  const float* lse;
+  const float* w;
+  const float* grad;
+  void* dlogits;
+};
+cudaError_t launch_dlogits(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st);
+
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceInfo& d,
+                        cudaStream_t st);
+
+}  // namespace grpo
