@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Benchmark of the Dr. GRPO loss hot path (forward + backward) on GB300.
+
+One step = grpo_mask -> grpo_advantage -> grpo_loss_fwd -> grpo_loss_bwd on
+one stream, over one batch of synthetic inputs already resident in HBM.  The
+default workload is the Qwen2.5-0.5B-shaped single group (B=1, G=8, P=128,
+C=256, V=151936, bf16 logits ~N(0, 3^2)); the logits (0.93 GB) are larger
+than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0):
+  value        completion tokens/s (valid tokens / device step time), all ranks
+  roofline     the dominant kernel (dlogits_kernel, one launch per step):
+               algorithmic bytes / its CUDA-event duration vs measured HBM peak
+  e2e          the same metric through the public API with host buffers:
+               pinned host -> device copies of the step's inputs and a
+               device -> host read of the loss inside the timed region
+  cpu_baseline the float64 CPU oracle, timed on a bounded sample
+``--impl reference`` times the oracle alone (host cores) as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from vocab_wide_logprob_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "completion tokens/s and logits GB/s (% of HBM roofline), Dr.GRPO loss fwd+bwd"
+UNIT = "completion tokens/s"
+KERNELS_PER_STEP = 6  # mask, advantage, prep, lse_gather, surrogate, dlogits
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=wl.QWEN_G8.name, choices=sorted(wl.BY_NAME))
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# byte counts (stated in the design doc)
+# --------------------------------------------------------------------------
+
+def algorithmic_bytes(w: wl.Workload, t_valid: int) -> dict:
+    e = w.elem_bytes
+    N, T, C, V = w.N, w.T, w.C, w.V
+    small = 4 * N * C * (3 + (w.old_sigma is not None) + (w.ref_sigma is not None))
+    return {
+        # the scored rows read once + ids of scored tokens + logp/lse/w vectors
+        "fwd": t_valid * V * e + 8 * t_valid + small,
+        # the scored rows read again + every row of dlogits written once
+        "bwd": t_valid * V * e + N * T * V * e + 16 * t_valid,
+        "mask_adv": 8 * N * C + N * C + 8 * N,
+        # the roofline count of the whole method: two reads + one write
+        "step_logits": 2 * t_valid * V * e + N * T * V * e,
+    }
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def csrc_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "vocab_wide_logprob_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, w: wl.Workload, units: float):
+    """DRAM bytes per launch from a committed ncu capture of the same kernel
+    source (profiles/traffic.json), scaled to `units`; None when absent or
+    when the kernel source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("csrc_sha") != csrc_sha():
+        return None
+    return rec["dram_bytes_per_unit"] * units
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    sm.append(float(parts[2]))
+                    smax.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[6:10]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# oracle on a bounded sample (CPU baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+class OracleSample:
+    """The float64 oracle's whole pipeline over rows of the workload: mask and
+    advantages of the batch, then for a run of rows of the [N, P+C] row space
+    (in order, cycling): log-probs, per-token loss terms and dlogits of the
+    scored rows, zeros for the rest.  Logits rows come from a seeded CPU pool
+    with the workload's distribution."""
+
+    def __init__(self, w: wl.Workload, pool_rows: int = 64):
+        import torch
+        import oracle
+        self.o = oracle.default()
+        self.w = w
+        self.ids = wl.make_ids(w)
+        self.R = wl.make_rewards(w)
+        _, self.lens = self.o.mask(self.ids, w.P, w.C, w.eos_id)
+        gen = torch.Generator().manual_seed(w.seed + 17)
+        x = torch.randn((pool_rows, w.V), generator=gen) * w.logit_std
+        x = x.to(torch.bfloat16 if w.dtype == "bf16" else torch.float32)
+        self.pool, self.dt = wl.logits_as_numpy(x)
+        self.noise_old, self.noise_ref = wl.make_noise(w)
+        self.cursor = 0
+        self.out = np.zeros(w.V)
+
+    def step(self, nrows: int) -> int:
+        """Processes the next nrows rows; returns the valid tokens among them."""
+        o, w = self.o, self.w
+        _, lens = o.mask(self.ids, w.P, w.C, w.eos_id)
+        A = o.advantage(self.R, w.G)
+        total = w.N * w.T
+        rows = [(self.cursor + k) % total for k in range(nrows)]
+        self.cursor = (self.cursor + nrows) % total
+        scored = []
+        for r in rows:
+            i, pos = divmod(r, w.T)
+            t = pos - (w.P - 1)
+            if 0 <= t < lens[i]:
+                scored.append((i, t, r))
+            else:
+                self.out[:] = 0.0
+        if not scored:
+            return 0
+        z = self.pool[[r % len(self.pool) for _, _, r in scored]]
+        y = np.array([self.ids[i, w.P + t] for i, t, _ in scored])
+        lp, lse = o.logp_rows(z, self.dt, y)
+        n = len(scored)
+        old = None if self.noise_old is None else (
+            lp + np.array([self.noise_old[i, t] for i, t, _ in scored]))[:, None]
+        ref = None if self.noise_ref is None else (
+            lp + np.array([self.noise_ref[i, t] for i, t, _ in scored]))[:, None]
+        Ai = np.array([A[i] for i, _, _ in scored])
+        _, wt, _ = o.loss(lp[:, None], old, ref, Ai, np.ones(n, np.int32), w.eps, w.beta,
+                          float(w.N * w.C))
+        for k in range(n):
+            self.out = o.dlogits_row(z[k], self.dt, int(y[k]), float(lse[k]), float(wt[k, 0]))
+        return n
+
+
+def time_oracle(w: wl.Workload, seconds: float, rows_per_call: int = 32):
+    """Runs the oracle on successive row runs until `seconds` have passed."""
+    s = OracleSample(w)
+    s.step(4)  # load and warm the library
+    tokens, rows, t0 = 0, 0, time.perf_counter()
+    while True:
+        tokens += s.step(rows_per_call)
+        rows += rows_per_call
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    import oracle
+    return {"value": tokens / el, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{rows} rows of the [N, P+C] row space of {w.name} in order "
+                      f"({tokens} scored tokens, {el:.1f} s): mask, advantage, log-probs, "
+                      "loss terms and dlogits in float64"}
+
+
+# --------------------------------------------------------------------------
+# the reference arm: the oracle alone
+# --------------------------------------------------------------------------
+
+def run_reference(args, w: wl.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    s = OracleSample(w)
+    # calibrate rows per step so the whole run takes about 90 s: one whole
+    # sequence (its prompt rows and its scored rows) gives the mean row cost
+    t0 = time.perf_counter()
+    s.step(w.T)
+    per_row = (time.perf_counter() - t0) / w.T
+    total_steps = args.steps + args.warmup
+    rows = max(1, int(90.0 / max(total_steps, 1) / max(per_row, 1e-6)))
+    for _ in range(args.warmup):
+        s.step(rows)
+    tokens = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tokens += s.step(rows)
+    el = time.perf_counter() - t0
+    value = tokens / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
+                   "logits_dtype": w.dtype, "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} rows of the [N, P+C] row space per step, cycling"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, w0: wl.Workload):
+    import torch
+    import torch.distributed as dist
+    from vocab_wide_logprob_gb300 import build as libbuild
+    libbuild.build()
+    from vocab_wide_logprob_gb300 import _native as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # weak scaling: each rank holds its own prompt groups (different seeds)
+    w = wl.variant(w0, seed=w0.seed + 1000 * rank)
+
+    ids_np = wl.make_ids(w)
+    R_np = wl.make_rewards(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    logits = torch.empty((w.N, w.T, w.V), dtype=tdt, device=dev)
+    wl.fill_logits_cuda(w, logits)
+    ids = torch.from_numpy(ids_np).to(dev)
+    R = torch.from_numpy(R_np).to(dev)
+    # old/ref log-probs: the current ones (computed by the library) + noise
+    mask, lens = g.grpo_mask(ids, w.P, w.C, w.eos_id)
+    adv = g.grpo_advantage(R, w.G)
+    cur = g.grpo_loss_fwd(logits, w.P, ids, lens, adv)
+    n_old, n_ref = wl.make_noise(w)
+    old = None if n_old is None else (cur["logp"] + torch.from_numpy(n_old).float().to(dev))
+    ref = None if n_ref is None else (cur["logp"] + torch.from_numpy(n_ref).float().to(dev))
+    t_valid = int(lens.sum().item())
+    dlogits = torch.empty_like(logits)
+    out = None
+    ws = cur["workspace"]
+    stream = torch.cuda.current_stream()
+
+    def step(record=None):
+        nonlocal out
+        if record is not None:
+            record[0].record(stream)
+        m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
+        a = g.grpo_advantage(R, w.G, adv)
+        if record is not None:
+            record[1].record(stream)
+        out = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, out, ws)
+        if record is not None:
+            record[2].record(stream)
+        g.grpo_loss_bwd(logits, w.P, ids, ln, out["lse"], out["w"], None, dlogits)
+        if record is not None:
+            record[3].record(stream)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    sampler = None if args.no_clocks else ClockSampler(gpu_id)
+    if sampler is not None:
+        time.sleep(1.0)  # nvidia-smi needs a moment before its first sample
+    for _ in range(max(args.warmup, 3)):
+        step()
+    assert g.grpo_check_error(ws) == 0
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        step(events[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    elapsed = start.elapsed_time(end) / 1e3
+    t_mask = statistics.mean(e[0].elapsed_time(e[1]) for e in events) / 1e3
+    t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in events) / 1e3
+    t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in events) / 1e3
+    loss_val = float(out["loss"].item())
+
+    # end to end through the public API: host inputs in, loss out
+    h_logits = logits.cpu().pin_memory()
+    h_ids = ids.cpu().pin_memory()
+    h_R = R.cpu().pin_memory()
+    h_old = None if old is None else old.cpu().pin_memory()
+    h_ref = None if ref is None else ref.cpu().pin_memory()
+    h_loss = torch.empty((1,), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_ids, h_R, h_old, h_ref)
+              if t is not None)
+
+    def e2e_step():
+        logits.copy_(h_logits, non_blocking=True)
+        ids.copy_(h_ids, non_blocking=True)
+        R.copy_(h_R, non_blocking=True)
+        if old is not None:
+            old.copy_(h_old, non_blocking=True)
+        if ref is not None:
+            ref.copy_(h_ref, non_blocking=True)
+        step()
+        h_loss.copy_(out["loss"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_el = e0.elapsed_time(e1) / 1e3
+
+    # aggregate over ranks: units of all ranks / max time
+    if world > 1:
+        t = torch.tensor([elapsed, e2e_el], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed, e2e_el = float(t[0]), float(t[1])
+        tv = torch.tensor([t_valid], device=dev, dtype=torch.int64)
+        dist.all_reduce(tv)
+        t_valid_all = int(tv.item())
+    else:
+        t_valid_all = t_valid
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, args.cpu_seconds)
+
+    if rank == 0:
+        peaks = measured_peaks()
+        peak = peaks.get("hbm_gbs")
+        peak_src = "measured" if peak else "fallback"
+        peak = peak or FALLBACK_HBM_GBS
+        b = algorithmic_bytes(w, t_valid)
+        ms = elapsed / args.steps
+        achieved = b["bwd"] / t_bwd / 1e9
+        traffic = recorded_traffic("dlogits_kernel", w, 1.0)
+        line = {
+            "metric": METRIC, "value": t_valid_all / ms, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
+                       "logits_dtype": w.dtype, "valid_tokens_per_rank": t_valid,
+                       "l2": f"inputs larger than L2 ({w.logits_bytes / 1e9:.2f} GB logits); "
+                             "no flush", "parallelism": f"dp{world} (independent groups)"},
+            "logits_gbs": b["step_logits"] / ms / 1e9,
+            "logits_roofline_frac": b["step_logits"] / ms / 1e9 / peak,
+            "kernel_ms": {"mask+advantage": t_mask * 1e3, "fwd": t_fwd * 1e3,
+                          "bwd": t_bwd * 1e3},
+            "fwd_gbs": b["fwd"] / t_fwd / 1e9,
+            "roofline": {"kernel": "dlogits_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes": b["bwd"]},
+            "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "loss": loss_val,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
