@@ -141,6 +141,38 @@ grpo_status grpo_loss_fwd(const void *logits, grpo_dtype dtype, int64_t N, int64
                           grpo_stream_t stream);
 
 /*
+ * grpo_loss_fwd_static -- grpo_loss_fwd without a workspace argument, for
+ * callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a convenience of this library.
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- inside a
+ * caching allocator or memory pool that must not be re-entered, in a plugin
+ * host that only lends out the buffers it owns, or in a runtime that forbids
+ * allocation once it has started.  Such callers still pass all inputs and
+ * outputs exactly as for grpo_loss_fwd (same arguments, same results).
+ *
+ * Scratch: a 64 KiB array compiled into the library as a __device__ variable;
+ * every GPU that loads the library holds it until the process exits.  It
+ * covers N <= 4096 completions; a larger N returns GRPO_ERR_UNSUPPORTED and
+ * enqueues nothing.  Nothing is allocated and no allocating routine is called.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ * All calls share the one array and it keeps the last call's contents; each
+ * call resets what must start at zero before using it.  Calls whose work can
+ * overlap on the GPU (different streams, or different host threads) race on
+ * the array and must be serialised by the caller.  Data-dependent errors are
+ * recorded in this shared array, so grpo_check_error cannot report them: a
+ * scored token id outside [0, V) still shows as a NaN log-prob.
+ */
+grpo_status grpo_loss_fwd_static(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, const int64_t *input_ids,
+                                 const int32_t *len, const float *adv, const float *old_logp,
+                                 const float *ref_logp, float eps, float beta, float norm,
+                                 float *logp, float *lse, float *w, float *loss,
+                                 grpo_stream_t stream);
+
+/*
  * grpo_loss_bwd -- gradient of (grad_loss * loss) with respect to the logits.
  *
  * Inputs as for grpo_loss_fwd, plus lse and w from it; grad_loss is one

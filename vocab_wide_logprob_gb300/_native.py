@@ -50,6 +50,8 @@ def _load():
         "grpo_loss_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, P], INT),
         "grpo_check_error": ([P, P], INT),
         "grpo_copy": ([P, P, SZ, P], INT),
+        "grpo_loss_fwd_static": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
+                                  P], INT),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -163,6 +165,34 @@ def grpo_loss_fwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
         _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(out["logp"]),
         _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _ptr(workspace), workspace.numel(),
         _stream(stream)), "grpo_loss_fwd")
+    return out
+
+
+def grpo_loss_fwd_static(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
+                         eps=0.2, beta=0.0, norm=0.0, out=None, stream=None):
+    """grpo_loss_fwd using the library's built-in scratch instead of a
+    caller-provided workspace (for callers that cannot allocate device
+    memory).  Returns ``logp``, ``lse``, ``w`` and ``loss`` like
+    :func:`grpo_loss_fwd`; ``out`` must be passed preallocated by a caller
+    that cannot allocate."""
+    _dev(logits, "logits")
+    N, T, V = logits.shape
+    C = T - P
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("adv", adv, torch.float32), ("old_logp", old_logp, torch.float32),
+                        ("ref_logp", ref_logp, torch.float32)):
+        _dev(t, name, dt)
+    dev = logits.device
+    if out is None:
+        out = {"logp": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "lse": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "w": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "loss": torch.empty((1,), dtype=torch.float32, device=dev)}
+    _check(_lib.grpo_loss_fwd_static(
+        _ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
+        _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(out["logp"]),
+        _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _stream(stream)),
+        "grpo_loss_fwd_static")
     return out
 
 
