@@ -93,18 +93,18 @@ def csrc_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, w: wl.Workload, units: float):
-    """DRAM bytes per launch from a committed ncu capture of the same kernel
-    source (profiles/traffic.json), scaled to `units`; None when absent or
-    when the kernel source changed since the capture."""
+def recorded_traffic(kernel: str, w: wl.Workload):
+    """DRAM bytes (read + write) per launch of `kernel` on workload `w` from a
+    committed ncu capture (profiles/traffic.json); None when there is none for
+    this workload or when the kernel sources changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(kernel)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("csrc_sha") != csrc_sha():
+    if not rec or rec.get("csrc_sha") != csrc_sha() or rec.get("workload") != w.name:
         return None
-    return rec["dram_bytes_per_unit"] * units
+    return rec["dram_bytes_per_launch"]
 
 
 # --------------------------------------------------------------------------
@@ -425,7 +425,7 @@ def run_ours(args, w0: wl.Workload):
         b = algorithmic_bytes(w, t_valid)
         ms = elapsed / args.steps
         achieved = b["bwd"] / t_bwd / 1e9
-        traffic = recorded_traffic("dlogits_kernel", w, 1.0)
+        traffic = recorded_traffic("dlogits_kernel", w)
         line = {
             "metric": METRIC, "value": t_valid_all / ms, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms * 1e3,
