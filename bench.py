@@ -54,6 +54,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-copy-ceiling", action="store_true")
     return p.parse_args()
 
 
@@ -105,6 +106,29 @@ def recorded_traffic(kernel: str, w: wl.Workload):
     if not rec or rec.get("csrc_sha") != csrc_sha() or rec.get("workload") != w.name:
         return None
     return rec["dram_bytes_per_launch"]
+
+
+def copy_ceiling(g, dev, nbytes: int = 4 << 30, reps: int = 10) -> float:
+    """Device-to-device copy with the library's 16-byte vector copy kernel
+    over two 4 GiB buffers: (read + write bytes) / best time, GB/s."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    for _ in range(2):
+        g.grpo_copy(dst, src)
+    best = float("inf")
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.grpo_copy(dst, src)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) / 1e3)
+    del src, dst
+    torch.cuda.empty_cache()
+    return 2 * nbytes / best / 1e9
 
 
 # --------------------------------------------------------------------------
@@ -413,6 +437,8 @@ def run_ours(args, w0: wl.Workload):
     else:
         t_valid_all = t_valid
 
+    copy_gbs = None if args.no_copy_ceiling else copy_ceiling(g, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds)
@@ -446,6 +472,7 @@ def run_ours(args, w0: wl.Workload):
                          "algorithmic_bytes": b["bwd"]},
             "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+            "copy_ceiling_gbs": copy_gbs,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "cpu_baseline": cpu,
             "clocks": clocks,

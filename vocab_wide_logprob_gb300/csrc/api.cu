@@ -9,7 +9,7 @@
 
 namespace grpo {
 
-int row_split(int64_t row_bytes, const char* env) {
+int row_split(int64_t row_bytes, const char* env, int max_split) {
   if (env != nullptr) {
     if (const char* s = getenv(env)) {
       const int k = atoi(s);
@@ -17,7 +17,7 @@ int row_split(int64_t row_bytes, const char* env) {
     }
   }
   int k = 1;
-  while (k < 8 && row_bytes / (2 * k) >= 32768) k *= 2;
+  while (k < max_split && row_bytes / (2 * k) >= 32768) k *= 2;
   return k;
 }
 

@@ -91,6 +91,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
+  __nv_bfloat162 h;
+  memcpy(&h, &u, sizeof h);
+  return h;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -133,6 +139,81 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named barrier 1 over the first `n` threads of the CTA (a subset of warps).
+__device__ __forceinline__ void bar_sync_named(int n) {
+  asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier and bulk-copy (TMA) helpers ----------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+// Makes barrier initialisation visible to the async proxy and the cluster.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Upper bound of any wait on an mbarrier: one second.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Waits for phase `parity` of the barrier to complete; false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+// One-dimensional bulk copy global -> this CTA's shared memory, completing
+// `bytes` of transaction count on the mbarrier.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t smem_dst, const void* gsrc, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_dst),
+      "l"(gsrc), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // Merge of two partial (max m, sum of exp(x - m)) pairs; the sums are kept
 // relative to their own maximum, so merging rescales the smaller side.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
@@ -169,6 +250,18 @@ struct Elt<float> {
     return __uint_as_float(w);
   }
   __device__ static float load1(const float* p) { return __ldg(p); }
+  template <int U>
+  __device__ static float batch_max(const uint4* d) {
+    float m = __uint_as_float(d[0].x);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m = fmaxf(m, __uint_as_float(d[u].x));
+      m = fmaxf(m, __uint_as_float(d[u].y));
+      m = fmaxf(m, __uint_as_float(d[u].z));
+      m = fmaxf(m, __uint_as_float(d[u].w));
+    }
+    return m;
+  }
   __device__ static uint4 pack(const float* o) {
     return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
                       __float_as_uint(o[3]));
@@ -197,6 +290,20 @@ struct Elt<uint16_t> {  // bfloat16 bit patterns
     return (e & 1) ? bf16_hi(w) : bf16_lo(w);
   }
   __device__ static float load1(const uint16_t* p) { return bf16_bits_to_float(__ldg(p)); }
+  // Maximum of U vectors with packed bfloat16x2 max (exact; ignores NaN like
+  // fmaxf), then one widening of the last pair.
+  template <int U>
+  __device__ static float batch_max(const uint4* d) {
+    __nv_bfloat162 m = as_bf162(d[0].x);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m = __hmax2(m, as_bf162(d[u].x));
+      m = __hmax2(m, as_bf162(d[u].y));
+      m = __hmax2(m, as_bf162(d[u].z));
+      m = __hmax2(m, as_bf162(d[u].w));
+    }
+    return fmaxf(__low2float(m), __high2float(m));
+  }
   __device__ static uint4 pack(const float* o) {
     return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                       pack_bf16x2(o[6], o[7]));
@@ -207,9 +314,9 @@ struct Elt<uint16_t> {  // bfloat16 bit patterns
 };
 
 // Number of CTAs a row of `row_bytes` is split over: the largest power of two
-// <= 8 that keeps at least 32 KiB of the row per CTA.  `env` names an
+// <= max_split that keeps at least 32 KiB of the row per CTA.  `env` names an
 // environment variable that may force 1, 2, 4 or 8.
-int row_split(int64_t row_bytes, const char* env);
+int row_split(int64_t row_bytes, const char* env, int max_split);
 
 // ---------------------------------------------------------------------------
 // launchers (defined in the kernel files, called by api.cu)

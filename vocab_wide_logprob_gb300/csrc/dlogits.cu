@@ -142,7 +142,7 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.lse = a.lse;
   p.w = a.w;
   p.grad = a.grad;
-  p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT");
+  p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT", 8);
   p.chunk = ((a.V + p.split - 1) / p.split + EPV - 1) / EPV * EPV;
   static int per_sm[2][64] = {};  // occupancy per (dtype, device); benign race
   int& occ = per_sm[sizeof(T) == 4 ? 0 : 1][d.device & 63];

@@ -105,6 +105,15 @@ struct LseParams {
   int64_t chunk;  // elements of a row per CTA of the cluster (multiple of kPerVec)
 };
 
+// Ring of shared-memory stages filled by bulk copies (TMA).
+constexpr int kStages = 3;
+constexpr int kStageBytes = 16384;
+constexpr int kConsumers = kThreads;          // 8 consumer warps
+constexpr int kLseThreads = kConsumers + 32;  // + 1 producer warp
+constexpr int kVecPerStage = kStageBytes / 16;
+constexpr int kVecPerThread = kVecPerStage / kConsumers;
+static_assert(kVecPerStage % kConsumers == 0, "stage must split evenly over consumers");
+
 // Online update of a thread's running (m, s0..s3) with one value.
 __device__ __forceinline__ void online1(float x, float& m, float& s0, float& s1, float& s2,
                                         float& s3) {
@@ -119,29 +128,125 @@ __device__ __forceinline__ void online1(float x, float& m, float& s0, float& s1,
   if (m != -INFINITY) s0 += ex2(fmaf(x, kLog2e, -m * kLog2e));
 }
 
+// Completion holding valid token r: the i with off[i] <= r < off[i+1].
+__device__ __forceinline__ int locate(const int32_t* off, int64_t N, int64_t r) {
+  int lo = 0, hi = (int)N;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= r)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Geometry of one CTA's share of one row: the slice [v0, v1) of the row,
+// its 16-byte aligned interior [a, a + 8*nvec/..) moved by bulk copies, and
+// the ragged head [v0, a) / tail [b, v1) read with scalar loads.
+template <typename T>
+struct Slice {
+  const T* row;
+  int64_t a, b, nvec;
+  uint32_t bytes;  // interior bytes (multiple of 16)
+  int nchunks;
+};
+
+template <typename T>
+__device__ __forceinline__ Slice<T> slice_of(const T* row, int64_t v0, int64_t v1) {
+  constexpr int EPV = Elt<T>::kPerVec;
+  Slice<T> sl;
+  sl.row = row;
+  if (v0 >= v1) {
+    sl.a = sl.b = v0;
+    sl.nvec = 0;
+  } else {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row + v0);
+    const int64_t skip = (int64_t)(((16u - (unsigned)(addr & 15u)) & 15u) / sizeof(T));
+    sl.a = min(v0 + skip, v1);
+    sl.nvec = (v1 - sl.a) / EPV;
+    sl.b = sl.a + sl.nvec * EPV;
+  }
+  sl.bytes = (uint32_t)(sl.nvec * 16);
+  sl.nchunks = (int)((sl.bytes + kStageBytes - 1) / kStageBytes);
+  return sl;
+}
+
+// CTA 0 of the cluster: merge the K partials of a row in rank order and
+// write logp and lse of token (i, t).
+template <int K, typename P>
+__device__ __forceinline__ void finalize_row(const P& p, const float4* part, int64_t i,
+                                             int64_t t) {
+  float4 pk = part[0];
+  float cm = pk.x, cs = pk.y, z = pk.z;
+  bool has = pk.w != 0.f;
+#pragma unroll
+  for (int k = 1; k < K; ++k) {
+    pk = part[k];
+    lse_merge(cm, cs, pk.x, pk.y);
+    if (pk.w != 0.f) {
+      z = pk.z;
+      has = true;
+    }
+  }
+  const float l = cm + logf(cs);
+  const int64_t o = i * p.C + t;
+  if (has) {
+    p.logp[o] = z - l;
+    p.lse[o] = l;
+  } else {  // y outside [0, V): no CTA saw it
+    p.logp[o] = __int_as_float(0x7fc00000);
+    p.lse[o] = __int_as_float(0x7fc00000);
+    atomicOr(&p.hdr->flags, kFlagTokenRange);
+  }
+}
+
+// Persistent cluster kernel.  Warps 0..7 consume, warp 8 produces: its lane 0
+// walks the same rows as the consumers and issues one bulk copy per stage of
+// each row's interior, running ahead across rows as far as the ring allows.
+// At the end of a row each CTA sends its (max, sum, target logit) partial to
+// CTA 0 through distributed shared memory and arrives on the cluster
+// barrier; the matching wait comes one row later, so no CTA stalls at the
+// barrier, and CTA 0 merges row r's partials then.  Partials rotate over
+// three slots: slot r%3 is rewritten for row r+3 only after every thread has
+// passed the wait of row r+1, which CTA 0 reaches after merging row r.
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads) lse_gather_kernel(const LseParams<T> p) {
+__global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LseParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
-  constexpr int U = E::kUnroll;
-  extern __shared__ int32_t s_off_dyn[];
-  __shared__ float4 s_part[2][K];     // CTA 0: partial (m, s, z_y, has z_y) of each rank
-  __shared__ float2 s_red[2][kWarps];  // per-warp (m, s)
-  __shared__ float s_zy[2];
-  __shared__ int64_t s_found[2];       // row whose target logit this CTA picked up
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t s_full[kStages];
+  __shared__ __align__(8) uint64_t s_empty[kStages];
+  __shared__ float4 s_part[3][K];     // CTA 0: partial (m, s, z_y, has z_y) of each rank
+  __shared__ float2 s_red[2][kWarps];  // per consumer warp (m, s)
+  __shared__ float s_zy[3];
+  __shared__ int64_t s_found[3];       // row whose target logit this CTA picked up
+  __shared__ int s_abort;              // a bounded wait gave up
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool producer = warp == kWarps;
   const uint32_t rank = K > 1 ? cluster_ctarank() : 0u;
   const int64_t q = K > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
   const int64_t nq = K > 1 ? (int64_t)nclusters_x() : (int64_t)gridDim.x;
+  const uint32_t ring = smem_u32(smem);
 
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
   const int32_t* off = p.offsets;
   if (p.N + 1 <= kSmemOffsets) {
-    for (int64_t k = tid; k <= p.N; k += kThreads) s_off_dyn[k] = p.offsets[k];
-    off = s_off_dyn;
+    for (int64_t k = tid; k <= p.N; k += kLseThreads) s_off[k] = p.offsets[k];
+    off = s_off;
   }
-  if (tid < 2) s_found[tid] = -1;
-  // every CTA of the cluster is running (and has initialised its shared
-  // memory) before any distributed-shared-memory store
+  if (tid < 3) s_found[tid] = -1;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(smem_u32(&s_full[k]), 1);
+      mbar_init(smem_u32(&s_empty[k]), kWarps);
+    }
+    mbar_init_fence();
+  }
+  // every CTA of the cluster is running and initialised before any
+  // distributed-shared-memory store or bulk copy
   if (K > 1)
     cluster_sync();
   else
@@ -150,79 +255,63 @@ __global__ void __launch_bounds__(kThreads) lse_gather_kernel(const LseParams<T>
   const int64_t tv = off[p.N];  // number of valid tokens
   const int64_t v0 = (int64_t)rank * p.chunk;
   const int64_t v1 = min(p.V, v0 + p.chunk);
-  int par = 0;
-  for (int64_t r = q; r < tv; r += nq, par ^= 1) {
-    // completion i holding valid token r: off[i] <= r < off[i+1]
-    int lo = 0, hi = (int)p.N;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (off[mid] <= r)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    const int64_t i = lo, t = r - off[lo];
-    const T* row = p.logits + (i * p.T_len + (p.P - 1 + t)) * p.V;
-    const int64_t y = p.ids[i * p.T_len + p.P + t];
+  int stage = 0;
+  uint32_t phase = 0;
+  int64_t prev_i = 0, prev_t = 0;
+  int64_t it = 0;
+  uint32_t issued = 0;  // producer: bulk copies issued
 
-    float m = -INFINITY, s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    float zy = 0.f;
-    bool found = false;
-    if (v0 < v1) {
-      // 16-byte aligned interior [a, b) of the slice [v0, v1)
-      const uintptr_t addr = reinterpret_cast<uintptr_t>(row + v0);
-      const int64_t skip = (int64_t)(((16u - (unsigned)(addr & 15u)) & 15u) / sizeof(T));
-      const int64_t a = min(v0 + skip, v1);
-      const int64_t nvec = (v1 - a) / EPV;
-      const int64_t b = a + nvec * EPV;
-      const uint4* vp = reinterpret_cast<const uint4*>(row + a);
-      const int64_t ky = (y >= a && y < b) ? (y - a) / EPV : -1;
-      const int ey = ky >= 0 ? (int)((y - a) % EPV) : 0;
-      for (int64_t k0 = tid; k0 < nvec; k0 += (int64_t)kThreads * U) {
-        uint4 d[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t k = k0 + (int64_t)u * kThreads;
-          d[u] = k < nvec ? ld_stream(vp + k)
-                          : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (k0 + (int64_t)u * kThreads == ky) {
-            zy = E::extract(d[u], ey);
-            found = true;
+  // the next row's (i, t, y) are fetched one row ahead, so the id load's
+  // latency hides behind the current row
+  int64_t i_nx = 0, t_nx = 0, y_nx = 0;
+  if (q < tv) {
+    i_nx = locate(off, p.N, q);
+    t_nx = q - off[i_nx];
+    if (!producer) y_nx = __ldg(p.ids + i_nx * p.T_len + p.P + t_nx);
+  }
+  for (int64_t r = q; r < tv; r += nq, ++it) {
+    const int slot = (int)(it % 3);
+    const int64_t i = i_nx, t = t_nx, y = y_nx;
+    if (r + nq < tv) {
+      i_nx = locate(off, p.N, r + nq);
+      t_nx = r + nq - off[i_nx];
+      if (!producer) y_nx = __ldg(p.ids + i_nx * p.T_len + p.P + t_nx);
+    }
+    const T* row = p.logits + (i * p.T_len + (p.P - 1 + t)) * p.V;
+    const Slice<T> sl = slice_of(row, v0, v1);
+
+    if (producer) {
+      if (lane == 0) {
+        const char* src = reinterpret_cast<const char*>(row + sl.a);
+        for (int c = 0; c < sl.nchunks; ++c) {
+          if (*(volatile int*)&s_abort) break;
+          if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u)) {
+            atomicOr(&p.hdr->flags, kFlagTimeout);
+            *(volatile int*)&s_abort = 1;
+            break;
           }
-        float x[U * EPV];
-#pragma unroll
-        for (int u = 0; u < U; ++u) E::unpack(d[u], x + u * EPV);
-        float bm = x[0];
-#pragma unroll
-        for (int k = 1; k < U * EPV; ++k) bm = fmaxf(bm, x[k]);
-        if (bm > m) {
-          const float sc = ex2((m - bm) * kLog2e);
-          s0 *= sc;
-          s1 *= sc;
-          s2 *= sc;
-          s3 *= sc;
-          m = bm;
-        }
-        if (m != -INFINITY) {
-          const float mL = m * kLog2e;
-#pragma unroll
-          for (int k = 0; k < U * EPV; k += 4) {
-            s0 += ex2(fmaf(x[k + 0], kLog2e, -mL));
-            s1 += ex2(fmaf(x[k + 1], kLog2e, -mL));
-            s2 += ex2(fmaf(x[k + 2], kLog2e, -mL));
-            s3 += ex2(fmaf(x[k + 3], kLog2e, -mL));
+          const uint32_t nb = min((uint32_t)kStageBytes, sl.bytes - (uint32_t)c * kStageBytes);
+          const uint32_t full = smem_u32(&s_full[stage]);
+          mbar_arrive_expect_tx(full, nb);
+          bulk_g2s(ring + stage * kStageBytes, src + (size_t)c * kStageBytes, nb, full);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
       }
-      // ragged head [v0, a) and tail [b, v1): fewer than EPV elements each
+      __syncwarp();
+    } else {
+      float m = -INFINITY, s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      float zy = 0.f;
+      bool found = false;
+      // ragged head and tail (fewer than EPV elements each)
       int64_t e = -1;
-      if (tid < a - v0)
+      if (tid < sl.a - v0)
         e = v0 + tid;
-      else if (tid >= 32 && tid - 32 < v1 - b)
-        e = b + (tid - 32);
+      else if (tid >= 32 && tid - 32 < v1 - sl.b)
+        e = sl.b + (tid - 32);
       if (e >= 0) {
         const float xv = E::load1(row + e);
         if (e == y) {
@@ -231,54 +320,115 @@ __global__ void __launch_bounds__(kThreads) lse_gather_kernel(const LseParams<T>
         }
         online1(xv, m, s0, s1, s2, s3);
       }
-    }
-    float s = (s0 + s1) + (s2 + s3);
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2b = __shfl_xor_sync(0xffffffffu, s, o);
-      lse_merge(m, s, m2, s2b);
-    }
-    if (lane == 0) s_red[par][warp] = make_float2(m, s);
-    if (found) {
-      s_zy[par] = zy;
-      s_found[par] = r;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float cm = s_red[par][0].x, cs = s_red[par][0].y;
+      // the target's vector: chunk cy, consumer thread ty, register slot uy
+      const int64_t ky = (y >= sl.a && y < sl.b) ? (y - sl.a) / EPV : -1;
+      const int ey = ky >= 0 ? (int)((y - sl.a) % EPV) : 0;
+      const int cy = ky >= 0 ? (int)(ky / kVecPerStage) : -1;
+      const int kl = ky >= 0 ? (int)(ky % kVecPerStage) : 0;
+      const int ty = kl % kConsumers, uy = kl / kConsumers;
+      for (int c = 0; c < sl.nchunks; ++c) {
+        bool ok = !*(volatile int*)&s_abort;
+        if (ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+          atomicOr(&p.hdr->flags, kFlagTimeout);
+          *(volatile int*)&s_abort = 1;
+          ok = false;
+        }
+        if (ok) {
+          const int64_t vbase = (int64_t)c * kVecPerStage;
+          (void)vbase;
+          const int nv = (int)min((int64_t)kVecPerStage, sl.nvec - vbase);
+          const uint32_t sbase = ring + stage * kStageBytes;
+          uint4 d[kVecPerThread];
 #pragma unroll
-      for (int k = 1; k < kWarps; ++k) lse_merge(cm, cs, s_red[par][k].x, s_red[par][k].y);
-      const bool has = s_found[par] == r;
-      const float4 part = make_float4(cm, cs, has ? s_zy[par] : 0.f, has ? 1.f : 0.f);
-      if (K > 1)
-        st_cluster_f32x4(map_to_rank(smem_u32(&s_part[par][rank]), 0), part);
-      else
-        s_part[par][0] = part;
-    }
-    if (K > 1) cluster_sync();
-    if (rank == 0 && tid == 0) {
-      float4 pk = s_part[par][0];
-      float cm = pk.x, cs = pk.y, z = pk.z;
-      bool has = pk.w != 0.f;
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            d[u] = k < nv ? ld_shared_v4(sbase + 16u * k)
+                          : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+          }
+          if (c == cy && tid == ty) {
 #pragma unroll
-      for (int k = 1; k < K; ++k) {
-        pk = s_part[par][k];
-        lse_merge(cm, cs, pk.x, pk.y);
-        if (pk.w != 0.f) {
-          z = pk.z;
-          has = true;
+            for (int u = 0; u < kVecPerThread; ++u)
+              if (u == uy) zy = E::extract(d[u], ey);
+            found = true;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));  // stage may be refilled
+          float x[kVecPerThread * EPV];
+#pragma unroll
+          for (int u = 0; u < kVecPerThread; ++u) E::unpack(d[u], x + u * EPV);
+          const float bm = E::template batch_max<kVecPerThread>(d);
+          if (bm > m) {
+            const float sc = ex2((m - bm) * kLog2e);
+            s0 *= sc;
+            s1 *= sc;
+            s2 *= sc;
+            s3 *= sc;
+            m = bm;
+          }
+          if (m != -INFINITY) {
+            const float mL = m * kLog2e;
+#pragma unroll
+            for (int k = 0; k < kVecPerThread * EPV; k += 4) {
+              s0 += ex2(fmaf(x[k + 0], kLog2e, -mL));
+              s1 += ex2(fmaf(x[k + 1], kLog2e, -mL));
+              s2 += ex2(fmaf(x[k + 2], kLog2e, -mL));
+              s3 += ex2(fmaf(x[k + 3], kLog2e, -mL));
+            }
+          }
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      const float l = cm + logf(cs);
-      const int64_t o = i * p.C + t;
-      if (has) {
-        p.logp[o] = z - l;
-        p.lse[o] = l;
-      } else {  // y outside [0, V): no CTA saw it
-        p.logp[o] = __int_as_float(0x7fc00000);
-        p.lse[o] = __int_as_float(0x7fc00000);
-        atomicOr(&p.hdr->flags, kFlagTokenRange);
+      float s = (s0 + s1) + (s2 + s3);
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2b = __shfl_xor_sync(0xffffffffu, s, o);
+        lse_merge(m, s, m2, s2b);
       }
+      const int rb = (int)(it & 1);
+      if (lane == 0) s_red[rb][warp] = make_float2(m, s);
+      if (found) {
+        s_zy[slot] = zy;
+        s_found[slot] = r;
+      }
+      bar_sync_named(kConsumers);
+      if (tid == 0) {
+        float cm = s_red[rb][0].x, cs = s_red[rb][0].y;
+#pragma unroll
+        for (int k = 1; k < kWarps; ++k) lse_merge(cm, cs, s_red[rb][k].x, s_red[rb][k].y);
+        const bool has = s_found[slot] == r;
+        const float4 part = make_float4(cm, cs, has ? s_zy[slot] : 0.f, has ? 1.f : 0.f);
+        if (K > 1)
+          st_cluster_f32x4(map_to_rank(smem_u32(&s_part[slot][rank]), 0), part);
+        else
+          s_part[slot][0] = part;
+      }
+    }
+    __syncwarp();  // the cluster barrier instructions are warp-aligned
+    if (K > 1) {
+      if (it > 0) {
+        cluster_wait();  // row it-1: every CTA's partial has landed in CTA 0
+        if (rank == 0 && tid == 0) finalize_row<K>(p, s_part[(it - 1) % 3], prev_i, prev_t);
+      }
+      cluster_arrive();
+    } else if (tid == 0) {
+      finalize_row<K>(p, s_part[slot], i, t);
+    }
+    prev_i = i;
+    prev_t = t;
+  }
+  __syncwarp();
+  if (K > 1 && it > 0) {
+    cluster_wait();
+    if (rank == 0 && tid == 0) finalize_row<K>(p, s_part[(it - 1) % 3], prev_i, prev_t);
+  }
+  // copies this CTA issued that no consumer waited for (only after a timeout)
+  if (producer && lane == 0 && *(volatile int*)&s_abort) {
+    for (uint32_t k = 0; k < kStages && k < issued; ++k) {
+      const uint32_t n = issued - 1 - k;  // copy number n used stage n % kStages
+      mbar_wait(smem_u32(&s_full[n % kStages]), (n / kStages) & 1u);
     }
   }
 }
@@ -311,15 +461,24 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.chunk = ((a.V + K - 1) / K + EPV - 1) / EPV * EPV;
 
-  const size_t smem = a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0;
+  const size_t smem = (size_t)kStages * kStageBytes +
+                      (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
   auto kern = lse_gather_kernel<T, K>;
+  static bool attr_set[2][4] = {};  // (dtype, log2 K); benign race: same value
+  bool& done = attr_set[sizeof(T) == 4 ? 0 : 1][K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
+  if (!done) {
+    const int max_smem = kStages * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+    done = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = K;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kLseThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -339,7 +498,7 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
       e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
     } else {
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLseThreads, smem);
       clusters = per_sm * d.sms;
     }
     if (e != cudaSuccess) return e;
@@ -355,7 +514,8 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
 
 template <typename T>
 cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_LSE_CLUSTER")) {
+  // clusters of more than 4 CTAs couple too many CTAs at every row's barrier
+  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_LSE_CLUSTER", 4)) {
     case 8:
       return launch_k<T, 8>(a, d, st);
     case 4:
