@@ -21,6 +21,14 @@ int row_split(int64_t row_bytes, const char* env, int max_split) {
   return k;
 }
 
+int grid_mult(const char* env, int def) {
+  if (const char* s = getenv(env)) {
+    const int k = atoi(s);
+    if (k > 0 && k <= 4096) return k;
+  }
+  return def;
+}
+
 namespace {
 
 int g_sms[64] = {};  // SM count per device ordinal; benign race (same value)

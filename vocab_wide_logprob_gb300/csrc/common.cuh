@@ -142,6 +142,16 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float4 v) {
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrive without ordering this thread's memory operations: threads that
+// stored nothing the other CTAs read skip the cluster-scope fence.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+// Release fence at cluster scope: orders this thread's earlier stores (to
+// another CTA's shared memory) before its later relaxed arrive.
+__device__ __forceinline__ void fence_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -155,6 +165,52 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation and calls pdl_wait() before its first global-memory access:
+// that waits for the previous kernel in the stream to complete and its
+// writes to be visible, so no ordering is lost, while the launch and the
+// shared-memory prologue overlap the previous kernel's tail.  pdl_trigger()
+// lets the next kernel start launching; it is issued once this kernel's
+// CTAs are all resident, so it cannot take their slots.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- packed float pairs (Blackwell f32x2 FMA/ADD/MUL: two lanes per
+// instruction, each rounded exactly as the scalar instruction) ------------
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// 2^x of both lanes on the SFU.
+__device__ __forceinline__ uint64_t f2_ex2(uint64_t a) {
+  float x, y;
+  f2_unpack(a, x, y);
+  return f2_pack(ex2(x), ex2(y));
 }
 
 // ---- mbarrier and bulk-copy (TMA) helpers ----------------------------------
@@ -173,14 +229,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint32_t addr) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
 }
+// Tests phase `parity` of the barrier; while it is incomplete the thread is
+// suspended in hardware (up to about 0.1 ms) instead of spinning, so waiting
+// warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(addr), "r"(parity)
+      : "r"(addr), "r"(parity), "r"(100000u)
       : "memory");
   return ok != 0;
 }
@@ -192,7 +251,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(addr, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 // One-dimensional bulk copy global -> this CTA's shared memory, completing
@@ -318,9 +377,34 @@ struct Elt<uint16_t> {  // bfloat16 bit patterns
 // environment variable that may force 1, 2, 4 or 8.
 int row_split(int64_t row_bytes, const char* env, int max_split);
 
+// CTAs per SM of an oversubscribed streaming grid: `def`, or the positive
+// integer in environment variable `env`.
+int grid_mult(const char* env, int def);
+
 // ---------------------------------------------------------------------------
 // launchers (defined in the kernel files, called by api.cu)
 // ---------------------------------------------------------------------------
+
+// Launch with programmatic stream serialisation (and an optional cluster).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = cluster_x;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 struct DeviceInfo {
   int device;

@@ -9,6 +9,8 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(uint4* __restrict__ dst,
                                                         const uint4* __restrict__ src,
                                                         int64_t nvec) {
   constexpr int U = 4;
+  pdl_wait();
+  pdl_trigger();
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t k0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; k0 < nvec; k0 += stride * U) {
     uint4 d[U];
@@ -25,20 +27,12 @@ cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceIn
                         cudaStream_t st) {
   const int64_t nvec = (int64_t)(bytes / 16);
   if (nvec == 0) return cudaSuccess;
-  static int per_sm[64] = {};
-  int& occ = per_sm[d.device & 63];
-  if (occ == 0) {
-    int o = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, copy_kernel, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    occ = o > 0 ? o : 1;
-  }
-  int64_t grid = (int64_t)occ * d.sms;
+  // oversubscribed grid-stride grid: faster than a persistent one for streams
+  int64_t grid = (int64_t)grid_mult("GRPO_COPY_GRID", 256) * d.sms;
   const int64_t need = (nvec + kThreads - 1) / kThreads;
   if (grid > need) grid = need;
-  copy_kernel<<<(unsigned)grid, kThreads, 0, st>>>(static_cast<uint4*>(dst),
-                                                  static_cast<const uint4*>(src), nvec);
-  return cudaGetLastError();
+  return launch_pdl(copy_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1,
+                    static_cast<uint4*>(dst), static_cast<const uint4*>(src), nvec);
 }
 
 }  // namespace grpo

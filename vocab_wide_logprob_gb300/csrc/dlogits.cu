@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
   constexpr int EPV = E::kPerVec;
   constexpr int U = E::kUnroll;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const float g = p.grad != nullptr ? __ldg(p.grad) : 1.f;
   const int64_t items = p.N * p.T_len * p.split;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -144,20 +146,13 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.grad = a.grad;
   p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT", 8);
   p.chunk = ((a.V + p.split - 1) / p.split + EPV - 1) / EPV * EPV;
-  static int per_sm[2][64] = {};  // occupancy per (dtype, device); benign race
-  int& occ = per_sm[sizeof(T) == 4 ? 0 : 1][d.device & 63];
-  if (occ == 0) {
-    int o = 0;
-    cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, dlogits_kernel<T>, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    occ = o > 0 ? o : 1;
-  }
+  // An oversubscribed grid (many more CTAs than fit at once, grid-stride over
+  // the items) streams stores faster than a persistent one: measured 7.3 vs
+  // 6.5 TB/s for a pure write stream on GB300.
   const int64_t items = a.N * (a.P + a.C) * p.split;
-  int64_t grid = (int64_t)occ * d.sms;
+  int64_t grid = (int64_t)grid_mult("GRPO_BWD_GRID", 256) * d.sms;
   if (grid > items) grid = items;
-  dlogits_kernel<T><<<(unsigned)grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(dlogits_kernel<T>, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, p);
 }
 
 }  // namespace

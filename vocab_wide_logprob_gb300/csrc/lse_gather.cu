@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
   __shared__ int32_t carry;
   __shared__ uint32_t flags;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     carry = 0;
     flags = 0;
@@ -87,10 +89,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
 cudaError_t launch_prep(const FwdArgs& a, cudaStream_t st) {
   const WsLayout l = ws_layout(a.N);
   char* ws = static_cast<char*>(a.ws);
-  prep_kernel<<<1, 1024, 0, st>>>(a.len, a.N, a.C, reinterpret_cast<WsHeader*>(ws),
-                                  reinterpret_cast<int32_t*>(ws + l.offsets),
-                                  reinterpret_cast<int32_t*>(ws + l.lens));
-  return cudaGetLastError();
+  return launch_pdl(prep_kernel, dim3(1), dim3(1024), 0, st, 1, a.len, a.N, a.C,
+                    reinterpret_cast<WsHeader*>(ws), reinterpret_cast<int32_t*>(ws + l.offsets),
+                    reinterpret_cast<int32_t*>(ws + l.lens));
 }
 
 template <typename T>
@@ -211,7 +212,7 @@ __device__ __forceinline__ void finalize_row(const P& p, const float4* part, int
 // three slots: slot r%3 is rewritten for row r+3 only after every thread has
 // passed the wait of row r+1, which CTA 0 reaches after merging row r.
 template <typename T, int K>
-__global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LseParams<T> p) {
+__global__ void __launch_bounds__(kLseThreads) lse_gather_kernel(const LseParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -230,12 +231,6 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
   const int64_t nq = K > 1 ? (int64_t)nclusters_x() : (int64_t)gridDim.x;
   const uint32_t ring = smem_u32(smem);
 
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
-  const int32_t* off = p.offsets;
-  if (p.N + 1 <= kSmemOffsets) {
-    for (int64_t k = tid; k <= p.N; k += kLseThreads) s_off[k] = p.offsets[k];
-    off = s_off;
-  }
   if (tid < 3) s_found[tid] = -1;
   if (tid == 0) {
     s_abort = 0;
@@ -244,6 +239,14 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
       mbar_init(smem_u32(&s_empty[k]), kWarps);
     }
     mbar_init_fence();
+  }
+  pdl_wait();  // the previous kernel's writes (offsets, ids) are visible from here
+  pdl_trigger();
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
+  const int32_t* off = p.offsets;
+  if (p.N + 1 <= kSmemOffsets) {
+    for (int64_t k = tid; k <= p.N; k += kLseThreads) s_off[k] = p.offsets[k];
+    off = s_off;
   }
   // every CTA of the cluster is running and initialised before any
   // distributed-shared-memory store or bulk copy
@@ -304,6 +307,8 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
       __syncwarp();
     } else {
       float m = -INFINITY, s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+      uint64_t acc01 = f2_pack(0.f, 0.f), acc23 = f2_pack(0.f, 0.f);
       float zy = 0.f;
       bool found = false;
       // ragged head and tail (fewer than EPV elements each)
@@ -359,20 +364,21 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
           const float bm = E::template batch_max<kVecPerThread>(d);
           if (bm > m) {
             const float sc = ex2((m - bm) * kLog2e);
-            s0 *= sc;
-            s1 *= sc;
-            s2 *= sc;
-            s3 *= sc;
+            const uint64_t sc2 = f2_pack(sc, sc);
+            acc01 = f2_mul(acc01, sc2);
+            acc23 = f2_mul(acc23, sc2);
+            s0 *= sc;  // holds the ragged elements, if any
             m = bm;
           }
           if (m != -INFINITY) {
             const float mL = m * kLog2e;
+            const uint64_t nmL2 = f2_pack(-mL, -mL);
+            // pairs: one packed FMA for two arguments, one packed add for
+            // two sums; the fixed pairing keeps the summation order fixed
 #pragma unroll
             for (int k = 0; k < kVecPerThread * EPV; k += 4) {
-              s0 += ex2(fmaf(x[k + 0], kLog2e, -mL));
-              s1 += ex2(fmaf(x[k + 1], kLog2e, -mL));
-              s2 += ex2(fmaf(x[k + 2], kLog2e, -mL));
-              s3 += ex2(fmaf(x[k + 3], kLog2e, -mL));
+              acc01 = f2_add(acc01, f2_ex2(f2_fma(f2_pack(x[k + 0], x[k + 1]), L2, nmL2)));
+              acc23 = f2_add(acc23, f2_ex2(f2_fma(f2_pack(x[k + 2], x[k + 3]), L2, nmL2)));
             }
           }
         }
@@ -380,6 +386,16 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
           stage = 0;
           phase ^= 1u;
         }
+      }
+      {
+        // the ragged elements went into s0 (relative to the same running max)
+        float a0, a1, a2, a3;
+        f2_unpack(acc01, a0, a1);
+        f2_unpack(acc23, a2, a3);
+        s0 += a0;
+        s1 += a1;
+        s2 += a2;
+        s3 += a3;
       }
       float s = (s0 + s1) + (s2 + s3);
       for (int o = 16; o > 0; o >>= 1) {
@@ -400,10 +416,12 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
         for (int k = 1; k < kWarps; ++k) lse_merge(cm, cs, s_red[rb][k].x, s_red[rb][k].y);
         const bool has = s_found[slot] == r;
         const float4 part = make_float4(cm, cs, has ? s_zy[slot] : 0.f, has ? 1.f : 0.f);
-        if (K > 1)
+        if (K > 1) {
           st_cluster_f32x4(map_to_rank(smem_u32(&s_part[slot][rank]), 0), part);
-        else
+          fence_cluster();  // the only store another CTA reads; see cluster_arrive_relaxed
+        } else {
           s_part[slot][0] = part;
+        }
       }
     }
     __syncwarp();  // the cluster barrier instructions are warp-aligned
@@ -412,7 +430,7 @@ __global__ void __launch_bounds__(kLseThreads, 4) lse_gather_kernel(const LsePar
         cluster_wait();  // row it-1: every CTA's partial has landed in CTA 0
         if (rank == 0 && tid == 0) finalize_row<K>(p, s_part[(it - 1) % 3], prev_i, prev_t);
       }
-      cluster_arrive();
+      cluster_arrive_relaxed();
     } else if (tid == 0) {
       finalize_row<K>(p, s_part[slot], i, t);
     }
@@ -473,16 +491,18 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
     done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = K;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kLseThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = K > 1 ? 1 : 0;
+  cfg.numAttrs = K > 1 ? 1 : 0;  // the occupancy query takes the cluster only
 
   int clusters = 0;
   const auto key = std::make_tuple(d.device, (int)sizeof(T), K, (int)smem);
@@ -509,13 +529,20 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   const int64_t max_rows = a.N * a.C;  // upper bound on the valid tokens
   const int64_t nq = clusters < max_rows ? clusters : max_rows;
   cfg.gridDim = dim3((unsigned)(nq * K));
+  if (K > 1) {
+    cfg.numAttrs = 2;
+  } else {
+    attr[0] = attr[1];
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <typename T>
 cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  // clusters of more than 4 CTAs couple too many CTAs at every row's barrier
-  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_LSE_CLUSTER", 4)) {
+  // pairs of CTAs measured fastest: larger clusters couple more CTAs at every
+  // row's barrier (4: -20%, 8: -50% on the batched workload)
+  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_LSE_CLUSTER", 2)) {
     case 8:
       return launch_k<T, 8>(a, d, st);
     case 4:

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(kThreads) mask_kernel(const int64_t* __restric
                                                         int64_t eos, uint8_t* __restrict__ mask,
                                                         int32_t* __restrict__ len) {
   __shared__ int64_t warp_min[kWarps];
+  pdl_wait();
+  pdl_trigger();
   const int64_t i = blockIdx.x;
   const int64_t* comp = ids + i * T + P;
   int64_t first = C;  // C stands for "no EOS"
@@ -47,8 +49,8 @@ __global__ void __launch_bounds__(kThreads) mask_kernel(const int64_t* __restric
 cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int64_t eos,
                         uint8_t* mask, int32_t* len, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  mask_kernel<<<(unsigned)N, kThreads, 0, st>>>(ids, P + C, P, C, eos, mask, len);
-  return cudaGetLastError();
+  return launch_pdl(mask_kernel, dim3((unsigned)N), dim3(kThreads), 0, st, 1, ids, P + C, P, C,
+                    eos, mask, len);
 }
 
 // One warp per group.  Lane l sums rewards l, l+32, ... of the group in that
@@ -57,6 +59,8 @@ cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int
 __global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __restrict__ R,
                                                              int64_t B, int64_t G,
                                                              float* __restrict__ adv) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t b = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -72,8 +76,7 @@ __global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __rest
 cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, float* adv, cudaStream_t st) {
   if (B == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((B + kWarps - 1) / kWarps);
-  advantage_kernel<<<blocks, kThreads, 0, st>>>(R, B, G, adv);
-  return cudaGetLastError();
+  return launch_pdl(advantage_kernel, dim3(blocks), dim3(kThreads), 0, st, 1, R, B, G, adv);
 }
 
 }  // namespace grpo

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(kThreads) surrogate_kernel(const SurParams p) 
   __shared__ double s_red[kWarps];
   __shared__ bool s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   const int64_t NC = p.N * p.C;
   const float lo = 1.f - p.eps, hi = 1.f + p.eps;
   double acc = 0.0;
@@ -124,8 +126,7 @@ cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st) {
   int64_t blocks = (NC + kThreads - 1) / kThreads;
   if (blocks > kMaxLossBlocks) blocks = kMaxLossBlocks;
   if (blocks < 1) blocks = 1;
-  surrogate_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(surrogate_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1, p);
 }
 
 }  // namespace grpo
