@@ -39,7 +39,7 @@ from vocab_wide_logprob_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "completion tokens/s and logits GB/s (% of HBM roofline), Dr.GRPO loss fwd+bwd"
 UNIT = "completion tokens/s"
-KERNELS_PER_STEP = 6  # mask, advantage, prep, lse_gather, surrogate, dlogits
+KERNELS_PER_STEP = 6  # mask, advantage, prep, lse_gather, surrogate, dlogits (fused: 5)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-copy-ceiling", action="store_true")
+    p.add_argument("--path", choices=["two_pass", "fused"], default="two_pass",
+                   help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd")
     return p.parse_args()
 
 
@@ -74,6 +76,9 @@ def algorithmic_bytes(w: wl.Workload, t_valid: int) -> dict:
         "mask_adv": 8 * N * C + N * C + 8 * N,
         # the roofline count of the whole method: two reads + one write
         "step_logits": 2 * t_valid * V * e + N * T * V * e,
+        # the fused call: one read of the scored rows + one write of dlogits
+        "fused": t_valid * V * e + N * T * V * e + 8 * t_valid + small,
+        "step_logits_fused": t_valid * V * e + N * T * V * e,
     }
 
 
@@ -342,6 +347,7 @@ def run_ours(args, w0: wl.Workload):
     out = None
     ws = cur["workspace"]
     stream = torch.cuda.current_stream()
+    fused = args.path == "fused"
 
     def step(record=None):
         nonlocal out
@@ -351,6 +357,13 @@ def run_ours(args, w0: wl.Workload):
         a = g.grpo_advantage(R, w.G, adv)
         if record is not None:
             record[1].record(stream)
+        if fused:
+            out = g.grpo_loss_fwd_bwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, None,
+                                      out, ws, dlogits)
+            if record is not None:
+                record[2].record(stream)
+                record[3].record(stream)
+            return
         out = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, out, ws)
         if record is not None:
             record[2].record(stream)
@@ -450,8 +463,15 @@ def run_ours(args, w0: wl.Workload):
         peak = peak or FALLBACK_HBM_GBS
         b = algorithmic_bytes(w, t_valid)
         ms = elapsed / args.steps
-        achieved = b["bwd"] / t_bwd / 1e9
-        traffic = recorded_traffic("dlogits_kernel", w)
+        if fused:
+            # the fused call: prep + zero-row writer + lse_grad_kernel, timed together
+            step_bytes = b["step_logits_fused"]
+            kernel, kbytes, kt = "grpo_loss_fwd_bwd", b["fused"], t_fwd
+        else:
+            step_bytes = b["step_logits"]
+            kernel, kbytes, kt = "dlogits_kernel", b["bwd"], t_bwd
+        achieved = kbytes / kt / 1e9
+        traffic = recorded_traffic(kernel, w)
         line = {
             "metric": METRIC, "value": t_valid_all / ms, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms * 1e3,
@@ -461,19 +481,21 @@ def run_ours(args, w0: wl.Workload):
                        "logits_dtype": w.dtype, "valid_tokens_per_rank": t_valid,
                        "l2": f"inputs larger than L2 ({w.logits_bytes / 1e9:.2f} GB logits); "
                              "no flush", "parallelism": f"dp{world} (independent groups)"},
-            "logits_gbs": b["step_logits"] / ms / 1e9,
-            "logits_roofline_frac": b["step_logits"] / ms / 1e9 / peak,
+            "path": args.path,
+            "logits_gbs": step_bytes / ms / 1e9,
+            "logits_roofline_frac": step_bytes / ms / 1e9 / peak,
+            "logits_bytes_per_step": step_bytes,
             "kernel_ms": {"mask+advantage": t_mask * 1e3, "fwd": t_fwd * 1e3,
                           "bwd": t_bwd * 1e3},
-            "fwd_gbs": b["fwd"] / t_fwd / 1e9,
-            "roofline": {"kernel": "dlogits_kernel", "bound": "hbm", "achieved": achieved,
+            "fwd_gbs": (b["fused"] if fused else b["fwd"]) / t_fwd / 1e9,
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved,
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes": b["bwd"]},
+                         "algorithmic_bytes": kbytes},
             "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
             "copy_ceiling_gbs": copy_gbs,
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": (KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP) * args.steps,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "loss": loss_val,

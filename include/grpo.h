@@ -191,6 +191,28 @@ grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64
                           void *dlogits, grpo_stream_t stream);
 
 /*
+ * grpo_loss_fwd_bwd -- grpo_loss_fwd and grpo_loss_bwd in one pass over each
+ * scored row: the row is read from HBM once (its log-sum-exp, log-prob and
+ * gradient weight are formed, then its gradient is written) instead of once by
+ * each call.  Same method ("compute_logprobs", "The loss", "loss.backward()"),
+ * composed per row; it needs the upstream gradient when the forward runs.
+ *
+ * Arguments: those of grpo_loss_fwd, then grad_loss (one float32 in device
+ * memory, or NULL for 1) and dlogits [N, P+C, V] as in grpo_loss_bwd.
+ * Results: logp, lse, w and dlogits have the same bits as grpo_loss_fwd
+ * followed by grpo_loss_bwd; the loss is summed in another fixed order
+ * (per cluster, then clusters in order), so it agrees to float rounding.
+ * When logits and dlogits do not start at the same offset modulo 16 bytes the
+ * call runs the two passes instead (same results).
+ */
+grpo_status grpo_loss_fwd_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
+                              int64_t C, int64_t V, const int64_t *input_ids, const int32_t *len,
+                              const float *adv, const float *old_logp, const float *ref_logp,
+                              float eps, float beta, float norm, const float *grad_loss,
+                              float *logp, float *lse, float *w, float *loss, void *dlogits,
+                              void *workspace, size_t workspace_bytes, grpo_stream_t stream);
+
+/*
  * grpo_check_error -- synchronises `stream`, then reports what the kernels of
  * the most recent grpo_loss_fwd on `workspace` recorded: GRPO_OK,
  * GRPO_ERR_TOKEN_RANGE (a scored id outside [0, V); its logp and lse are NaN),

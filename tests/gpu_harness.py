@@ -62,16 +62,23 @@ def dev(x, device="cuda"):
 
 
 def run_gpu(w: wl.Workload, logits, ids, R, old, ref, grad=None, dlogits=None, eps=None,
-            beta=None, norm=0.0):
-    """mask -> advantage -> fwd -> bwd through the C ABI; returns tensors."""
+            beta=None, norm=0.0, fused=False):
+    """mask -> advantage -> fwd -> bwd (or the fused fwd+bwd) through the C
+    ABI; returns tensors."""
     n = g()
     t_ids = dev(ids)
     mask, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
     adv = n.grpo_advantage(dev(R), w.G)
-    out = n.grpo_loss_fwd(logits, w.P, t_ids, lens, adv, dev(old), dev(ref),
-                          w.eps if eps is None else eps, w.beta if beta is None else beta, norm)
     gt = None if grad is None else torch.tensor([grad], dtype=torch.float32, device="cuda")
-    dl = n.grpo_loss_bwd(logits, w.P, t_ids, lens, out["lse"], out["w"], gt, dlogits)
+    e = w.eps if eps is None else eps
+    b = w.beta if beta is None else beta
+    if fused:
+        out = n.grpo_loss_fwd_bwd(logits, w.P, t_ids, lens, adv, dev(old), dev(ref), e, b, norm,
+                                  gt, dlogits=dlogits)
+        dl = out["dlogits"]
+    else:
+        out = n.grpo_loss_fwd(logits, w.P, t_ids, lens, adv, dev(old), dev(ref), e, b, norm)
+        dl = n.grpo_loss_bwd(logits, w.P, t_ids, lens, out["lse"], out["w"], gt, dlogits)
     status = n.grpo_check_error(out["workspace"])
     torch.cuda.synchronize()
     out.update(mask=mask, lens=lens, adv=adv, dlogits=dl, status=status)
@@ -118,7 +125,8 @@ def to_host_logits(t: torch.Tensor):
     return wl.logits_as_numpy(t.cpu())
 
 
-def check_small(w: wl.Workload, logits_cpu=None, grad=None, norm=0.0, logits_gpu=None):
+def check_small(w: wl.Workload, logits_cpu=None, grad=None, norm=0.0, logits_gpu=None,
+                fused=False, dlogits=None):
     """Whole-batch element-wise comparison (sizes the oracle finishes fast)."""
     ids = wl.make_ids(w)
     R = wl.make_rewards(w)
@@ -137,7 +145,8 @@ def check_small(w: wl.Workload, logits_cpu=None, grad=None, norm=0.0, logits_gpu
     d_o = oracle.dlogits(z, dt, w.P, w.C, ids, len_o, lse_o, w_o, gval)
 
     logits = logits_cpu.cuda() if logits_gpu is None else logits_gpu
-    out = run_gpu(w, logits, ids, R, old, ref, grad=grad, norm=norm)
+    out = run_gpu(w, logits, ids, R, old, ref, grad=grad, norm=norm, fused=fused,
+                  dlogits=dlogits)
     assert out["status"] == 0
     assert np.array_equal(out["mask"].cpu().numpy(), m_o)
     assert np.array_equal(out["lens"].cpu().numpy(), len_o)

@@ -1,0 +1,120 @@
+"""The fused forward+backward (grpo_loss_fwd_bwd) against the float64 oracle
+and against the two-call path: logp, lse, w and dlogits must have the same
+bits as grpo_loss_fwd followed by grpo_loss_bwd (same arithmetic per element,
+same per-token terms); the loss is summed in another fixed order and must
+agree to float rounding."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+import oracle
+from vocab_wide_logprob_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def _both(w, logits_cpu=None, grad=None, norm=0.0, logits_gpu=None, dlogits=None):
+    ids = wl.make_ids(w)
+    R = wl.make_rewards(w)
+    if logits_cpu is None:
+        logits_cpu = wl.make_logits_cpu(w)
+    z, dt = wl.logits_as_numpy(logits_cpu)
+    m_o, len_o = oracle.mask(ids, w.P, w.C, w.eos_id)
+    lp_o, _ = oracle.logp(z, dt, w.P, w.C, ids, len_o)
+    old, ref = H.host_inputs(w, lp_o, m_o)
+    logits = logits_cpu.cuda() if logits_gpu is None else logits_gpu
+    a = H.run_gpu(w, logits, ids, R, old, ref, grad=grad, norm=norm)
+    b = H.run_gpu(w, logits, ids, R, old, ref, grad=grad, norm=norm, fused=True, dlogits=dlogits)
+    return a, b
+
+
+CASES = [
+    wl.variant(wl.TINY, name="tiny_terms", old_sigma=0.1, ref_sigma=0.1, beta=0.04),
+    wl.variant(wl.QWEN_G8, name="bf16_small", B=1, G=4, P=8, C=24, reward_p=0.5,
+               old_sigma=0.1, ref_sigma=0.1, beta=0.04, trunc=0.25, seed=77),
+    wl.variant(wl.TINY, name="ragged_bf16", V=50001, dtype="bf16", old_sigma=0.1,
+               ref_sigma=0.1, beta=0.04, logit_std=3.0, seed=11),
+    wl.variant(wl.TINY, name="ragged_f32", V=65539, dtype="f32", old_sigma=0.1, ref_sigma=0.1,
+               beta=0.04, logit_std=3.0, seed=12),
+    wl.variant(wl.TINY, name="tiny_V7", V=7, dtype="bf16", old_sigma=0.1, seed=13),
+    wl.variant(wl.TINY, name="C1", C=1, old_sigma=0.1, ref_sigma=0.1, beta=0.04),
+    wl.variant(wl.TINY, name="G32", G=32, B=2, reward_p=0.5, old_sigma=0.1),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fused_matches_oracle(w):
+    H.check_small(H.with_contrast(w), fused=True)
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fused_same_bits_as_two_calls(w):
+    a, b = _both(H.with_contrast(w), grad=3.0)
+    for k in ("logp", "lse", "w", "dlogits", "mask", "lens", "adv"):
+        x, y = a[k], b[k]
+        if x.dtype in (torch.float32, torch.bfloat16):
+            assert torch.equal(_bits(x), _bits(y)), k
+        else:
+            assert torch.equal(x, y), k
+    la, lb = float(a["loss"].item()), float(b["loss"].item())
+    assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
+
+
+def test_fused_scaled_gradient():
+    w = wl.variant(wl.TINY, old_sigma=0.1, ref_sigma=0.1, beta=0.04)
+    H.check_small(w, grad=float(w.N * w.C), fused=True)
+
+
+def test_fused_phase_mismatch_falls_back():
+    """dlogits one element off the logits' 16-byte phase: the call runs the
+    two passes; results still match the oracle."""
+    w = wl.variant(wl.TINY, name="phase", V=1000, dtype="bf16", old_sigma=0.1, seed=99)
+    base = torch.empty(w.N * w.T * w.V + 1, dtype=torch.bfloat16, device="cuda")
+    H.check_small(w, fused=True, dlogits=base[1:].view(w.N, w.T, w.V))
+
+
+def test_fused_reports_bad_token():
+    w = wl.TINY
+    ids = wl.make_ids(w)
+    ids[0, w.P + 3] = -1
+    g = H.g()
+    logits = wl.make_logits_cpu(w).cuda()
+    t_ids = torch.from_numpy(ids).cuda()
+    _, lens = g.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = torch.zeros((w.N,), device="cuda")
+    out = g.grpo_loss_fwd_bwd(logits, w.P, t_ids, lens, adv)
+    assert g.grpo_check_error(out["workspace"]) == 6
+    assert np.isnan(out["logp"].cpu().numpy()[0, 3])
+
+
+@pytest.mark.parametrize("w", [wl.QWEN_G8, wl.BATCHED], ids=lambda w: w.name)
+def test_fused_full_size_same_bits(w):
+    w = H.with_contrast(w)
+    ids = wl.make_ids(w)
+    R = wl.make_rewards(w)
+    logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    wl.fill_logits_cuda(w, logits)
+    n_old, n_ref = wl.make_noise(w)
+    g = H.g()
+    t_ids = torch.from_numpy(ids).cuda()
+    _, lens = g.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = g.grpo_advantage(torch.from_numpy(R).cuda(), w.G)
+    cur = g.grpo_loss_fwd(logits, w.P, t_ids, lens, adv)
+    old = cur["logp"] + torch.from_numpy(n_old).float().cuda()
+    a = g.grpo_loss_fwd(logits, w.P, t_ids, lens, adv, old, None, w.eps, w.beta)
+    da = g.grpo_loss_bwd(logits, w.P, t_ids, lens, a["lse"], a["w"])
+    b = g.grpo_loss_fwd_bwd(logits, w.P, t_ids, lens, adv, old, None, w.eps, w.beta)
+    torch.cuda.synchronize()
+    assert g.grpo_check_error(b["workspace"]) == 0
+    for k in ("logp", "lse", "w"):
+        assert torch.equal(_bits(a[k]), _bits(b[k])), k
+    assert torch.equal(_bits(da), _bits(b["dlogits"]))
+    la, lb = float(a["loss"].item()), float(b["loss"].item())
+    assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
+    del logits, da, b
+    torch.cuda.empty_cache()

@@ -8,7 +8,8 @@ generators stay usable on machines without the built library.
 """
 
 _NAMES = ("grpo_mask", "grpo_advantage", "grpo_workspace_size", "grpo_loss_fwd",
-          "grpo_loss_bwd", "grpo_check_error", "grpo_copy", "GrpoError")
+          "grpo_loss_bwd", "grpo_loss_fwd_bwd", "grpo_loss_fwd_static", "grpo_check_error",
+          "grpo_copy", "GrpoError")
 
 
 def __getattr__(name):

@@ -52,6 +52,8 @@ def _load():
         "grpo_copy": ([P, P, SZ, P], INT),
         "grpo_loss_fwd_static": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
                                   P], INT),
+        "grpo_loss_fwd_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P, P,
+                               P, P, SZ, P], INT),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -213,6 +215,41 @@ def grpo_loss_bwd(logits, P, input_ids, lens, lse, w, grad_loss=None, dlogits=No
                               _ptr(lens), _ptr(lse), _ptr(w), _ptr(grad_loss), _ptr(dlogits),
                               _stream(stream)), "grpo_loss_bwd")
     return dlogits
+
+
+def grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
+                      beta=0.0, norm=0.0, grad_loss=None, out=None, workspace=None,
+                      dlogits=None, stream=None):
+    """Forward and backward in one pass over each scored row.  Returns the
+    dict of :func:`grpo_loss_fwd` plus ``dlogits``."""
+    _dev(logits, "logits")
+    N, T, V = logits.shape
+    C = T - P
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("adv", adv, torch.float32), ("old_logp", old_logp, torch.float32),
+                        ("ref_logp", ref_logp, torch.float32),
+                        ("grad_loss", grad_loss, torch.float32)):
+        _dev(t, name, dt)
+    dev = logits.device
+    if out is None:
+        out = {"logp": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "lse": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "w": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "loss": torch.empty((1,), dtype=torch.float32, device=dev)}
+    need = grpo_workspace_size(N, C, V)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    _dev(dlogits, "dlogits", logits.dtype)
+    out["workspace"] = workspace
+    out["dlogits"] = dlogits
+    _check(_lib.grpo_loss_fwd_bwd(
+        _ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
+        _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(grad_loss),
+        _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _ptr(dlogits),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "grpo_loss_fwd_bwd")
+    return out
 
 
 def grpo_check_error(workspace, stream=None) -> int:

@@ -223,6 +223,87 @@ grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64
   return from_cuda(launch_dlogits(a, d, (cudaStream_t)stream));
 }
 
+grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                              int64_t C, int64_t V, const int64_t* input_ids, const int32_t* len,
+                              const float* adv, const float* old_logp, const float* ref_logp,
+                              float eps, float beta, float norm, const float* grad_loss,
+                              float* logp, float* lse, float* w, float* loss, void* dlogits,
+                              void* workspace, size_t workspace_bytes, grpo_stream_t stream) {
+  grpo_status s = check_shapes(dtype, N, P, C, V);
+  if (s != GRPO_OK) return s;
+  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
+  if (N > 0 && dlogits == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(dlogits, esize) || !aligned(grad_loss, 4)) return GRPO_ERR_MISALIGNED;
+  if (N > 0 && logits != nullptr) {
+    const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
+    const char* lo = static_cast<const char*>(logits);
+    const char* dl = static_cast<const char*>(dlogits);
+    if (dl < lo + bytes && lo < dl + bytes) return GRPO_ERR_INVALID_ARG;
+  }
+  const bool same_phase = ((reinterpret_cast<uintptr_t>(logits) ^
+                            reinterpret_cast<uintptr_t>(dlogits)) & 15u) == 0;
+  if (N == 0 || C == 0 || !same_phase) {  // nothing to fuse, or no common vector grid
+    s = grpo_loss_fwd(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                      beta, norm, logp, lse, w, loss, workspace, workspace_bytes, stream);
+    if (s != GRPO_OK) return s;
+    return grpo_loss_bwd(logits, dtype, N, P, C, V, input_ids, len, lse, w, grad_loss, dlogits,
+                         stream);
+  }
+  // the forward's validation (pointers, eps, beta, norm, workspace)
+  if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) || isinf(norm))
+    return GRPO_ERR_INVALID_ARG;
+  if (loss == nullptr || workspace == nullptr || len == nullptr || adv == nullptr ||
+      logits == nullptr || input_ids == nullptr || logp == nullptr || lse == nullptr ||
+      w == nullptr)
+    return GRPO_ERR_INVALID_ARG;
+  if (beta != 0.f && ref_logp == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(logits, esize) || !aligned(input_ids, 8) || !aligned(len, 4) ||
+      !aligned(adv, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(logp, 4) ||
+      !aligned(lse, 4) || !aligned(w, 4) || !aligned(loss, 4) || !aligned(workspace, 256))
+    return GRPO_ERR_MISALIGNED;
+  if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
+
+  FwdArgs a;
+  a.logits = logits;
+  a.dtype = dtype == GRPO_F32 ? 0 : 1;
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.ids = input_ids;
+  a.len = len;
+  a.adv = adv;
+  a.old_logp = old_logp;
+  a.ref_logp = beta != 0.f ? ref_logp : nullptr;
+  a.eps = eps;
+  a.beta = beta;
+  a.norm = norm;
+  a.logp = logp;
+  a.lse = lse;
+  a.w = w;
+  a.loss = loss;
+  a.ws = workspace;
+  BwdArgs b;
+  b.logits = logits;
+  b.dtype = a.dtype;
+  b.N = N;
+  b.P = P;
+  b.C = C;
+  b.V = V;
+  b.ids = input_ids;
+  b.len = len;
+  b.lse = lse;
+  b.w = w;
+  b.grad = grad_loss;
+  b.dlogits = dlogits;
+  const cudaStream_t st = (cudaStream_t)stream;
+  DeviceInfo d;
+  if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_zero_rows(b, d, st, logp, lse, w) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_lse_grad(a, b, d, st));
+}
+
 grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
   if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
   uint32_t flags = 0;

@@ -287,6 +287,44 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 }
 
 // ---------------------------------------------------------------------------
+// per-token loss terms ("The loss" / grpo_loss; the k3 KL term)
+// ---------------------------------------------------------------------------
+
+// For one valid token with log-prob lp: the per-token loss ell and
+// w = d loss / d logp (before dividing by the normaliser).
+//   r   = exp(lp - old)                      (1 when there is no old log-prob)
+//   s   = min(r*A, clamp(r, 1-eps, 1+eps)*A)  -- clip the ratio, then * A
+//   k3  = exp(d) - d - 1, d = ref - lp        (written expm1(d) - d)
+//   ell = -s + beta*k3
+//   w   = -(A*r if min() takes r*A, else 0) + beta*(1 - exp(d))
+// NaN inputs give NaN results (the comparisons keep NaN).  Shared by the
+// unfused and the fused forward so both give the same bits.
+struct TokenTerms {
+  float ell, w;
+};
+__device__ __forceinline__ TokenTerms token_terms(float lp, float A, bool has_old, float old,
+                                                  float beta, float ref, float eps) {
+  const float lo = 1.f - eps, hi = 1.f + eps;
+  const float r = has_old ? expf(lp - old) : 1.f;
+  const float unclipped = r * A;
+  const float rc = r < lo ? lo : (r > hi ? hi : r);
+  const float clipped = rc * A;
+  const float s = unclipped < clipped ? unclipped : clipped;
+  const float ds = unclipped <= clipped ? A * r : 0.f;
+  float k3 = 0.f, dk3 = 0.f;
+  if (beta != 0.f) {
+    const float d = ref - lp;
+    const float em1 = expm1f(d);
+    k3 = em1 - d;
+    dk3 = -em1;
+  }
+  TokenTerms tt;
+  tt.ell = -s + beta * k3;
+  tt.w = -ds + beta * dk3;
+  return tt;
+}
+
+// ---------------------------------------------------------------------------
 // element types: 16-byte vectors of float32 (4) or bfloat16 bit patterns (8)
 // ---------------------------------------------------------------------------
 
@@ -447,6 +485,12 @@ struct BwdArgs {
   void* dlogits;
 };
 cudaError_t launch_dlogits(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st);
+// Store-only pass of the fused path: zero dlogits rows and masked logp/lse/w.
+cudaError_t launch_zero_rows(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st, float* logp,
+                             float* lse, float* w);
+// Fused forward + backward over the scored rows (after prep and zero rows).
+cudaError_t launch_lse_grad(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d,
+                            cudaStream_t st);
 
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceInfo& d,
                         cudaStream_t st);

@@ -29,9 +29,16 @@ struct DlParams {
   const float* grad;  // device scalar or nullptr (1)
   int64_t chunk;      // elements per work item (multiple of kPerVec)
   int64_t split;      // work items per row
+  // store-only mode (the fused forward+backward writes the scored rows):
+  // also zero logp, lse and w [N, C] past each length
+  float* logp_out;
+  float* lse_out;
+  float* w_out;
 };
 
-template <typename T>
+// kZeroOnly: write only the rows that score nothing (and the masked
+// per-token outputs); scored rows are left to lse_grad_kernel.
+template <typename T, bool kZeroOnly>
 __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
@@ -42,6 +49,19 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
   const float g = p.grad != nullptr ? __ldg(p.grad) : 1.f;
   const int64_t items = p.N * p.T_len * p.split;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  if (kZeroOnly) {
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + tid; k < p.N * p.C;
+         k += (int64_t)gridDim.x * kThreads) {
+      const int64_t i = k / p.C;
+      int64_t L = __ldg(p.len + i);
+      L = L < 0 ? 0 : (L > p.C ? p.C : L);
+      if (k - i * p.C >= L) {
+        p.logp_out[k] = 0.f;
+        p.lse_out[k] = 0.f;
+        p.w_out[k] = 0.f;
+      }
+    }
+  }
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int64_t row = item / p.split;
     const int64_t j = item - row * p.split;
@@ -68,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
       if (tid >= 32 && tid - 32 < v1 - b) E::store1(orow + b + (tid - 32), 0.f);
       continue;
     }
+    if (kZeroOnly) continue;
     const int64_t k_tok = i * p.C + t;
     const float gw = g * __ldg(p.w + k_tok);
     const float ngw = -gw;
@@ -128,8 +149,9 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
 
 namespace {
 
-template <typename T>
-cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
+template <typename T, bool kZeroOnly>
+cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st, float* logp,
+                     float* lse, float* w_out) {
   constexpr int EPV = Elt<T>::kPerVec;
   DlParams<T> p;
   p.logits = static_cast<const T*>(a.logits);
@@ -144,6 +166,9 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.lse = a.lse;
   p.w = a.w;
   p.grad = a.grad;
+  p.logp_out = logp;
+  p.lse_out = lse;
+  p.w_out = w_out;
   p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT", 8);
   p.chunk = ((a.V + p.split - 1) / p.split + EPV - 1) / EPV * EPV;
   // An oversubscribed grid (many more CTAs than fit at once, grid-stride over
@@ -152,14 +177,23 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   const int64_t items = a.N * (a.P + a.C) * p.split;
   int64_t grid = (int64_t)grid_mult("GRPO_BWD_GRID", 256) * d.sms;
   if (grid > items) grid = items;
-  return launch_pdl(dlogits_kernel<T>, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, p);
+  return launch_pdl(dlogits_kernel<T, kZeroOnly>, dim3((unsigned)grid), dim3(kThreads), 0, st,
+                    1, p);
 }
 
 }  // namespace
 
 cudaError_t launch_dlogits(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   if (a.N == 0) return cudaSuccess;
-  return a.dtype == 0 ? launch_t<float>(a, d, st) : launch_t<uint16_t>(a, d, st);
+  return a.dtype == 0 ? launch_t<float, false>(a, d, st, nullptr, nullptr, nullptr)
+                      : launch_t<uint16_t, false>(a, d, st, nullptr, nullptr, nullptr);
+}
+
+cudaError_t launch_zero_rows(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st, float* logp,
+                             float* lse, float* w) {
+  if (a.N == 0) return cudaSuccess;
+  return a.dtype == 0 ? launch_t<float, true>(a, d, st, logp, lse, w)
+                      : launch_t<uint16_t, true>(a, d, st, logp, lse, w);
 }
 
 }  // namespace grpo

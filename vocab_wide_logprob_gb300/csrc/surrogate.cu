@@ -42,7 +42,6 @@ __global__ void __launch_bounds__(kThreads) surrogate_kernel(const SurParams p) 
   pdl_wait();
   pdl_trigger();
   const int64_t NC = p.N * p.C;
-  const float lo = 1.f - p.eps, hi = 1.f + p.eps;
   double acc = 0.0;
   for (int64_t k = (int64_t)blockIdx.x * kThreads + tid; k < NC;
        k += (int64_t)gridDim.x * kThreads) {
@@ -54,22 +53,12 @@ __global__ void __launch_bounds__(kThreads) surrogate_kernel(const SurParams p) 
       continue;
     }
     const float lp = p.logp[k];
-    const float A = p.adv[i];
-    const float r = p.old_logp != nullptr ? expf(lp - p.old_logp[k]) : 1.f;
-    const float unclipped = r * A;
-    const float rc = r < lo ? lo : (r > hi ? hi : r);  // NaN stays NaN
-    const float clipped = rc * A;
-    const float s = unclipped < clipped ? unclipped : clipped;
-    const float ds = unclipped <= clipped ? A * r : 0.f;
-    float k3 = 0.f, dk3 = 0.f;
-    if (p.beta != 0.f) {
-      const float d = p.ref_logp[k] - lp;
-      const float em1 = expm1f(d);
-      k3 = em1 - d;
-      dk3 = -em1;
-    }
-    const float ell = -s + p.beta * k3;
-    p.w[k] = (float)((double)(-ds + p.beta * dk3) / p.norm);
+    const TokenTerms tt =
+        token_terms(lp, p.adv[i], p.old_logp != nullptr,
+                    p.old_logp != nullptr ? p.old_logp[k] : 0.f, p.beta,
+                    p.beta != 0.f ? p.ref_logp[k] : 0.f, p.eps);
+    p.w[k] = (float)((double)tt.w / p.norm);
+    const float ell = tt.ell;
     acc += (double)ell;
   }
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
