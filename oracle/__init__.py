@@ -97,6 +97,8 @@ class Oracle:
         sig = {
             "oracle_mask": [P, I64, I64, I64, I64, P, P],
             "oracle_advantage": [P, I64, I64, P],
+            "oracle_advantage_std": [P, I64, I64, D, P],
+            "oracle_loss_agg": [P, P, P, P, P, I64, I64, D, D, D, INT, P, P, P],
             "oracle_logp_rows": [P, INT, I64, I64, P, P, P],
             "oracle_logp": [P, INT, I64, I64, I64, I64, P, P, P, P],
             "oracle_loss": [P, P, P, P, P, I64, I64, D, D, D, P, P, P],
@@ -144,6 +146,17 @@ class Oracle:
         _check(self.lib.oracle_advantage(_ptr(R), R.size // G, G, _ptr(A)), "advantage")
         return A
 
+    def advantage_std(self, rewards: np.ndarray, G: int, std_eps: float = 0.0) -> np.ndarray:
+        """Original GRPO: A_i = (R_i - mean) / (std + std_eps) within the group
+        (std over the G rewards, dividing by G)."""
+        R = np.ascontiguousarray(rewards, dtype=np.float64).reshape(-1)
+        if G < 1 or R.size % G:
+            raise ValueError("len(rewards) must be a multiple of G >= 1")
+        A = np.zeros_like(R)
+        _check(self.lib.oracle_advantage_std(_ptr(R), R.size // G, G, float(std_eps), _ptr(A)),
+               "advantage_std")
+        return A
+
     # -- "compute_logprobs" --------------------------------------------------
     def logp_rows(self, rows: np.ndarray, dtype: str, y: np.ndarray):
         """Independent rows [n, V] -> ``(logp [n], lse [n])``,
@@ -174,11 +187,21 @@ class Oracle:
         return lp, ls
 
     # -- "The loss" ------------------------------------------------------------
+    def loss_seq_mean(self, logp, old, ref, adv, lens, eps: float, beta: float,
+                      norm: float = 0.0):
+        """Original GRPO aggregation: each completion's token sum divided by its
+        length, summed over completions and divided by ``norm`` (<= 0: N).
+        Returns ``(loss, w, ell)`` like :meth:`loss`."""
+        return self._loss(logp, old, ref, adv, lens, eps, beta, norm, 1)
+
     def loss(self, logp, old, ref, adv, lens, eps: float, beta: float, norm: float = 0.0):
         """Dr. GRPO loss.  ``old=None``: old log-probs equal current ones
         (ratio exactly 1).  ``ref`` may be None only when beta == 0.
         ``norm <= 0`` selects N*C.  Returns ``(loss, w [N, C], ell [N, C])``,
         ell the per-token loss and w = d loss / d logp."""
+        return self._loss(logp, old, ref, adv, lens, eps, beta, norm, 0)
+
+    def _loss(self, logp, old, ref, adv, lens, eps, beta, norm, agg):
         lp = np.ascontiguousarray(logp, dtype=np.float64)
         N, C = lp.shape
         old = None if old is None else np.ascontiguousarray(old, dtype=np.float64)
@@ -188,9 +211,9 @@ class Oracle:
         out = ctypes.c_double(0.0)
         w = np.zeros((N, C))
         ell = np.zeros((N, C))
-        _check(self.lib.oracle_loss(_ptr(lp), _ptr(old), _ptr(ref), _ptr(A), _ptr(lens), N, C,
-                                    float(eps), float(beta), float(norm), ctypes.addressof(out),
-                                    _ptr(w), _ptr(ell)), "loss")
+        _check(self.lib.oracle_loss_agg(_ptr(lp), _ptr(old), _ptr(ref), _ptr(A), _ptr(lens), N, C,
+                                        float(eps), float(beta), float(norm), int(agg),
+                                        ctypes.addressof(out), _ptr(w), _ptr(ell)), "loss")
         return out.value, w, ell
 
     # -- "loss.backward()" -----------------------------------------------------
@@ -236,6 +259,14 @@ def mask(*a, **k):
 
 def advantage(*a, **k):
     return default().advantage(*a, **k)
+
+
+def advantage_std(*a, **k):
+    return default().advantage_std(*a, **k)
+
+
+def loss_seq_mean(*a, **k):
+    return default().loss_seq_mean(*a, **k)
 
 
 def logp_rows(*a, **k):

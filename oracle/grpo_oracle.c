@@ -210,6 +210,32 @@ int oracle_advantage(const double *R, int64_t B, int64_t G, double *A)
     return 0;
 }
 
+/*
+ * Original GRPO advantage (section "GRPO": "Compute the advantage as
+ * A_i = (R_i - mu)/sigma inside the group"; section "Dr. GRPO" removes the
+ * sigma).  sigma is the standard deviation of the group's rewards,
+ * sqrt(sum (R - mu)^2 / G); std_eps is added to it so a uniform group gives 0
+ * instead of 0/0.
+ */
+int oracle_advantage_std(const double *R, int64_t B, int64_t G, double std_eps, double *A)
+{
+    if (B < 0 || G < 1 || !(std_eps >= 0.0) || (B > 0 && (!R || !A)))
+        return -1;
+    for (int64_t b = 0; b < B; ++b) {
+        double sum = 0.0;
+        for (int64_t g = 0; g < G; ++g)
+            sum += R[b * G + g];
+        double mu = sum / (double)G;
+        double ss = 0.0;
+        for (int64_t g = 0; g < G; ++g)
+            ss += (R[b * G + g] - mu) * (R[b * G + g] - mu);
+        double sigma = sqrt(ss / (double)G);
+        for (int64_t g = 0; g < G; ++g)
+            A[b * G + g] = (R[b * G + g] - mu) / (sigma + std_eps);
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* log-probabilities  ("compute_logprobs": shift, log_softmax, gather)       */
 /* ------------------------------------------------------------------------ */
@@ -360,10 +386,32 @@ static double clamp_d(double x, double lo, double hi)
  *   w = (-(d s / d logp) + beta*(d k3 / d logp)) / norm.
  * Masked positions (t >= len_i) give w = ell = 0 and are never read.
  */
+/*
+ * agg selects the aggregation (section "Dr. GRPO"):
+ *   0  token sum divided by a constant: loss = sum_i sum_t ell / norm
+ *      (norm <= 0 selects N*C) -- Dr. GRPO;
+ *   1  per-response mean, then the mean over responses: loss =
+ *      sum_i (sum_t ell) / len_i / norm (norm <= 0 selects N) -- original
+ *      GRPO's 1/|o_i|; a completion with no valid token contributes 0.
+ * w = d loss / d logp follows the same weights.
+ */
+int oracle_loss_agg(const double *logp, const double *old, const double *ref, const double *A,
+                    const int32_t *len, int64_t N, int64_t C, double eps, double beta,
+                    double norm, int agg, double *loss, double *w, double *ell);
+
 int oracle_loss(const double *logp, const double *old, const double *ref, const double *A,
                 const int32_t *len, int64_t N, int64_t C, double eps, double beta, double norm,
                 double *loss, double *w, double *ell)
 {
+    return oracle_loss_agg(logp, old, ref, A, len, N, C, eps, beta, norm, 0, loss, w, ell);
+}
+
+int oracle_loss_agg(const double *logp, const double *old, const double *ref, const double *A,
+                    const int32_t *len, int64_t N, int64_t C, double eps, double beta,
+                    double norm, int agg, double *loss, double *w, double *ell)
+{
+    if (agg != 0 && agg != 1)
+        return -1;
     if (N < 0 || C < 0 || !loss || !(eps >= 0.0 && eps < 1.0) || !(beta >= 0.0))
         return -1;
     if (beta != 0.0 && !ref)
@@ -371,10 +419,12 @@ int oracle_loss(const double *logp, const double *old, const double *ref, const 
     if (N > 0 && C > 0 && (!logp || !A || !len))
         return -1;
     if (!(norm > 0.0))
-        norm = (double)N * (double)C;
+        norm = agg == 0 ? (double)N * (double)C : (double)N;
     long double total = 0.0L;
     for (int64_t i = 0; i < N; ++i) {
         double a = A[i];
+        /* the constant every token of completion i is divided by */
+        double denom = agg == 0 ? norm : norm * (double)(len[i] > 0 ? len[i] : 1);
         for (int64_t t = 0; t < C; ++t) {
             int64_t k = i * C + t;
             if (t >= len[i]) {
@@ -397,9 +447,9 @@ int oracle_loss(const double *logp, const double *old, const double *ref, const 
                 dk3 = 1.0 - exp(d);
             }
             double l = -s + beta * k3;
-            total += (long double)l;
+            total += (long double)l * ((long double)norm / (long double)denom);
             if (w)
-                w[k] = (-ds + beta * dk3) / norm;
+                w[k] = (-ds + beta * dk3) / denom;
             if (ell)
                 ell[k] = l;
         }

@@ -429,7 +429,98 @@ def pin_dlogits_row_closed_form(o):
     assert np.allclose(out, expect, rtol=0, atol=1e-16)
 
 
+# --------------------------------------------------------------------------
+# original GRPO options: sigma-normalised advantage, per-response mean
+# --------------------------------------------------------------------------
+
+def pin_advantage_std_examples(o):
+    """Section "GRPO": A_i = (R_i - mu)/sigma inside the group.  One success
+    among four: mu = 1/4, sigma = sqrt(3)/4, so A = (sqrt 3, -1/sqrt 3, ...);
+    in general a success scores sqrt((1-p)/p) for p = k/G.  The advantage is
+    unchanged by scaling or shifting the rewards (the "difficulty bias" the
+    page attributes to dividing by sigma)."""
+    s3 = math.sqrt(3.0)
+    A = o.advantage_std(np.array([1, 0, 0, 0.]), 4)
+    assert np.allclose(A, [s3, -1 / s3, -1 / s3, -1 / s3], rtol=0, atol=1e-15), A
+    for k, G in [(1, 8), (3, 8), (5, 16)]:
+        R = np.zeros(G)
+        R[:k] = 1
+        p = k / G
+        A = o.advantage_std(R, G)
+        assert abs(A[0] - math.sqrt((1 - p) / p)) < 1e-14 and abs(A[-1] + math.sqrt(p / (1 - p))) < 1e-14
+    R = np.array([0.3, 1.7, -2.0, 0.5, 4.0, 4.0, 0.0, 1.0])
+    base = o.advantage_std(R, 4)
+    assert np.allclose(o.advantage_std(3 * R + 5, 4), base, rtol=0, atol=1e-13)
+    assert np.allclose(base.reshape(2, 4).sum(1), 0.0, atol=1e-13)
+    assert np.allclose((base.reshape(2, 4) ** 2).mean(1), 1.0, atol=1e-13)  # unit variance
+    # a uniform group: 0 / (0 + std_eps) = 0
+    assert o.advantage_std(np.ones(4), 4, 1e-4).tolist() == [0.0] * 4
+
+
+def pin_seq_mean_aggregation(o):
+    """Section "Dr. GRPO": the original loss averages per response by 1/|o_i|.
+    Two completions of lengths 2 and 4, ratio 1, A = (0.5, -0.5): every token's
+    loss is -A_i, so loss = ((-0.5*2)/2 + (0.5*4)/4) / 2 = 0, and
+    w = -A_i / (N * len_i) = (-0.125, 0.0625)."""
+    lp = np.full((2, 4), -3.0)
+    lens = np.array([2, 4], np.int32)
+    loss, w, ell = o.loss_seq_mean(lp, None, None, np.array([0.5, -0.5]), lens, 0.2, 0.0)
+    assert abs(loss) < 1e-15, loss
+    assert np.allclose(w, [[-0.125, -0.125, 0, 0], [0.0625] * 4], rtol=0, atol=1e-16), w
+    # lengths no longer weight the loss: doubling one response's length with
+    # the same per-token loss leaves its contribution unchanged
+    A = np.array([1.0, 1.0])
+    l1, _, _ = o.loss_seq_mean(lp, None, None, A, np.array([1, 2], np.int32), 0.2, 0.0)
+    l2, _, _ = o.loss_seq_mean(lp, None, None, A, np.array([2, 4], np.int32), 0.2, 0.0)
+    assert abs(l1 - l2) < 1e-15 and abs(l1 + 1.0) < 1e-15
+    # with equal lengths L it equals the token sum over the constant N*L
+    w0 = wl.TINY
+    ids = wl.make_ids(w0)
+    _, ln = o.mask(ids, w0.P, w0.C, w0.eos_id)
+    L = np.full_like(ln, 7)
+    rng = np.random.default_rng(8)
+    lpr = rng.normal(-5, 1, size=(w0.N, w0.C))
+    old = lpr + rng.normal(0, 0.2, size=lpr.shape)
+    Ar = rng.normal(0, 1, size=w0.N)
+    a, wa, _ = o.loss_seq_mean(lpr, old, None, Ar, L, 0.2, 0.0)
+    b, wb, _ = o.loss(lpr, old, None, Ar, L, 0.2, 0.0, float(w0.N * 7))
+    assert abs(a - b) < 1e-14 and np.allclose(wa, wb, rtol=0, atol=1e-16)
+
+
+def pin_dlogits_fd_seq_mean(o):
+    """Finite differences of the per-response-mean loss on the micro batch."""
+    B, G, P, C, V = 2, 2, 2, 4, 8
+    rng = np.random.default_rng(31)
+    z = rng.normal(0, 2, size=(B * G, P + C, V))
+    ids = rng.integers(3, V, size=(B * G, P + C))
+    ids[1, P + 2] = 2
+    _, lens = o.mask(ids, P, C, 2)
+    A = o.advantage_std(np.array([1, 0, 0, 1.]), G, 1e-4)
+    lp, _ = o.logp(z, "f64", P, C, ids, lens)
+    old = lp + _away_from_kinks(rng, lp.shape, 0.2)
+    ref = lp + rng.normal(0, 0.3, lp.shape)
+
+    def f(zz):
+        lpz, _ = o.logp(zz, "f64", P, C, ids, lens)
+        return o.loss_seq_mean(lpz, old, ref, A, lens, 0.2, 0.1)[0]
+
+    lp, ls = o.logp(z, "f64", P, C, ids, lens)
+    _, wt, _ = o.loss_seq_mean(lp, old, ref, A, lens, 0.2, 0.1)
+    an = o.dlogits(z, "f64", P, C, ids, lens, ls, wt)
+    h = 1e-5
+    for i in range(B * G):
+        for r in range(P + C):
+            for v in range(0, V, 3):
+                zp = z.copy()
+                zp[i, r, v] += h
+                zm = z.copy()
+                zm[i, r, v] -= h
+                fd = (f(zp) - f(zm)) / (2 * h)
+                assert abs(fd - an[i, r, v]) <= 1e-9 + 1e-5 * abs(an[i, r, v]), (i, r, v)
+
+
 ALL_CHEAP = [
+    pin_advantage_std_examples, pin_seq_mean_aggregation, pin_dlogits_fd_seq_mean,
     pin_mask_golden, pin_mask_batch_matches_rows, pin_advantage_examples,
     pin_logp_constant_row, pin_logp_two_level, pin_logp_library, pin_logp_token_range,
     pin_logp_shift, pin_surrogate_golden, pin_kl_golden, pin_step0_identity,

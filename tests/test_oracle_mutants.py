@@ -19,7 +19,15 @@ MUTANTS = {
     "mask_no_eos_all_zero": ("j <= first_eos : 1)", "j <= first_eos : 0)"),
     "len_off_by_one": ("first_eos + 1 : C", "first_eos : C"),
     # advantage
-    "advantage_divides_by_G_minus_1": ("sum / (double)G", "sum / (double)(G - 1)"),
+    "advantage_divides_by_G_minus_1": ("mu = sum / (double)G;\n        for (int64_t g = 0; g < G; ++g)\n            A[b * G + g] = R[b * G + g] - mu;",
+                                       "mu = sum / (double)(G - 1);\n        for (int64_t g = 0; g < G; ++g)\n            A[b * G + g] = R[b * G + g] - mu;"),
+    # original GRPO advantage
+    "std_sample_not_population": ("sqrt(ss / (double)G)", "sqrt(ss / (double)(G - 1))"),
+    "std_missing_sqrt": ("double sigma = sqrt(ss / (double)G);", "double sigma = ss / (double)G;"),
+    "std_not_divided": ("(R[b * G + g] - mu) / (sigma + std_eps);", "(R[b * G + g] - mu);"),
+    # per-response mean aggregation
+    "seq_mean_divides_by_C": ("norm * (double)(len[i] > 0 ? len[i] : 1)", "norm * (double)C"),
+    "seq_mean_loss_unweighted": ("(long double)l * ((long double)norm / (long double)denom)", "(long double)l"),
     "advantage_sign": ("R[b * G + g] - mu;", "mu - R[b * G + g];"),
     # compute_logprobs
     "shift_off_by_one": ("i * c->T + (c->P - 1 + t)", "i * c->T + (c->P + t)"),
@@ -35,7 +43,7 @@ MUTANTS = {
     "surrogate_sign": ("double l = -s + beta * k3;", "double l = s + beta * k3;"),
     "kl_dropped": ("double l = -s + beta * k3;", "double l = -s;"),
     "k3_sign": ("k3 = exp(d) - d - 1.0;", "k3 = exp(d) + d - 1.0;"),
-    "norm_per_response": ("norm = (double)N * (double)C;", "norm = (double)N;"),
+    "norm_per_response": ("agg == 0 ? (double)N * (double)C : (double)N", "agg == 0 ? (double)N : (double)N"),
     "mask_off_by_one_in_loss": ("if (t >= len[i]) {\n                if (w)", "if (t > len[i]) {\n                if (w)"),
     # the gradient
     "grad_ignores_clip": ("unclipped <= clipped ? a * r : 0.0", "a * r"),
