@@ -55,6 +55,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-copy-ceiling", action="store_true")
+    p.add_argument("--skip-zero-weight", action="store_true",
+                   help="backward skips reading rows whose gradient weight is exactly 0; "
+                        "the skipped reads are left out of the byte count")
     p.add_argument("--path", choices=["two_pass", "fused"], default="two_pass",
                    help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd")
     return p.parse_args()
@@ -64,18 +67,21 @@ def parse_args():
 # byte counts (stated in the design doc)
 # --------------------------------------------------------------------------
 
-def algorithmic_bytes(w: wl.Workload, t_valid: int) -> dict:
+def algorithmic_bytes(w: wl.Workload, t_valid: int, t_read_bwd: int | None = None) -> dict:
+    """Bytes each call must move.  t_read_bwd: scored rows the backward reads
+    (all of them, unless rows with zero gradient weight are skipped)."""
     e = w.elem_bytes
     N, T, C, V = w.N, w.T, w.C, w.V
     small = 4 * N * C * (3 + (w.old_sigma is not None) + (w.ref_sigma is not None))
+    tr = t_valid if t_read_bwd is None else t_read_bwd
     return {
         # the scored rows read once + ids of scored tokens + logp/lse/w vectors
         "fwd": t_valid * V * e + 8 * t_valid + small,
         # the scored rows read again + every row of dlogits written once
-        "bwd": t_valid * V * e + N * T * V * e + 16 * t_valid,
+        "bwd": tr * V * e + N * T * V * e + 16 * t_valid,
         "mask_adv": 8 * N * C + N * C + 8 * N,
         # the roofline count of the whole method: two reads + one write
-        "step_logits": 2 * t_valid * V * e + N * T * V * e,
+        "step_logits": (t_valid + tr) * V * e + N * T * V * e,
         # the fused call: one read of the scored rows + one write of dlogits
         "fused": t_valid * V * e + N * T * V * e + 8 * t_valid + small,
         "step_logits_fused": t_valid * V * e + N * T * V * e,
@@ -343,6 +349,12 @@ def run_ours(args, w0: wl.Workload):
     old = None if n_old is None else (cur["logp"] + torch.from_numpy(n_old).float().to(dev))
     ref = None if n_ref is None else (cur["logp"] + torch.from_numpy(n_ref).float().to(dev))
     t_valid = int(lens.sum().item())
+    adv_ex, n_contrast = g.grpo_advantage_ex(R, w.G, count_contrast=True)
+    contrast_groups = int(n_contrast.item())
+    # scored rows with a nonzero gradient weight (the only ones a backward
+    # that skips zero-weight rows reads)
+    wfull = g.grpo_loss_fwd(logits, w.P, ids, lens, adv, old, ref, w.eps, w.beta)["w"]
+    t_nonzero = int((wfull != 0).sum().item())
     dlogits = torch.empty_like(logits)
     out = None
     ws = cur["workspace"]
@@ -367,7 +379,8 @@ def run_ours(args, w0: wl.Workload):
         out = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, out, ws)
         if record is not None:
             record[2].record(stream)
-        g.grpo_loss_bwd(logits, w.P, ids, ln, out["lse"], out["w"], None, dlogits)
+        g.grpo_loss_bwd(logits, w.P, ids, ln, out["lse"], out["w"], None, dlogits,
+                        flags=1 if args.skip_zero_weight else None)
         if record is not None:
             record[3].record(stream)
 
@@ -461,7 +474,7 @@ def run_ours(args, w0: wl.Workload):
         peak = peaks.get("hbm_gbs")
         peak_src = "measured" if peak else "fallback"
         peak = peak or FALLBACK_HBM_GBS
-        b = algorithmic_bytes(w, t_valid)
+        b = algorithmic_bytes(w, t_valid, t_nonzero if args.skip_zero_weight else None)
         ms = elapsed / args.steps
         if fused:
             # the fused call: prep + zero-row writer + lse_grad_kernel, timed together
@@ -479,6 +492,9 @@ def run_ours(args, w0: wl.Workload):
             if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
                        "logits_dtype": w.dtype, "valid_tokens_per_rank": t_valid,
+                       "nonzero_weight_tokens_per_rank": t_nonzero,
+                       "groups_with_reward_contrast_per_rank": f"{contrast_groups}/{w.B}",
+                       "skip_zero_weight": bool(args.skip_zero_weight),
                        "l2": f"inputs larger than L2 ({w.logits_bytes / 1e9:.2f} GB logits); "
                              "no flush", "parallelism": f"dp{world} (independent groups)"},
             "path": args.path,

@@ -63,6 +63,24 @@ typedef enum {
 
 typedef enum { GRPO_F32 = 0, GRPO_BF16 = 1 } grpo_dtype;
 
+/* Group advantage ("GRPO" and "Dr. GRPO" sections). */
+typedef enum {
+    GRPO_ADV_DR = 0, /* A = R - mean (Dr. GRPO: no sigma)                        */
+    GRPO_ADV_STD = 1 /* A = (R - mean) / (sigma + std_eps) (original GRPO)       */
+} grpo_adv_mode;
+
+/* Aggregation of the per-token loss ("Dr. GRPO" section). */
+typedef enum {
+    GRPO_AGG_TOKEN_SUM = 0, /* sum over valid tokens / norm (Dr. GRPO; norm <= 0: N*C)   */
+    GRPO_AGG_SEQ_MEAN = 1   /* sum_i (sum_t / len_i) / norm (original GRPO 1/|o_i|;
+                               norm <= 0: N)                                            */
+} grpo_aggregation;
+
+/* grpo_loss_bwd_ex flags. */
+#define GRPO_BWD_SKIP_ZERO_WEIGHT 1u /* a row whose g*w_t is exactly 0 is written with +0 and
+                                        not read (the reads it saves are left out of the
+                                        byte count a caller reports)                       */
+
 /* Static English description of a status code. */
 const char *grpo_status_string(grpo_status status);
 
@@ -94,6 +112,20 @@ grpo_status grpo_mask(const int64_t *input_ids, int64_t N, int64_t P, int64_t C,
  */
 grpo_status grpo_advantage(const float *rewards, int64_t B, int64_t G, float *adv,
                            grpo_stream_t stream);
+
+/*
+ * grpo_advantage_ex -- grpo_advantage with the original GRPO option and the
+ * reward-contrast count.  mode GRPO_ADV_DR is grpo_advantage; GRPO_ADV_STD
+ * divides by sigma + std_eps, sigma = sqrt(sum over the group (R - mean)^2 / G)
+ * (section "GRPO": "Compute the advantage as A_i = (R_i - mu)/sigma inside the
+ * group"); std_eps >= 0 keeps a uniform group at 0.  n_contrast, if not NULL,
+ * is one int32 in device memory that receives the number of groups whose
+ * rewards are not all equal (the analysis page's "useful groups": a uniform
+ * group has no task-reward advantage).
+ */
+grpo_status grpo_advantage_ex(const float *rewards, int64_t B, int64_t G, grpo_adv_mode mode,
+                              float std_eps, float *adv, int32_t *n_contrast,
+                              grpo_stream_t stream);
 
 /*
  * grpo_workspace_size -- bytes of device scratch grpo_loss_fwd needs for N
@@ -173,6 +205,33 @@ grpo_status grpo_loss_fwd_static(const void *logits, grpo_dtype dtype, int64_t N
                                  grpo_stream_t stream);
 
 /*
+ * grpo_loss_fwd_ex -- grpo_loss_fwd with a choice of aggregation:
+ * GRPO_AGG_TOKEN_SUM is grpo_loss_fwd; GRPO_AGG_SEQ_MEAN divides each
+ * completion's token sum by its length, then the sum over completions by norm
+ * (norm <= 0 selects N): the original GRPO's per-response 1/|o_i| mean that
+ * Dr. GRPO replaces (section "Dr. GRPO").  w includes the same weights.
+ */
+grpo_status grpo_loss_fwd_ex(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
+                             int64_t C, int64_t V, const int64_t *input_ids, const int32_t *len,
+                             const float *adv, const float *old_logp, const float *ref_logp,
+                             float eps, float beta, float norm, grpo_aggregation agg,
+                             float *logp, float *lse, float *w, float *loss, void *workspace,
+                             size_t workspace_bytes, grpo_stream_t stream);
+
+/*
+ * grpo_logprobs -- log-probs only, no loss: the no-grad passes of the update
+ * loop ("old_logprobs = policy.logprobs(completions).detach()", the same for
+ * the reference policy; section "Dr. GRPO" pseudo-code and "Putting it
+ * together").  logp, lse [N, C] float32 as in grpo_loss_fwd (0 past each
+ * length); workspace as for grpo_loss_fwd.  grpo_check_error reports token and
+ * length errors.
+ */
+grpo_status grpo_logprobs(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t *input_ids, const int32_t *len, float *logp,
+                          float *lse, void *workspace, size_t workspace_bytes,
+                          grpo_stream_t stream);
+
+/*
  * grpo_loss_bwd -- gradient of (grad_loss * loss) with respect to the logits.
  *
  * Inputs as for grpo_loss_fwd, plus lse and w from it; grad_loss is one
@@ -189,6 +248,18 @@ grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64
                           int64_t V, const int64_t *input_ids, const int32_t *len,
                           const float *lse, const float *w, const float *grad_loss,
                           void *dlogits, grpo_stream_t stream);
+
+/*
+ * grpo_loss_bwd_ex -- grpo_loss_bwd with flags (0 or GRPO_BWD_SKIP_ZERO_WEIGHT).
+ * With GRPO_BWD_SKIP_ZERO_WEIGHT a scored row whose g*w_t is exactly 0 (a
+ * group with no reward contrast and beta == 0, as the analysis page's
+ * "no contrast" case) is written with +0 without reading its logits; its exact
+ * gradient is (+/-)0 everywhere.
+ */
+grpo_status grpo_loss_bwd_ex(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
+                             int64_t C, int64_t V, const int64_t *input_ids, const int32_t *len,
+                             const float *lse, const float *w, const float *grad_loss,
+                             void *dlogits, uint32_t flags, grpo_stream_t stream);
 
 /*
  * grpo_loss_fwd_bwd -- grpo_loss_fwd and grpo_loss_bwd in one pass over each
@@ -211,6 +282,15 @@ grpo_status grpo_loss_fwd_bwd(const void *logits, grpo_dtype dtype, int64_t N, i
                               float eps, float beta, float norm, const float *grad_loss,
                               float *logp, float *lse, float *w, float *loss, void *dlogits,
                               void *workspace, size_t workspace_bytes, grpo_stream_t stream);
+
+/* grpo_loss_fwd_bwd with the aggregation choice of grpo_loss_fwd_ex. */
+grpo_status grpo_loss_fwd_bwd_ex(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, const int64_t *input_ids,
+                                 const int32_t *len, const float *adv, const float *old_logp,
+                                 const float *ref_logp, float eps, float beta, float norm,
+                                 grpo_aggregation agg, const float *grad_loss, float *logp,
+                                 float *lse, float *w, float *loss, void *dlogits, void *workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream);
 
 /*
  * grpo_check_error -- synchronises `stream`, then reports what the kernels of

@@ -23,6 +23,9 @@ STATUS_NAMES = {
     6: "GRPO_ERR_TOKEN_RANGE", 7: "GRPO_ERR_LENGTH_RANGE", 8: "GRPO_ERR_TIMEOUT",
 }
 GRPO_F32, GRPO_BF16 = 0, 1
+GRPO_ADV_DR, GRPO_ADV_STD = 0, 1
+GRPO_AGG_TOKEN_SUM, GRPO_AGG_SEQ_MEAN = 0, 1
+GRPO_BWD_SKIP_ZERO_WEIGHT = 1
 
 
 class GrpoError(RuntimeError):
@@ -54,6 +57,14 @@ def _load():
                                   P], INT),
         "grpo_loss_fwd_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P, P,
                                P, P, SZ, P], INT),
+        "grpo_advantage_ex": ([P, I64, I64, INT, F, P, P, P], INT),
+        "grpo_loss_fwd_ex": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P, P, P, P,
+                              P, SZ, P], INT),
+        "grpo_loss_fwd_bwd_ex": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P, P,
+                                  P, P, P, P, P, SZ, P], INT),
+        "grpo_loss_bwd_ex": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_uint32, P],
+                             INT),
+        "grpo_logprobs": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -131,6 +142,23 @@ def grpo_advantage(rewards: torch.Tensor, G: int, adv=None, stream=None):
     return adv
 
 
+def grpo_advantage_ex(rewards: torch.Tensor, G: int, mode: int = GRPO_ADV_DR, std_eps: float = 0.0,
+                      adv=None, count_contrast: bool = False, stream=None):
+    """Group advantage with the original GRPO option (mode GRPO_ADV_STD) and,
+    if asked, the number of groups with reward contrast (an int32 device
+    tensor).  Returns ``(adv, n_contrast or None)``."""
+    _dev(rewards, "rewards", torch.float32)
+    if adv is None:
+        adv = torch.empty_like(rewards)
+    n = rewards.numel()
+    if G < 1 or n % G:
+        raise ValueError("len(rewards) must be a multiple of G >= 1")
+    cnt = torch.empty((1,), dtype=torch.int32, device=rewards.device) if count_contrast else None
+    _check(_lib.grpo_advantage_ex(_ptr(rewards), n // G, G, int(mode), float(std_eps), _ptr(adv),
+                                  _ptr(cnt), _stream(stream)), "grpo_advantage_ex")
+    return adv, cnt
+
+
 def grpo_workspace_size(N: int, C: int, V: int) -> int:
     out = ctypes.c_size_t(0)
     _check(_lib.grpo_workspace_size(N, C, V, ctypes.byref(out)), "grpo_workspace_size")
@@ -138,7 +166,7 @@ def grpo_workspace_size(N: int, C: int, V: int) -> int:
 
 
 def grpo_loss_fwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
-                  beta=0.0, norm=0.0, out=None, workspace=None, stream=None):
+                  beta=0.0, norm=0.0, out=None, workspace=None, stream=None, agg=None):
     """Per-token log-probs, gradient weights and the Dr. GRPO loss.
 
     ``logits`` [N, P+C, V] float32/bfloat16.  Returns a dict with ``logp``,
@@ -162,12 +190,45 @@ def grpo_loss_fwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     out["workspace"] = workspace
-    _check(_lib.grpo_loss_fwd(
-        _ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
-        _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(out["logp"]),
-        _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _ptr(workspace), workspace.numel(),
-        _stream(stream)), "grpo_loss_fwd")
+    head = (_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
+            _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm))
+    tail = (_ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if agg is None:
+        _check(_lib.grpo_loss_fwd(*head, *tail), "grpo_loss_fwd")
+    else:
+        _check(_lib.grpo_loss_fwd_ex(*head, int(agg), *tail), "grpo_loss_fwd_ex")
     return out
+
+
+def grpo_loss_fwd_ex(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
+                     beta=0.0, norm=0.0, agg=GRPO_AGG_TOKEN_SUM, out=None, workspace=None,
+                     stream=None):
+    """grpo_loss_fwd with the aggregation choice (GRPO_AGG_TOKEN_SUM or
+    GRPO_AGG_SEQ_MEAN)."""
+    return grpo_loss_fwd(logits, P, input_ids, lens, adv, old_logp, ref_logp, eps, beta, norm,
+                         out, workspace, stream, agg=agg)
+
+
+def grpo_logprobs(logits, P, input_ids, lens, out=None, workspace=None, stream=None):
+    """Log-probs only (the no-grad old/reference passes): ``(logp, lse,
+    workspace)``, [N, C] float32, 0 past each length."""
+    _dev(logits, "logits")
+    N, T, V = logits.shape
+    C = T - P
+    _dev(input_ids, "input_ids", torch.int64)
+    _dev(lens, "lens", torch.int32)
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((N, C), dtype=torch.float32, device=dev),
+               torch.empty((N, C), dtype=torch.float32, device=dev))
+    need = grpo_workspace_size(N, C, V)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    _check(_lib.grpo_logprobs(_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids),
+                              _ptr(lens), _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
+                              workspace.numel(), _stream(stream)), "grpo_logprobs")
+    return out[0], out[1], workspace
 
 
 def grpo_loss_fwd_static(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
@@ -199,7 +260,7 @@ def grpo_loss_fwd_static(logits, P, input_ids, lens, adv, old_logp=None, ref_log
 
 
 def grpo_loss_bwd(logits, P, input_ids, lens, lse, w, grad_loss=None, dlogits=None,
-                  stream=None):
+                  stream=None, flags=None):
     """d (grad_loss * loss) / d logits, same shape and dtype as ``logits``."""
     _dev(logits, "logits")
     N, T, V = logits.shape
@@ -211,15 +272,24 @@ def grpo_loss_bwd(logits, P, input_ids, lens, lse, w, grad_loss=None, dlogits=No
     if dlogits is None:
         dlogits = torch.empty_like(logits)
     _dev(dlogits, "dlogits", logits.dtype)
-    _check(_lib.grpo_loss_bwd(_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids),
-                              _ptr(lens), _ptr(lse), _ptr(w), _ptr(grad_loss), _ptr(dlogits),
-                              _stream(stream)), "grpo_loss_bwd")
+    args = (_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(lse),
+            _ptr(w), _ptr(grad_loss), _ptr(dlogits))
+    if flags is None:
+        _check(_lib.grpo_loss_bwd(*args, _stream(stream)), "grpo_loss_bwd")
+    else:
+        _check(_lib.grpo_loss_bwd_ex(*args, int(flags), _stream(stream)), "grpo_loss_bwd_ex")
     return dlogits
+
+
+def grpo_loss_bwd_ex(logits, P, input_ids, lens, lse, w, grad_loss=None, dlogits=None, flags=0,
+                     stream=None):
+    """grpo_loss_bwd with flags (GRPO_BWD_SKIP_ZERO_WEIGHT)."""
+    return grpo_loss_bwd(logits, P, input_ids, lens, lse, w, grad_loss, dlogits, stream, flags)
 
 
 def grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
                       beta=0.0, norm=0.0, grad_loss=None, out=None, workspace=None,
-                      dlogits=None, stream=None):
+                      dlogits=None, stream=None, agg=None):
     """Forward and backward in one pass over each scored row.  Returns the
     dict of :func:`grpo_loss_fwd` plus ``dlogits``."""
     _dev(logits, "logits")
@@ -244,12 +314,23 @@ def grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=N
     _dev(dlogits, "dlogits", logits.dtype)
     out["workspace"] = workspace
     out["dlogits"] = dlogits
-    _check(_lib.grpo_loss_fwd_bwd(
-        _ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
-        _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm), _ptr(grad_loss),
-        _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]), _ptr(dlogits),
-        _ptr(workspace), workspace.numel(), _stream(stream)), "grpo_loss_fwd_bwd")
+    head = (_ptr(logits), _dtype_code(logits), N, P, C, V, _ptr(input_ids), _ptr(lens), _ptr(adv),
+            _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm))
+    tail = (_ptr(grad_loss), _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]),
+            _ptr(out["loss"]), _ptr(dlogits), _ptr(workspace), workspace.numel(), _stream(stream))
+    if agg is None:
+        _check(_lib.grpo_loss_fwd_bwd(*head, *tail), "grpo_loss_fwd_bwd")
+    else:
+        _check(_lib.grpo_loss_fwd_bwd_ex(*head, int(agg), *tail), "grpo_loss_fwd_bwd_ex")
     return out
+
+
+def grpo_loss_fwd_bwd_ex(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None, eps=0.2,
+                         beta=0.0, norm=0.0, agg=GRPO_AGG_TOKEN_SUM, grad_loss=None, out=None,
+                         workspace=None, dlogits=None, stream=None):
+    """grpo_loss_fwd_bwd with the aggregation choice."""
+    return grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp, ref_logp, eps, beta, norm,
+                             grad_loss, out, workspace, dlogits, stream, agg=agg)
 
 
 def grpo_check_error(workspace, stream=None) -> int:

@@ -121,7 +121,21 @@ grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* ad
   if (rewards == nullptr || adv == nullptr) return GRPO_ERR_INVALID_ARG;
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4)) return GRPO_ERR_MISALIGNED;
-  return from_cuda(launch_advantage(rewards, B, G, adv, (cudaStream_t)stream));
+  return from_cuda(launch_advantage(rewards, B, G, 0, 0.f, adv, nullptr, (cudaStream_t)stream));
+}
+
+grpo_status grpo_advantage_ex(const float* rewards, int64_t B, int64_t G, grpo_adv_mode mode,
+                              float std_eps, float* adv, int32_t* n_contrast,
+                              grpo_stream_t stream) {
+  if (B < 0 || G < 1) return GRPO_ERR_INVALID_ARG;
+  if (mode != GRPO_ADV_DR && mode != GRPO_ADV_STD) return GRPO_ERR_UNSUPPORTED;
+  if (!(std_eps >= 0.f) || isinf(std_eps)) return GRPO_ERR_INVALID_ARG;
+  if (B > 0 && (rewards == nullptr || adv == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
+  if (!aligned(rewards, 4) || !aligned(adv, 4) || !aligned(n_contrast, 4))
+    return GRPO_ERR_MISALIGNED;
+  return from_cuda(launch_advantage(rewards, B, G, (int)mode, std_eps, adv, n_contrast,
+                                    (cudaStream_t)stream));
 }
 
 grpo_status grpo_workspace_size(int64_t N, int64_t C, int64_t V, size_t* bytes) {
@@ -131,23 +145,30 @@ grpo_status grpo_workspace_size(int64_t N, int64_t C, int64_t V, size_t* bytes) 
   return GRPO_OK;
 }
 
-grpo_status grpo_loss_fwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+}  // extern "C"
+
+namespace {
+
+// mode 0: full forward; 1: log-probs only (no loss, w or adv needed).
+grpo_status loss_fwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
                           int64_t V, const int64_t* input_ids, const int32_t* len,
                           const float* adv, const float* old_logp, const float* ref_logp,
-                          float eps, float beta, float norm, float* logp, float* lse, float* w,
-                          float* loss, void* workspace, size_t workspace_bytes,
-                          grpo_stream_t stream) {
+                          float eps, float beta, float norm, int agg, float* logp, float* lse,
+                          float* w, float* loss, void* workspace, size_t workspace_bytes,
+                          grpo_stream_t stream, int mode) {
   grpo_status s = check_shapes(dtype, N, P, C, V);
   if (s != GRPO_OK) return s;
   if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) || isinf(norm))
     return GRPO_ERR_INVALID_ARG;
-  if (loss == nullptr || workspace == nullptr) return GRPO_ERR_INVALID_ARG;
-  if (N > 0 && (len == nullptr || adv == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (agg != 0 && agg != 1) return GRPO_ERR_UNSUPPORTED;
+  if ((mode == 0 && loss == nullptr) || workspace == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && (len == nullptr || (mode == 0 && adv == nullptr))) return GRPO_ERR_INVALID_ARG;
   if (N > 0 && C > 0 &&
       (logits == nullptr || input_ids == nullptr || logp == nullptr || lse == nullptr ||
-       w == nullptr))
+       (mode == 0 && w == nullptr)))
     return GRPO_ERR_INVALID_ARG;
-  if (beta != 0.f && ref_logp == nullptr && N > 0 && C > 0) return GRPO_ERR_INVALID_ARG;
+  if (mode == 0 && beta != 0.f && ref_logp == nullptr && N > 0 && C > 0)
+    return GRPO_ERR_INVALID_ARG;
   const size_t esize = dtype == GRPO_F32 ? 4 : 2;
   if (!aligned(logits, esize) || !aligned(input_ids, 8) || !aligned(len, 4) ||
       !aligned(adv, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(logp, 4) ||
@@ -170,6 +191,7 @@ grpo_status grpo_loss_fwd(const void* logits, grpo_dtype dtype, int64_t N, int64
   a.eps = eps;
   a.beta = beta;
   a.norm = norm;
+  a.agg = agg;
   a.logp = logp;
   a.lse = lse;
   a.w = w;
@@ -181,15 +203,52 @@ grpo_status grpo_loss_fwd(const void* logits, grpo_dtype dtype, int64_t N, int64
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
   // the prep kernel also resets the error flags and the reduction ticket
   if ((e = launch_prep(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
-  if (N == 0 || C == 0) return from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st));
+  if (N == 0 || C == 0)
+    return mode == 0 ? from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st)) : GRPO_OK;
   if ((e = launch_lse_gather(a, d, st)) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (mode == 1) return from_cuda(launch_mask_fill(a, st));
   return from_cuda(launch_surrogate(a, st));
 }
 
-grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_loss_fwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
                           int64_t V, const int64_t* input_ids, const int32_t* len,
-                          const float* lse, const float* w, const float* grad_loss,
-                          void* dlogits, grpo_stream_t stream) {
+                          const float* adv, const float* old_logp, const float* ref_logp,
+                          float eps, float beta, float norm, float* logp, float* lse, float* w,
+                          float* loss, void* workspace, size_t workspace_bytes,
+                          grpo_stream_t stream) {
+  return loss_fwd_impl(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                       beta, norm, 0, logp, lse, w, loss, workspace, workspace_bytes, stream, 0);
+}
+
+grpo_status grpo_loss_fwd_ex(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                             int64_t C, int64_t V, const int64_t* input_ids, const int32_t* len,
+                             const float* adv, const float* old_logp, const float* ref_logp,
+                             float eps, float beta, float norm, grpo_aggregation agg,
+                             float* logp, float* lse, float* w, float* loss, void* workspace,
+                             size_t workspace_bytes, grpo_stream_t stream) {
+  return loss_fwd_impl(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                       beta, norm, (int)agg, logp, lse, w, loss, workspace, workspace_bytes,
+                       stream, 0);
+}
+
+grpo_status grpo_logprobs(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t* input_ids, const int32_t* len, float* logp,
+                          float* lse, void* workspace, size_t workspace_bytes,
+                          grpo_stream_t stream) {
+  return loss_fwd_impl(logits, dtype, N, P, C, V, input_ids, len, nullptr, nullptr, nullptr, 0.f,
+                       0.f, 0.f, 0, logp, lse, nullptr, nullptr, workspace, workspace_bytes,
+                       stream, 1);
+}
+
+grpo_status grpo_loss_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                             int64_t C, int64_t V, const int64_t* input_ids, const int32_t* len,
+                             const float* lse, const float* w, const float* grad_loss,
+                             void* dlogits, uint32_t flags, grpo_stream_t stream) {
+  if (flags & ~(uint32_t)GRPO_BWD_SKIP_ZERO_WEIGHT) return GRPO_ERR_UNSUPPORTED;
   grpo_status s = check_shapes(dtype, N, P, C, V);
   if (s != GRPO_OK) return s;
   if (N == 0) return GRPO_OK;
@@ -218,17 +277,28 @@ grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64
   a.w = w;
   a.grad = grad_loss;
   a.dlogits = dlogits;
+  a.skip_zero_weight = (flags & GRPO_BWD_SKIP_ZERO_WEIGHT) != 0;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
   return from_cuda(launch_dlogits(a, d, (cudaStream_t)stream));
 }
 
-grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
-                              int64_t C, int64_t V, const int64_t* input_ids, const int32_t* len,
-                              const float* adv, const float* old_logp, const float* ref_logp,
-                              float eps, float beta, float norm, const float* grad_loss,
-                              float* logp, float* lse, float* w, float* loss, void* dlogits,
-                              void* workspace, size_t workspace_bytes, grpo_stream_t stream) {
+grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                          int64_t V, const int64_t* input_ids, const int32_t* len,
+                          const float* lse, const float* w, const float* grad_loss,
+                          void* dlogits, grpo_stream_t stream) {
+  return grpo_loss_bwd_ex(logits, dtype, N, P, C, V, input_ids, len, lse, w, grad_loss, dlogits, 0u,
+                          stream);
+}
+
+grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, const int64_t* input_ids,
+                                 const int32_t* len, const float* adv, const float* old_logp,
+                                 const float* ref_logp, float eps, float beta, float norm,
+                                 grpo_aggregation agg, const float* grad_loss, float* logp,
+                                 float* lse, float* w, float* loss, void* dlogits, void* workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream) {
+  if (agg != GRPO_AGG_TOKEN_SUM && agg != GRPO_AGG_SEQ_MEAN) return GRPO_ERR_UNSUPPORTED;
   grpo_status s = check_shapes(dtype, N, P, C, V);
   if (s != GRPO_OK) return s;
   const size_t esize = dtype == GRPO_F32 ? 4 : 2;
@@ -243,8 +313,8 @@ grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, i
   const bool same_phase = ((reinterpret_cast<uintptr_t>(logits) ^
                             reinterpret_cast<uintptr_t>(dlogits)) & 15u) == 0;
   if (N == 0 || C == 0 || !same_phase) {  // nothing to fuse, or no common vector grid
-    s = grpo_loss_fwd(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
-                      beta, norm, logp, lse, w, loss, workspace, workspace_bytes, stream);
+    s = grpo_loss_fwd_ex(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                         beta, norm, agg, logp, lse, w, loss, workspace, workspace_bytes, stream);
     if (s != GRPO_OK) return s;
     return grpo_loss_bwd(logits, dtype, N, P, C, V, input_ids, len, lse, w, grad_loss, dlogits,
                          stream);
@@ -278,6 +348,7 @@ grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, i
   a.eps = eps;
   a.beta = beta;
   a.norm = norm;
+  a.agg = (int)agg;
   a.logp = logp;
   a.lse = lse;
   a.w = w;
@@ -296,12 +367,24 @@ grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, i
   b.w = w;
   b.grad = grad_loss;
   b.dlogits = dlogits;
+  b.skip_zero_weight = false;
   const cudaStream_t st = (cudaStream_t)stream;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (launch_zero_rows(b, d, st, logp, lse, w) != cudaSuccess) return GRPO_ERR_CUDA;
   return from_cuda(launch_lse_grad(a, b, d, st));
+}
+
+grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                              int64_t C, int64_t V, const int64_t* input_ids, const int32_t* len,
+                              const float* adv, const float* old_logp, const float* ref_logp,
+                              float eps, float beta, float norm, const float* grad_loss,
+                              float* logp, float* lse, float* w, float* loss, void* dlogits,
+                              void* workspace, size_t workspace_bytes, grpo_stream_t stream) {
+  return grpo_loss_fwd_bwd_ex(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp,
+                              eps, beta, norm, GRPO_AGG_TOKEN_SUM, grad_loss, logp, lse, w, loss,
+                              dlogits, workspace, workspace_bytes, stream);
 }
 
 grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {

@@ -451,7 +451,8 @@ struct DeviceInfo {
 
 cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int64_t eos,
                         uint8_t* mask, int32_t* len, cudaStream_t st);
-cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, float* adv, cudaStream_t st);
+cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, int mode, float std_eps,
+                             float* adv, int32_t* n_contrast, cudaStream_t st);
 
 struct FwdArgs {
   const void* logits;
@@ -463,15 +464,22 @@ struct FwdArgs {
   const float* old_logp;
   const float* ref_logp;
   float eps, beta, norm;
+  int agg;  // 0: token sum / norm (Dr. GRPO); 1: per-response mean / norm
   float* logp;
   float* lse;
   float* w;
   float* loss;
   void* ws;
 };
+// The constant the token sum is divided by when norm <= 0.
+inline double default_norm(const FwdArgs& a) {
+  return a.norm > 0.f ? (double)a.norm : (a.agg == 0 ? (double)a.N * (double)a.C : (double)a.N);
+}
 cudaError_t launch_prep(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st);
 cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st);
+// logp = lse = 0 past each length (the log-prob-only pass).
+cudaError_t launch_mask_fill(const FwdArgs& a, cudaStream_t st);
 
 struct BwdArgs {
   const void* logits;
@@ -483,6 +491,7 @@ struct BwdArgs {
   const float* w;
   const float* grad;
   void* dlogits;
+  bool skip_zero_weight;  // rows with g*w == 0: zeros, logits not read
 };
 cudaError_t launch_dlogits(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st);
 // Store-only pass of the fused path: zero dlogits rows and masked logp/lse/w.

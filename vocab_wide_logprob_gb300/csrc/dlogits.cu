@@ -34,6 +34,7 @@ struct DlParams {
   float* logp_out;
   float* lse_out;
   float* w_out;
+  int skip_zero_weight;  // a scored row with g*w == 0 is written with zeros, not read
 };
 
 // kZeroOnly: write only the rows that score nothing (and the masked
@@ -82,7 +83,13 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
     const int64_t b = a + nvec * EPV;
     uint4* ovp = reinterpret_cast<uint4*>(orow + a);
 
-    if (t < 0 || t >= L) {  // row scores nothing: zeros, logits not read
+    bool zero_row = t < 0 || t >= L;  // the row scores nothing
+    float gw = 0.f;
+    if (!zero_row && !kZeroOnly) {
+      gw = g * __ldg(p.w + i * p.C + t);
+      if (p.skip_zero_weight && gw == 0.f) zero_row = true;  // its gradient is 0
+    }
+    if (zero_row) {  // zeros, logits not read
       for (int64_t k = tid; k < nvec; k += kThreads) st_stream(ovp + k, zero);
       if (tid < a - v0) E::store1(orow + v0 + tid, 0.f);
       if (tid >= 32 && tid - 32 < v1 - b) E::store1(orow + b + (tid - 32), 0.f);
@@ -90,7 +97,6 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
     }
     if (kZeroOnly) continue;
     const int64_t k_tok = i * p.C + t;
-    const float gw = g * __ldg(p.w + k_tok);
     const float ngw = -gw;
     const float lse_t = __ldg(p.lse + k_tok);
     const float lseL = lse_t * kLog2e;
@@ -169,6 +175,7 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st, flo
   p.logp_out = logp;
   p.lse_out = lse;
   p.w_out = w_out;
+  p.skip_zero_weight = a.skip_zero_weight ? 1 : 0;
   p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT", 8);
   p.chunk = ((a.V + p.split - 1) / p.split + EPV - 1) / EPV * EPV;
   // An oversubscribed grid (many more CTAs than fit at once, grid-stride over

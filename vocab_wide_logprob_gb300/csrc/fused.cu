@@ -52,6 +52,7 @@ struct FusedParams {
   const float* ref_logp;
   const float* grad;       // device scalar or nullptr (1)
   float eps, beta;
+  int agg;
   double norm;
   float* logp;
   float* lse;
@@ -358,8 +359,10 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
             token_terms(lp, p.adv[i], p.old_logp != nullptr,
                         p.old_logp != nullptr ? p.old_logp[o] : 0.f, p.beta,
                         p.beta != 0.f ? p.ref_logp[o] : 0.f, p.eps);
-        wv = (float)((double)tt.w / p.norm);
-        if (rank == 0) loss_acc += (double)tt.ell;
+        const double len_i = (double)(off[i + 1] - off[i]);
+        const double denom = p.agg == 0 ? p.norm : p.norm * len_i;
+        wv = (float)((double)tt.w / denom);
+        if (rank == 0) loss_acc += p.agg == 0 ? (double)tt.ell : (double)tt.ell / len_i;
       } else {  // y outside [0, V)
         lp = __int_as_float(0x7fc00000);
         wv = lp;
@@ -477,7 +480,8 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   p.grad = bw.grad;
   p.eps = a.eps;
   p.beta = a.beta;
-  p.norm = a.norm > 0.f ? (double)a.norm : (double)a.N * (double)a.C;
+  p.agg = a.agg;
+  p.norm = default_norm(a);
   p.logp = a.logp;
   p.lse = a.lse;
   p.w = a.w;

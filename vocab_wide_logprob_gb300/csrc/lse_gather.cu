@@ -561,4 +561,32 @@ cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_
   return a.dtype == 0 ? launch_t<float>(a, d, st) : launch_t<uint16_t>(a, d, st);
 }
 
+// logp = lse = 0 at positions past each completion's (clamped) length.
+__global__ void __launch_bounds__(kThreads) mask_fill_kernel(const int32_t* __restrict__ lens,
+                                                             int64_t N, int64_t C,
+                                                             float* __restrict__ logp,
+                                                             float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < N * C;
+       k += (int64_t)gridDim.x * kThreads) {
+    const int64_t i = k / C;
+    if (k - i * C >= lens[i]) {
+      logp[k] = 0.f;
+      lse[k] = 0.f;
+    }
+  }
+}
+
+cudaError_t launch_mask_fill(const FwdArgs& a, cudaStream_t st) {
+  const int64_t NC = a.N * a.C;
+  if (NC == 0) return cudaSuccess;
+  const WsLayout l = ws_layout(a.N);
+  const char* ws = static_cast<const char*>(a.ws);
+  int64_t blocks = (NC + kThreads - 1) / kThreads;
+  if (blocks > 1024) blocks = 1024;
+  return launch_pdl(mask_fill_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1,
+                    reinterpret_cast<const int32_t*>(ws + l.lens), a.N, a.C, a.logp, a.lse);
+}
+
 }  // namespace grpo

@@ -56,9 +56,15 @@ cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int
 // One warp per group.  Lane l sums rewards l, l+32, ... of the group in that
 // order; a butterfly of shuffles then leaves the same total in every lane
 // (each step adds the same two operands in both partner lanes).
+//   mode 0 (Dr. GRPO):      A = R - mu
+//   mode 1 (original GRPO): A = (R - mu) / (sigma + std_eps), sigma over the G
+//                           rewards (dividing by G), IEEE sqrt and division
+// n_contrast (optional) counts the groups whose rewards are not all equal.
 __global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __restrict__ R,
-                                                             int64_t B, int64_t G,
-                                                             float* __restrict__ adv) {
+                                                             int64_t B, int64_t G, int mode,
+                                                             float std_eps,
+                                                             float* __restrict__ adv,
+                                                             int32_t* __restrict__ n_contrast) {
   pdl_wait();
   pdl_trigger();
   const int64_t b = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -70,13 +76,32 @@ __global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __rest
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   // IEEE division: k/G is exact for binary rewards and power-of-two G
   const float mu = __fdiv_rn(sum, (float)G);
-  for (int64_t g = lane; g < G; g += 32) adv[b * G + g] = r[g] - mu;
+  float scale = 1.f;
+  if (mode == 1) {
+    float ss = 0.f;
+    for (int64_t g = lane; g < G; g += 32) ss += (r[g] - mu) * (r[g] - mu);
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    scale = __fadd_rn(__fsqrt_rn(__fdiv_rn(ss, (float)G)), std_eps);
+  }
+  for (int64_t g = lane; g < G; g += 32)
+    adv[b * G + g] = mode == 1 ? __fdiv_rn(r[g] - mu, scale) : r[g] - mu;
+  if (n_contrast != nullptr) {
+    bool differs = false;
+    for (int64_t g = lane; g < G; g += 32) differs |= r[g] != r[0];
+    if (__any_sync(0xffffffffu, differs) && lane == 0) atomicAdd(n_contrast, 1);
+  }
 }
 
-cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, float* adv, cudaStream_t st) {
-  if (B == 0) return cudaSuccess;
+cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, int mode, float std_eps,
+                             float* adv, int32_t* n_contrast, cudaStream_t st) {
+  if (B == 0) return n_contrast ? cudaMemsetAsync(n_contrast, 0, sizeof(int32_t), st) : cudaSuccess;
+  if (n_contrast != nullptr) {
+    cudaError_t e = cudaMemsetAsync(n_contrast, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+  }
   const unsigned blocks = (unsigned)((B + kWarps - 1) / kWarps);
-  return launch_pdl(advantage_kernel, dim3(blocks), dim3(kThreads), 0, st, 1, R, B, G, adv);
+  return launch_pdl(advantage_kernel, dim3(blocks), dim3(kThreads), 0, st, 1, R, B, G, mode,
+                    std_eps, adv, n_contrast);
 }
 
 }  // namespace grpo

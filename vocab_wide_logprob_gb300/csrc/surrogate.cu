@@ -26,6 +26,7 @@ struct SurParams {
   const float* old_logp;
   const float* ref_logp;
   float eps, beta;
+  int agg;
   double norm;
   float* logp;
   float* lse;
@@ -57,9 +58,11 @@ __global__ void __launch_bounds__(kThreads) surrogate_kernel(const SurParams p) 
         token_terms(lp, p.adv[i], p.old_logp != nullptr,
                     p.old_logp != nullptr ? p.old_logp[k] : 0.f, p.beta,
                     p.beta != 0.f ? p.ref_logp[k] : 0.f, p.eps);
-    p.w[k] = (float)((double)tt.w / p.norm);
-    const float ell = tt.ell;
-    acc += (double)ell;
+    // the constant this token is divided by; the per-response mean also
+    // divides by the completion's length
+    const double denom = p.agg == 0 ? p.norm : p.norm * (double)p.lens[i];
+    p.w[k] = (float)((double)tt.w / denom);
+    acc += p.agg == 0 ? (double)tt.ell : (double)tt.ell / (double)p.lens[i];
   }
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) s_red[warp] = acc;
@@ -104,7 +107,8 @@ cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st) {
   p.ref_logp = a.ref_logp;
   p.eps = a.eps;
   p.beta = a.beta;
-  p.norm = a.norm > 0.f ? (double)a.norm : (double)a.N * (double)a.C;
+  p.agg = a.agg;
+  p.norm = default_norm(a);
   p.logp = a.logp;
   p.lse = a.lse;
   p.w = a.w;
