@@ -58,8 +58,12 @@ def parse_args():
     p.add_argument("--skip-zero-weight", action="store_true",
                    help="backward skips reading rows whose gradient weight is exactly 0; "
                         "the skipped reads are left out of the byte count")
-    p.add_argument("--path", choices=["two_pass", "fused"], default="two_pass",
-                   help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd")
+    p.add_argument("--path", choices=["two_pass", "fused", "lmhead_logprobs"], default="two_pass",
+                   help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd; "
+                        "lmhead_logprobs: log-probs from hidden states with the LM-head "
+                        "projection on the tensor cores (the no-grad old/reference pass)")
+    p.add_argument("--hidden", type=int, default=896,
+                   help="hidden size for --path lmhead_logprobs (Qwen2.5-0.5B: 896)")
     return p.parse_args()
 
 
@@ -522,11 +526,72 @@ def run_ours(args, w0: wl.Workload):
         dist.destroy_process_group()
 
 
+def run_lmhead(args, w: wl.Workload):
+    """Times grpo_mask + grpo_lmhead_logprobs: log-probs of the sampled tokens
+    from hidden states [N, P+C, d] and a [V, d] LM head, logits never
+    materialised.  Roofline: tensor (2 * T_valid * V * d FLOPs per call)."""
+    import torch
+    from vocab_wide_logprob_gb300 import build as libbuild
+    libbuild.build()
+    from vocab_wide_logprob_gb300 import _native as g
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    d = args.hidden
+    hidden = wl.make_hidden(w, d, "cuda")
+    weight = wl.make_lm_head(w, d, "cuda")
+    ids = torch.from_numpy(wl.make_ids(w)).to(dev)
+    mask, lens = g.grpo_mask(ids, w.P, w.C, w.eos_id)
+    t_valid = int(lens.sum().item())
+    lp, lse, ws = g.grpo_lmhead_logprobs(hidden, weight, w.P, ids, lens)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
+        g.grpo_lmhead_logprobs(hidden, weight, w.P, ids, lens, (lp, lse), ws)
+
+    sampler = None if args.no_clocks else ClockSampler(None)
+    if sampler is not None:
+        time.sleep(1.0)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    assert g.grpo_check_error(ws) == 0
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
+    ms = a.elapsed_time(b) / args.steps
+    flops = 2.0 * t_valid * w.V * d
+    peaks = measured_peaks()
+    peak = peaks.get("bf16_tflops") or 1900.0
+    tflops = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "completion tokens/s, log-probs from hidden states (LM head fused, no grad)",
+        "value": t_valid / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "path": "lmhead_logprobs",
+        "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
+                   "hidden": d, "valid_tokens": t_valid},
+        "roofline": {"kernel": "lmhead_lse_kernel (+ gather, merge)", "bound": "tensor",
+                     "achieved": tflops, "peak": peak,
+                     "peak_source": "measured" if peaks.get("bf16_tflops") else "fallback",
+                     "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None},
+        "gpu_launches": 5 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     w = wl.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.path == "lmhead_logprobs":
+        run_lmhead(args, w)
     else:
         run_ours(args, w)
 

@@ -293,6 +293,28 @@ grpo_status grpo_loss_fwd_bwd_ex(const void *logits, grpo_dtype dtype, int64_t N
                                  size_t workspace_bytes, grpo_stream_t stream);
 
 /*
+ * grpo_lmhead_logprobs -- log-probs of the sampled tokens straight from the
+ * policy's last hidden states, with the LM-head projection fused in: the
+ * logits (hidden x W^T, "model(...).logits" in "compute_logprobs") are formed
+ * tile by tile on the tensor cores and reduced on the fly, never written to
+ * memory.  Same results as grpo_logprobs on logits = hidden x W^T computed in
+ * float32 (up to the order of the float32 sums).
+ *
+ * hidden [N, P+C, d] bfloat16 (row P-1+t of sequence i scores token t);
+ * weight [V, d] bfloat16 (the LM head, row v = the output embedding of token
+ * v); both 16-byte aligned; d a multiple of 64.  input_ids, len, logp, lse as
+ * for grpo_logprobs (0 past each length).  workspace: at least
+ * grpo_lmhead_workspace_size bytes (it holds a dense copy of the scored rows'
+ * hidden states, 2*d bytes per completion token, and a few KB of partials).
+ */
+grpo_status grpo_lmhead_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
+                                       size_t *bytes);
+grpo_status grpo_lmhead_logprobs(const void *hidden, const void *weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
+                                 const int32_t *len, float *logp, float *lse, void *workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream);
+
+/*
  * grpo_check_error -- synchronises `stream`, then reports what the kernels of
  * the most recent grpo_loss_fwd on `workspace` recorded: GRPO_OK,
  * GRPO_ERR_TOKEN_RANGE (a scored id outside [0, V); its logp and lse are NaN),

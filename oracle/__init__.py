@@ -186,6 +186,34 @@ class Oracle:
                                     _ptr(lp), _ptr(ls)), "logp")
         return lp, ls
 
+    def lmhead_logp(self, hidden, weight, P: int, C: int, ids, lens):
+        """Log-probs from hidden states [N, P+C, d] and the LM head [V, d]
+        ("model(...).logits" = hidden x W^T, then "compute_logprobs"): the
+        scored rows' logits in float64 (numpy matmul of the exactly widened
+        bf16 inputs), then :meth:`logp_rows`.  Inputs are uint16 bf16 bit
+        patterns or float arrays.  Returns ``(logp, lse)`` [N, C]."""
+        def wide(x):
+            x = np.asarray(x)
+            if x.dtype == np.uint16:
+                return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            return x.astype(np.float64)
+        H = wide(hidden)
+        W = wide(weight)
+        N = H.shape[0]
+        ids = np.asarray(ids, dtype=np.int64)
+        lens = np.asarray(lens, dtype=np.int32)
+        lp = np.zeros((N, C))
+        ls = np.zeros((N, C))
+        for i in range(N):
+            L = int(lens[i])
+            if L == 0:
+                continue
+            z = H[i, P - 1:P - 1 + L] @ W.T
+            a, b = self.logp_rows(z, "f64", ids[i, P:P + L])
+            lp[i, :L] = a
+            ls[i, :L] = b
+        return lp, ls
+
     # -- "The loss" ------------------------------------------------------------
     def loss_seq_mean(self, logp, old, ref, adv, lens, eps: float, beta: float,
                       norm: float = 0.0):
@@ -279,6 +307,10 @@ def logp(*a, **k):
 
 def loss(*a, **k):
     return default().loss(*a, **k)
+
+
+def lmhead_logp(*a, **k):
+    return default().lmhead_logp(*a, **k)
 
 
 def dlogits_row(*a, **k):

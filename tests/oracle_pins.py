@@ -519,7 +519,31 @@ def pin_dlogits_fd_seq_mean(o):
                 assert abs(fd - an[i, r, v]) <= 1e-9 + 1e-5 * abs(an[i, r, v]), (i, r, v)
 
 
+def pin_lmhead_reduces_to_logits(o):
+    """With W = I (d = V) the projection is the identity: the LM-head log-probs
+    equal the log-probs of the hidden states taken as logits; permuting W's
+    rows permutes the vocabulary, so relabelling the ids gives the same
+    log-probs."""
+    N, P, C, V = 3, 4, 6, 16
+    rng = np.random.default_rng(41)
+    H = rng.normal(0, 2, size=(N, P + C, V))
+    ids = rng.integers(3, V, size=(N, P + C))
+    ids[1, P + 3] = 2
+    _, lens = o.mask(ids, P, C, 2)
+    a, la = o.lmhead_logp(H, np.eye(V), P, C, ids, lens)
+    b, lb = o.logp(H, "f64", P, C, ids, lens)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+    perm = rng.permutation(V)
+    W = np.eye(V)[perm]            # row v of W picks coordinate perm[v]
+    inv = np.argsort(perm)         # token u's logit is coordinate perm[u]...
+    ids2 = ids.copy()
+    ids2[:, P:] = inv[ids[:, P:]]  # ...so ask for the token whose row is the old one
+    c, _ = o.lmhead_logp(H, W, P, C, ids2, lens)
+    assert np.allclose(c, b, rtol=0, atol=1e-12)
+
+
 ALL_CHEAP = [
+    pin_lmhead_reduces_to_logits,
     pin_advantage_std_examples, pin_seq_mean_aggregation, pin_dlogits_fd_seq_mean,
     pin_mask_golden, pin_mask_batch_matches_rows, pin_advantage_examples,
     pin_logp_constant_row, pin_logp_two_level, pin_logp_library, pin_logp_token_range,

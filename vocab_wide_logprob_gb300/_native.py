@@ -65,6 +65,8 @@ def _load():
         "grpo_loss_bwd_ex": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_uint32, P],
                              INT),
         "grpo_logprobs": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
+        "grpo_lmhead_workspace_size": ([I64, I64, I64, I64, ctypes.POINTER(SZ)], INT),
+        "grpo_lmhead_logprobs": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -331,6 +333,35 @@ def grpo_loss_fwd_bwd_ex(logits, P, input_ids, lens, adv, old_logp=None, ref_log
     """grpo_loss_fwd_bwd with the aggregation choice."""
     return grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp, ref_logp, eps, beta, norm,
                              grad_loss, out, workspace, dlogits, stream, agg=agg)
+
+
+def grpo_lmhead_logprobs(hidden, weight, P, input_ids, lens, out=None, workspace=None,
+                         stream=None):
+    """Log-probs from hidden states [N, P+C, d] and the LM head [V, d] (both
+    bfloat16), with the projection fused on the tensor cores.  Returns
+    ``(logp, lse, workspace)``."""
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(weight, "weight", torch.bfloat16)
+    _dev(input_ids, "input_ids", torch.int64)
+    _dev(lens, "lens", torch.int32)
+    N, T, d = hidden.shape
+    V = weight.shape[0]
+    C = T - P
+    if weight.shape[1] != d:
+        raise ValueError("weight must be [V, d]")
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty((N, C), dtype=torch.float32, device=dev),
+               torch.empty((N, C), dtype=torch.float32, device=dev))
+    need = ctypes.c_size_t(0)
+    _check(_lib.grpo_lmhead_workspace_size(N, C, V, d, ctypes.byref(need)),
+           "grpo_lmhead_workspace_size")
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
+    _check(_lib.grpo_lmhead_logprobs(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
+                                     _ptr(lens), _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "grpo_lmhead_logprobs")
+    return out[0], out[1], workspace
 
 
 def grpo_check_error(workspace, stream=None) -> int:

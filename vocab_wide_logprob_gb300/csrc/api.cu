@@ -387,6 +387,53 @@ grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, i
                               dlogits, workspace, workspace_bytes, stream);
 }
 
+grpo_status grpo_lmhead_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
+                                       size_t* bytes) {
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1 || d < 64 || d % 64 != 0)
+    return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  *bytes = lm_layout(N, C, d, dev.sms).total;
+  return GRPO_OK;
+}
+
+grpo_status grpo_lmhead_logprobs(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                 const int32_t* len, float* logp, float* lse, void* workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream) {
+  grpo_status s = check_shapes(GRPO_BF16, N, P, C, V);
+  if (s != GRPO_OK) return s;
+  if (d < 64 || d % 64 != 0) return GRPO_ERR_UNSUPPORTED;
+  if (V > (int64_t)INT32_MAX - 256 || mul3(N, P + C, d) < 0) return GRPO_ERR_UNSUPPORTED;
+  if (workspace == nullptr || (N > 0 && len == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 &&
+      (hidden == nullptr || weight == nullptr || input_ids == nullptr || logp == nullptr ||
+       lse == nullptr))
+    return GRPO_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(input_ids, 8) || !aligned(len, 4) ||
+      !aligned(logp, 4) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return GRPO_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (workspace_bytes < lm_layout(N, C, d, dev.sms).total) return GRPO_ERR_WORKSPACE;
+  FwdArgs a = {};
+  a.dtype = 1;
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.ids = input_ids;
+  a.len = len;
+  a.logp = logp;
+  a.lse = lse;
+  a.ws = workspace;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (N == 0 || C == 0) return GRPO_OK;
+  return from_cuda(launch_lmhead(hidden, weight, a, d, dev, st));
+}
+
 grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
   if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
   uint32_t flags = 0;

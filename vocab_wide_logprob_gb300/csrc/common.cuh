@@ -504,4 +504,16 @@ cudaError_t launch_lse_grad(const FwdArgs& a, const BwdArgs& b, const DeviceInfo
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceInfo& d,
                         cudaStream_t st);
 
+// LM-head log-probs (tensor cores): workspace beyond the base layout holds a
+// dense copy of the scored rows' hidden states and the per-item partials.
+struct LmLayout {
+  size_t dense;     // bf16 [N*C, d]
+  size_t partials;  // float4 [items][128]
+  size_t total;
+};
+LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms);
+// After launch_prep: gather, tensor-core log-sum-exp, merge.
+cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs& a, int64_t d,
+                          const DeviceInfo& dev, cudaStream_t st);
+
 }  // namespace grpo

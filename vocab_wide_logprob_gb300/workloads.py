@@ -218,6 +218,24 @@ def fill_logits_cuda(w: Workload, out) -> None:
         del x
 
 
+def make_hidden(w: Workload, d: int, device="cpu"):
+    """Last hidden states [N, P+C, d] bfloat16 ~ N(0, 1) (seeded), for the
+    LM-head path."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(w.seed + 7)
+    x = torch.randn((w.N, w.T, d), generator=g, device=device, dtype=torch.float32)
+    return x.to(torch.bfloat16)
+
+
+def make_lm_head(w: Workload, d: int, device="cpu"):
+    """LM-head weight [V, d] bfloat16 ~ N(0, (std / sqrt(d))^2), so that the
+    logits hidden x W^T have the workload's logit standard deviation."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(w.seed + 9)
+    x = torch.randn((w.V, d), generator=g, device=device, dtype=torch.float32)
+    return x.mul_(w.logit_std / d ** 0.5).to(torch.bfloat16)
+
+
 def logits_as_numpy(t):
     """(numpy array, dtype tag) of a CPU tensor: float32 as is, bfloat16 as its
     uint16 bit patterns."""
