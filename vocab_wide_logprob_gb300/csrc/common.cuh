@@ -507,6 +507,7 @@ cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceIn
 // LM-head log-probs (tensor cores): workspace beyond the base layout holds a
 // dense copy of the scored rows' hidden states and the per-item partials.
 struct LmLayout {
+  size_t geometry;  // int4: row blocks, vocabulary splits, tiles per split
   size_t dense;     // bf16 [N*C, d]
   size_t partials;  // float4 [items][128]
   size_t total;

@@ -40,26 +40,56 @@ constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB
 constexpr int kStageBytesLm = kABytes + kBBytes;
 constexpr int kLmThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kMaxSplits = 64;
+constexpr int kMaxSplits = 256;  // = kThreads: one candidate per thread
 
 struct LmParams {
   int64_t N, P, C, V, d;
   const int32_t* offsets;  // prefix sums of the clamped lengths ([N+1])
+  int4* geometry;          // (row blocks, splits, tiles per split): written by the gather
   float4* partials;        // [items][kBM] (max, sum, target logit, has target)
   WsHeader* hdr;
   int sms;                 // CTAs in the grid: the split count is chosen from it
 };
 
-// Row blocks and vocabulary splits for t_valid rows (same on every kernel).
-__device__ __forceinline__ void lm_geometry(int64_t t_valid, int64_t V, int sms, int64_t& mb,
-                                            int64_t& splits, int64_t& tiles_per_split) {
-  const int64_t ntiles = (V + kBN - 1) / kBN;
-  mb = (t_valid + kBM - 1) / kBM;
-  splits = mb > 0 ? (sms + mb - 1) / mb : 1;
-  if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits > ntiles) splits = ntiles;
-  if (splits < 1) splits = 1;
-  tiles_per_split = (ntiles + splits - 1) / splits;
+// Row blocks and vocabulary splits for t_valid rows, computed once by the
+// first CTA of gather_rows_kernel and read by the later kernels.  Candidate
+// split counts s = 1 .. 256 (one per thread) are scored by how well their work
+// items (row block, 1/s of the vocabulary tiles) fill the grid's rounds,
+// counting both the items per round and the uneven last split of tiles; the
+// smallest s within 0.01 of the best score wins (less merging, and every split
+// re-reads its row block).  items = mb * s never exceeds 4 * sms + 2 * mb, the
+// size of the partials buffer.
+__device__ float lm_split_score(int32_t mb, int32_t sp, int32_t ntiles, int sms) {
+  const int32_t items = mb * sp;
+  if (sp > ntiles || items > 4 * sms + 2 * mb) return -1.f;
+  const int32_t rounds = (items + sms - 1) / sms;
+  const int32_t tps = (ntiles + sp - 1) / sp;
+  return (float)items / (float)(rounds * sms) * (float)ntiles / (float)(tps * sp);
+}
+
+// Called by all kThreads (= kMaxSplits) threads of one CTA.
+__device__ int4 lm_geometry_block(int64_t t_valid, int64_t V, int sms) {
+  __shared__ float s_best[kWarps];
+  __shared__ int s_pick[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t ntiles = (int32_t)((V + kBN - 1) / kBN);
+  const int32_t mb = (int32_t)((t_valid + kBM - 1) / kBM);
+  const int32_t sp = tid + 1;
+  const float score = mb > 0 ? lm_split_score(mb, sp, ntiles, sms) : (sp == 1 ? 1.f : -1.f);
+  float best = score;
+  for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) s_best[warp] = best;
+  __syncthreads();
+  best = s_best[0];
+  for (int k = 1; k < kWarps; ++k) best = fmaxf(best, s_best[k]);
+  int pick = (score >= 0.f && score >= best - 0.01f) ? sp : 1 << 30;
+  for (int o = 16; o > 0; o >>= 1) pick = min(pick, __shfl_xor_sync(0xffffffffu, pick, o));
+  if (lane == 0) s_pick[warp] = pick;
+  __syncthreads();
+  pick = s_pick[0];
+  for (int k = 1; k < kWarps; ++k) pick = min(pick, s_pick[k]);
+  if (pick > kMaxSplits) pick = 1;
+  return make_int4(mb, pick, (ntiles + pick - 1) / pick, 0);
 }
 
 // ---- tensor memory and tcgen05 helpers ----------------------------------------
@@ -128,10 +158,15 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
                                                                uint16_t* __restrict__ dense,
                                                                const int32_t* __restrict__ off,
                                                                int64_t N, int64_t T, int64_t P,
-                                                               int64_t d) {
+                                                               int64_t d, int64_t V, int sms,
+                                                               int4* __restrict__ geometry) {
   pdl_wait();
   pdl_trigger();
   const int64_t tv = off[N];
+  if (blockIdx.x == 0) {
+    const int4 g = lm_geometry_block(tv, V, sms);
+    if (threadIdx.x == 0) *geometry = g;
+  }
   const int64_t vec_per_row = d / 8;  // 16-byte vectors
   for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < tv * vec_per_row;
        k += (int64_t)gridDim.x * kThreads) {
@@ -194,8 +229,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   pdl_trigger();
 
   const int64_t tv = p.offsets[p.N];
-  int64_t mb, splits, tps;
-  lm_geometry(tv, p.V, p.sms, mb, splits, tps);
+  const int4 geo = *p.geometry;
+  const int64_t mb = geo.x, splits = geo.y, tps = geo.z;
   const int64_t ntiles = (p.V + kBN - 1) / kBN;
   const int64_t items = mb * splits;
   const int kblocks = (int)(p.d / kBK);
@@ -386,10 +421,7 @@ __global__ void __launch_bounds__(kThreads) lmhead_merge_kernel(const LmParams p
                                                                 const int32_t* __restrict__ lens) {
   pdl_wait();
   pdl_trigger();
-  const int64_t tv = p.offsets[p.N];
-  int64_t mb, splits, tps;
-  lm_geometry(tv, p.V, p.sms, mb, splits, tps);
-  (void)tps;
+  const int64_t splits = p.geometry->y;
   const int64_t NC = p.N * p.C;
   for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < NC;
        k += (int64_t)gridDim.x * kThreads) {
@@ -466,10 +498,11 @@ LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms) {
   LmLayout l;
   const WsLayout base = ws_layout(N);
   const int64_t rows = N * C;
-  l.dense = align_up(base.total, 1024);
+  l.geometry = base.total;  // 16 bytes
+  l.dense = align_up(base.total + 16, 1024);
   l.partials = align_up(l.dense + (size_t)rows * (size_t)d * 2, 256);
   const int64_t mb_max = (rows + kBM - 1) / kBM;
-  const int64_t items_max = (int64_t)sms + mb_max;  // mb * splits <= sms + mb
+  const int64_t items_max = 4 * (int64_t)sms + 2 * mb_max;  // mb * splits bound
   l.total = align_up(l.partials + (size_t)items_max * kBM * sizeof(float4), 256);
   return l;
 }
@@ -483,9 +516,10 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   uint16_t* dense = reinterpret_cast<uint16_t*>(ws + ll.dense);
   const int64_t rows = a.N * a.C;
 
+  int4* geometry = reinterpret_cast<int4*>(ws + ll.geometry);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(hidden), dense, off, a.N,
-                             a.P + a.C, a.P, d);
+                             a.P + a.C, a.P, d, a.V, dev.sms, geometry);
   if (e != cudaSuccess) return e;
 
   CUtensorMap map_h, map_w;
@@ -499,6 +533,7 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   p.V = a.V;
   p.d = d;
   p.offsets = off;
+  p.geometry = geometry;
   p.partials = reinterpret_cast<float4*>(ws + ll.partials);
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.sms = dev.sms;
