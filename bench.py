@@ -62,6 +62,8 @@ def parse_args():
                    help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd; "
                         "lmhead_logprobs: log-probs from hidden states with the LM-head "
                         "projection on the tensor cores (the no-grad old/reference pass)")
+    p.add_argument("--no-other-path", dest="also_other_path", action="store_false",
+                   help="skip timing the other forward+backward path for the record")
     p.add_argument("--hidden", type=int, default=896,
                    help="hidden size for --path lmhead_logprobs (Qwen2.5-0.5B: 896)")
     return p.parse_args()
@@ -414,6 +416,40 @@ def run_ours(args, w0: wl.Workload):
         dist.barrier()
     clocks = sampler.stop() if sampler is not None else None
     elapsed = start.elapsed_time(end) / 1e3
+
+    # the other path on the same inputs, for the record (its own byte count)
+    alt = None
+    if args.also_other_path and world == 1:
+        alt_fused = not fused
+        alt_out = {}
+        def alt_step():
+            m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
+            a = g.grpo_advantage(R, w.G, adv)
+            if alt_fused:
+                alt_out["o"] = g.grpo_loss_fwd_bwd(logits, w.P, ids, ln, a, old, ref, w.eps,
+                                                   w.beta, 0.0, None, alt_out.get("o"), ws, dlogits)
+            else:
+                o = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0,
+                                    alt_out.get("o"), ws)
+                alt_out["o"] = o
+                g.grpo_loss_bwd(logits, w.P, ids, ln, o["lse"], o["w"], None, dlogits)
+        for _ in range(max(args.warmup, 3)):
+            alt_step()
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            alt_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        alt_ms = s0.elapsed_time(s1) / args.steps
+        bb = algorithmic_bytes(w, t_valid)
+        alt_bytes = bb["step_logits_fused"] if alt_fused else bb["step_logits"]
+        alt = {"path": "fused" if alt_fused else "two_pass", "ms_per_step": alt_ms,
+               "value": t_valid / (alt_ms * 1e-3), "unit": UNIT,
+               "logits_bytes_per_step": alt_bytes,
+               "logits_gbs": alt_bytes / (alt_ms * 1e-3) / 1e9}
     t_mask = statistics.mean(e[0].elapsed_time(e[1]) for e in events) / 1e3
     t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in events) / 1e3
     t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in events) / 1e3
@@ -515,6 +551,8 @@ def run_ours(args, w0: wl.Workload):
             "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
             "copy_ceiling_gbs": copy_gbs,
+            "other_path": None if alt is None else dict(
+                alt, logits_roofline_frac=alt["logits_gbs"] / peak),
             "gpu_launches": (KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP) * args.steps,
             "cpu_baseline": cpu,
             "clocks": clocks,
