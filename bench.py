@@ -103,24 +103,34 @@ def measured_peaks() -> dict:
         return {}
 
 
-def csrc_sha() -> str:
+# the source files that define each kernel (the capture's hash covers these)
+KERNEL_SOURCES = {
+    "dlogits_kernel": ("dlogits.cu", "common.cuh"),
+    "lse_gather_kernel": ("lse_gather.cu", "common.cuh"),
+    "grpo_loss_fwd_bwd": ("fused.cu", "dlogits.cu", "lse_gather.cu", "common.cuh"),
+    "lmhead_lse_kernel": ("lmhead.cu", "common.cuh"),
+}
+
+
+def sources_sha(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "vocab_wide_logprob_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "vocab_wide_logprob_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, w: wl.Workload):
+def recorded_traffic(kernel: str, w: wl.Workload, hidden: int | None = None):
     """DRAM bytes (read + write) per launch of `kernel` on workload `w` from a
     committed ncu capture (profiles/traffic.json); None when there is none for
-    this workload or when the kernel sources changed since the capture."""
+    this workload or when the kernel's sources changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(kernel)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("csrc_sha") != csrc_sha() or rec.get("workload") != w.name:
+    if (not rec or rec.get("sources_sha") != sources_sha(kernel) or rec.get("workload") != w.name
+            or rec.get("hidden") != hidden):
         return None
     return rec["dram_bytes_per_launch"]
 
@@ -617,7 +627,8 @@ def run_lmhead(args, w: wl.Workload):
         "roofline": {"kernel": "lmhead_lse_kernel (+ gather, merge)", "bound": "tensor",
                      "achieved": tflops, "peak": peak,
                      "peak_source": "measured" if peaks.get("bf16_tflops") else "fallback",
-                     "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None},
+                     "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": recorded_traffic("lmhead_lse_kernel", w, d)},
         "gpu_launches": 5 * args.steps, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

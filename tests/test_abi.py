@@ -30,6 +30,11 @@ def lib():
     lib.grpo_loss_bwd.argtypes = [P, INT, I64, I64, I64, I64, P, P, P, P, P, P, P]
     lib.grpo_check_error.argtypes = [P, P]
     lib.grpo_copy.argtypes = [P, P, SZ, P]
+    lib.grpo_lmhead_logprobs.argtypes = [P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P]
+    lib.grpo_advantage_ex.argtypes = [P, I64, I64, INT, F, P, P, P]
+    lib.grpo_loss_bwd_ex.argtypes = [P, INT, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_uint32, P]
+    lib.grpo_loss_fwd_ex.argtypes = [P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P, P,
+                                     P, P, P, SZ, P]
     return lib
 
 
@@ -144,3 +149,28 @@ def test_copy_validation(lib):
     assert lib.grpo_copy(A(0x1000), A(0x1010), 64, None) == INVALID   # overlap
     assert lib.grpo_copy(None, None, 0, None) == OK
     assert lib.grpo_check_error(None, None) == INVALID
+
+
+def test_extended_entry_validation(lib):
+    a = A(0x10000)
+    # advantage modes and epsilon
+    assert lib.grpo_advantage_ex(a, 2, 4, 7, 0.0, A(0x20000), None, None) == UNSUPPORTED
+    assert lib.grpo_advantage_ex(a, 2, 4, 1, -1.0, A(0x20000), None, None) == INVALID
+    assert lib.grpo_advantage_ex(a, 2, 4, 1, 0.0, A(0x20000), A(0x30002), None) == MISALIGNED
+    # backward flags
+    assert lib.grpo_loss_bwd_ex(a, 1, 8, 4, 8, 64, A(0x20000), A(0x30000), A(0x40000),
+                                A(0x50000), None, A(0x10000000), 2, None) == UNSUPPORTED
+    # aggregation
+    assert lib.grpo_loss_fwd_ex(a, 1, 8, 4, 8, 64, A(0x20000), A(0x30000), A(0x40000), None, None,
+                                0.2, 0.0, 0.0, 5, A(0x50000), A(0x60000), A(0x70000), A(0x80000),
+                                A(0x100000), 1 << 20, None) == UNSUPPORTED
+    # LM head: hidden size a multiple of 64, 16-byte aligned operands
+    args = [a, A(0x200000), 8, 4, 8, 1000, 96, A(0x20000), A(0x30000), A(0x40000), A(0x50000),
+            A(0x100000), 1 << 30, None]
+    assert lib.grpo_lmhead_logprobs(*args) == UNSUPPORTED
+    args[6] = 128
+    args[0] = A(0x10008)
+    assert lib.grpo_lmhead_logprobs(*args) == MISALIGNED
+    args[0] = a
+    args[11] = None
+    assert lib.grpo_lmhead_logprobs(*args) == INVALID

@@ -95,3 +95,24 @@ def test_lmhead_bad_token_reported():
     lp, _, ws = g.grpo_lmhead_logprobs(hidden, weight, w.P, t_ids, lens)
     assert g.grpo_check_error(ws) == 6
     assert np.isnan(lp[0, 2].item())
+
+
+@pytest.mark.parametrize("V,d,B,G,C", [(200, 64, 1, 2, 3), (256, 128, 1, 1, 1), (257, 64, 2, 2, 5)],
+                         ids=["V_below_tile", "one_row", "V_tile_plus_one"])
+def test_lmhead_edge_shapes(V, d, B, G, C):
+    w = wl.variant(wl.QWEN_G8, name=f"lm_edge_{V}", B=B, G=G, P=3, C=C, V=V, eos_id=V - 1,
+                   seed=70 + V)
+    hidden, weight, ids, lens, lp, lse, status = _run(w, d)
+    assert status == 0
+    lp_o, lse_o = oracle.lmhead_logp(_bits16(hidden), _bits16(weight), w.P, w.C, ids, lens)
+    assert np.max(np.abs(lp - lp_o)) <= TOL and np.max(np.abs(lse - lse_o)) <= TOL
+
+
+def test_lmhead_empty_batch():
+    g = H.g()
+    hidden = torch.zeros((0, 6, 64), dtype=torch.bfloat16, device="cuda")
+    weight = torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((0, 6), dtype=torch.int64, device="cuda")
+    lens = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    lp, lse, ws = g.grpo_lmhead_logprobs(hidden, weight, 2, ids, lens)
+    assert lp.numel() == 0 and g.grpo_check_error(ws) == 0
