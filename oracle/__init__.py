@@ -21,6 +21,9 @@ with ctypes and marshals numpy arrays.  Each method cites the part of the page
   aggregation over a constant normaliser
 * :meth:`Oracle.dlogits`, :meth:`Oracle.dlogits_row` -- "loss.backward()": the
   gradient with respect to the logits (chain rule; the page prints none)
+* :meth:`Oracle.lmhead_logp`, :meth:`Oracle.lmhead_grads` -- the same through
+  the LM-head projection ``model(...).logits`` = hidden x W^T: log-probs from
+  hidden states, and the gradients with respect to the hidden states and W
 
 Logits are numpy arrays of ``float32`` (``"f32"``), ``float64`` (``"f64"``,
 for finite differences) or ``uint16`` holding bfloat16 bit patterns
@@ -84,6 +87,14 @@ def _logits_arg(x, dtype):
     if x.dtype != _NP[code]:
         raise TypeError(f"{dtype} logits must be a {np.dtype(_NP[code]).name} array")
     return x, code
+
+
+def _wide(x):
+    """float64 copy of a float array or of uint16 bfloat16 bit patterns (exact)."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
 
 
 class Oracle:
@@ -192,13 +203,8 @@ class Oracle:
         scored rows' logits in float64 (numpy matmul of the exactly widened
         bf16 inputs), then :meth:`logp_rows`.  Inputs are uint16 bf16 bit
         patterns or float arrays.  Returns ``(logp, lse)`` [N, C]."""
-        def wide(x):
-            x = np.asarray(x)
-            if x.dtype == np.uint16:
-                return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-            return x.astype(np.float64)
-        H = wide(hidden)
-        W = wide(weight)
+        H = _wide(hidden)
+        W = _wide(weight)
         N = H.shape[0]
         ids = np.asarray(ids, dtype=np.int64)
         lens = np.asarray(lens, dtype=np.int32)
@@ -213,6 +219,64 @@ class Oracle:
             lp[i, :L] = a
             ls[i, :L] = b
         return lp, ls
+
+    def lmhead_grads(self, hidden, weight, P: int, C: int, ids, lens, lse, w, g: float = 1.0,
+                     rows=None, vocab=None, magnitudes: bool = False):
+        """Gradients of ``g * loss`` through the LM head ("loss.backward()" of
+        the loss over ``model(...).logits`` = hidden x W^T): each scored row's
+        logits gradient dz from :meth:`dlogits_row` (lse and w as the forward
+        left them), then by the chain rule through z = h W^T
+        dhidden[i, P-1+t] = dz W and dweight = sum over scored rows of dz^T h
+        (numpy float64 matmuls of the exactly widened inputs).  Rows that score
+        nothing get a zero dhidden.
+
+        ``rows``: None for the whole dhidden [N, P+C, d], or a list of
+        completion positions (i, t) for just those rows ([len(rows), d];
+        positions that score nothing give zero rows).  ``vocab``: None for the
+        whole dweight [V, d], or vocabulary ids for just those rows.
+        ``magnitudes``: also return |dz| |W| and |dz|^T |h| with the same
+        shapes (the sums whose terms a rounding of dz perturbs).
+        Returns ``dict(dhidden=..., dweight=...[, dhidden_mag=..., dweight_mag=...])``."""
+        H = _wide(hidden)
+        W = _wide(weight)
+        N, T, d = H.shape
+        V = W.shape[0]
+        ids = np.asarray(ids, dtype=np.int64)
+        lens = np.asarray(lens, dtype=np.int32)
+        lse = np.asarray(lse, dtype=np.float64)
+        w = np.asarray(w, dtype=np.float64)
+        vsel = np.arange(V) if vocab is None else np.asarray(vocab, dtype=np.int64)
+        dH = np.zeros((N, T, d) if rows is None else (len(rows), d))
+        dW = np.zeros((len(vsel), d))
+        mH = np.zeros_like(dH) if magnitudes else None
+        mW = np.zeros_like(dW) if magnitudes else None
+        absW = np.abs(W) if magnitudes else None
+        for i in range(N):
+            L = int(lens[i])
+            if L == 0:
+                continue
+            h = H[i, P - 1:P - 1 + L]           # the rows that score tokens 0..L-1
+            z = h @ W.T
+            dz = np.stack([self.dlogits_row(z[t], "f64", int(ids[i, P + t]), lse[i, t],
+                                            g * w[i, t]) for t in range(L)])
+            if rows is None:
+                dH[i, P - 1:P - 1 + L] = dz @ W
+                if magnitudes:
+                    mH[i, P - 1:P - 1 + L] = np.abs(dz) @ absW
+            else:
+                for k, (ii, t) in enumerate(rows):
+                    if ii == i and 0 <= t < L:
+                        dH[k] = dz[t] @ W
+                        if magnitudes:
+                            mH[k] = np.abs(dz[t]) @ absW
+            dzs = dz[:, vsel]
+            dW += dzs.T @ h
+            if magnitudes:
+                mW += np.abs(dzs).T @ np.abs(h)
+        out = dict(dhidden=dH, dweight=dW)
+        if magnitudes:
+            out.update(dhidden_mag=mH, dweight_mag=mW)
+        return out
 
     # -- "The loss" ------------------------------------------------------------
     def loss_seq_mean(self, logp, old, ref, adv, lens, eps: float, beta: float,
@@ -311,6 +375,10 @@ def loss(*a, **k):
 
 def lmhead_logp(*a, **k):
     return default().lmhead_logp(*a, **k)
+
+
+def lmhead_grads(*a, **k):
+    return default().lmhead_grads(*a, **k)
 
 
 def dlogits_row(*a, **k):

@@ -542,8 +542,101 @@ def pin_lmhead_reduces_to_logits(o):
     assert np.allclose(c, b, rtol=0, atol=1e-12)
 
 
+def _lmhead_micro(o, seed):
+    """A micro batch through an LM head: 3 completions (one stops at EOS),
+    P=2, C=3, V=7, d=5, float64 hidden states and weights."""
+    N, P, C, V, d = 3, 2, 3, 7, 5
+    rng = np.random.default_rng(seed)
+    H = rng.normal(0, 1, size=(N, P + C, d))
+    W = rng.normal(0, 0.8, size=(V, d))
+    ids = rng.integers(3, V, size=(N, P + C))
+    ids[2, P + 1] = 2                      # completion 2 ends after 2 tokens
+    _, lens = o.mask(ids, P, C, 2)
+    A = np.array([0.7, -0.3, -0.4])
+    lp, _ = o.lmhead_logp(H, W, P, C, ids, lens)
+    old = lp + _away_from_kinks(rng, lp.shape, 0.2)
+    ref = lp + rng.normal(0, 0.3, lp.shape)
+    return H, W, ids, lens, A, old, ref, P, C
+
+
+def pin_lmhead_grads_fd(o):
+    """Chain rule through logits = hidden x W^T: central finite differences of
+    the loss as a function of every hidden-state and every weight entry
+    (prompt rows, the last row and rows past the EOS included: their
+    derivative is 0), with the clipped surrogate and the KL term both active
+    and an upstream gradient g = 2.5."""
+    H, W, ids, lens, A, old, ref, P, C = _lmhead_micro(o, 51)
+    g = 2.5
+
+    def f(HH, WW):
+        lpz, _ = o.lmhead_logp(HH, WW, P, C, ids, lens)
+        return g * o.loss(lpz, old, ref, A, lens, 0.2, 0.1)[0]
+
+    lp, ls = o.lmhead_logp(H, W, P, C, ids, lens)
+    _, wt, _ = o.loss(lp, old, ref, A, lens, 0.2, 0.1)
+    an = o.lmhead_grads(H, W, P, C, ids, lens, ls, wt, g)
+    h = 1e-6
+    for idx in np.ndindex(H.shape):
+        Hp = H.copy()
+        Hp[idx] += h
+        Hm = H.copy()
+        Hm[idx] -= h
+        fd = (f(Hp, W) - f(Hm, W)) / (2 * h)
+        assert abs(fd - an["dhidden"][idx]) <= 1e-9 + 1e-5 * abs(an["dhidden"][idx]), idx
+    for idx in np.ndindex(W.shape):
+        Wp = W.copy()
+        Wp[idx] += h
+        Wm = W.copy()
+        Wm[idx] -= h
+        fd = (f(H, Wp) - f(H, Wm)) / (2 * h)
+        assert abs(fd - an["dweight"][idx]) <= 1e-9 + 1e-5 * abs(an["dweight"][idx]), idx
+
+
+def pin_lmhead_grads_identity_and_subsets(o):
+    """With W = I (d = V) the hidden states are the logits, so dhidden equals
+    the logits gradient; dweight is then sum over scored rows of dz^T h,
+    checked by a plain loop; the row and vocabulary subsets equal the
+    matching slices of the full result; the columns of dweight sum to 0
+    (each row of dz does), and |value| <= magnitude everywhere."""
+    N, P, C, V = 3, 4, 5, 9
+    rng = np.random.default_rng(43)
+    H = rng.normal(0, 2, size=(N, P + C, V))
+    ids = rng.integers(3, V, size=(N, P + C))
+    ids[0, P + 1] = 2
+    _, lens = o.mask(ids, P, C, 2)
+    lp, ls = o.lmhead_logp(H, np.eye(V), P, C, ids, lens)
+    old = lp + _away_from_kinks(rng, lp.shape, 0.2)
+    _, wt, _ = o.loss(lp, old, None, np.array([1.0, -0.5, -0.5]), lens, 0.2, 0.0)
+    gr = o.lmhead_grads(H, np.eye(V), P, C, ids, lens, ls, wt, 1.5, magnitudes=True)
+    dz = o.dlogits(H, "f64", P, C, ids, lens, ls, wt, 1.5)
+    assert np.allclose(gr["dhidden"], dz, rtol=0, atol=1e-15)
+    ref = np.zeros((V, V))
+    for i in range(N):
+        for t in range(int(lens[i])):
+            r = P - 1 + t
+            for v in range(V):
+                for k in range(V):
+                    ref[v, k] += dz[i, r, v] * H[i, r, k]
+    assert np.allclose(gr["dweight"], ref, rtol=0, atol=1e-13)
+    assert np.all(np.abs(gr["dweight"].sum(axis=0)) < 1e-12)
+    assert np.all(np.abs(gr["dhidden"]) <= gr["dhidden_mag"] + 1e-15)
+    assert np.all(np.abs(gr["dweight"]) <= gr["dweight_mag"] + 1e-15)
+    Hb, Wb, ids_b, lens_b, A, old_b, ref_b, Pb, Cb = _lmhead_micro(o, 52)
+    lp, ls = o.lmhead_logp(Hb, Wb, Pb, Cb, ids_b, lens_b)
+    _, wt, _ = o.loss(lp, old_b, ref_b, A, lens_b, 0.2, 0.1)
+    full = o.lmhead_grads(Hb, Wb, Pb, Cb, ids_b, lens_b, ls, wt)
+    rows = [(2, 1), (0, 0), (2, 2), (1, 2)]     # (2, 2) is past completion 2's EOS
+    vocab = [6, 0, 3]
+    part = o.lmhead_grads(Hb, Wb, Pb, Cb, ids_b, lens_b, ls, wt, rows=rows, vocab=vocab)
+    for k, (i, t) in enumerate(rows):
+        assert np.allclose(part["dhidden"][k], full["dhidden"][i, Pb - 1 + t], rtol=0, atol=1e-15)
+    assert not part["dhidden"][2].any()
+    assert np.allclose(part["dweight"], full["dweight"][vocab], rtol=0, atol=1e-15)
+    assert not full["dhidden"][:, :Pb - 1].any() and not full["dhidden"][:, -1].any()
+
+
 ALL_CHEAP = [
-    pin_lmhead_reduces_to_logits,
+    pin_lmhead_reduces_to_logits, pin_lmhead_grads_fd, pin_lmhead_grads_identity_and_subsets,
     pin_advantage_std_examples, pin_seq_mean_aggregation, pin_dlogits_fd_seq_mean,
     pin_mask_golden, pin_mask_batch_matches_rows, pin_advantage_examples,
     pin_logp_constant_row, pin_logp_two_level, pin_logp_library, pin_logp_token_range,

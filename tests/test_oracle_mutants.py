@@ -6,6 +6,7 @@ page "Making Dr GRPO go brrr" warns about), compiled on the CPU into a
 temporary library.  The test requires at least one pin of
 ``oracle_pins.ALL_CHEAP`` to reject it.  CPU only."""
 import os
+import types
 
 import pytest
 
@@ -69,6 +70,39 @@ def test_mutant_is_caught(name, source, tmp_path):
     src.write_text(source.replace(old, new))
     lib = oracle.compile_source(str(src), str(tmp_path / f"{name}.so"))
     o = oracle.Oracle(lib)
+    failures = []
+    for pin in pins.ALL_CHEAP:
+        try:
+            pin(o)
+        except (AssertionError, ValueError) as e:
+            failures.append(pin.__name__)
+            break
+    assert failures, f"mutant {name} passed every pin"
+
+
+# Planted mistakes in the numpy side of the oracle (the LM-head chain rule in
+# oracle/__init__.py), loaded as a module of their own over the real C library.
+PY_MUTANTS = {
+    "lmhead_grad_rows_unshifted": ("h = H[i, P - 1:P - 1 + L]", "h = H[i, P:P + L]"),
+    "lmhead_dhidden_misplaced": ("dH[i, P - 1:P - 1 + L] = dz @ W", "dH[i, P:P + L] = dz @ W"),
+    "lmhead_drops_upstream": ("g * w[i, t]) for t", "w[i, t]) for t"),
+    "lmhead_dweight_sign": ("dW += dzs.T @ h", "dW -= dzs.T @ h"),
+    "lmhead_dweight_next_row": ("dW += dzs.T @ h", "dW += dzs.T @ H[i, P:P + L]"),
+    "lmhead_dhidden_uses_transpose": ("dH[i, P - 1:P - 1 + L] = dz @ W\n",
+                                      "dH[i, P - 1:P - 1 + L] = (W.T @ dz.T).T[:, ::-1]\n"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_python_mutant_is_caught(name):
+    with open(oracle.__file__) as f:
+        src = f.read()
+    old, new = PY_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique/present"
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = oracle.__file__
+    exec(compile(src.replace(old, new), oracle.__file__, "exec"), mod.__dict__)
+    o = mod.Oracle(oracle.build())
     failures = []
     for pin in pins.ALL_CHEAP:
         try:
