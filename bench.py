@@ -58,14 +58,17 @@ def parse_args():
     p.add_argument("--skip-zero-weight", action="store_true",
                    help="backward skips reading rows whose gradient weight is exactly 0; "
                         "the skipped reads are left out of the byte count")
-    p.add_argument("--path", choices=["two_pass", "fused", "lmhead_logprobs"], default="two_pass",
+    p.add_argument("--path", choices=["two_pass", "fused", "lmhead_logprobs", "lmhead_fwd_bwd"],
+                   default="two_pass",
                    help="two_pass: grpo_loss_fwd then grpo_loss_bwd; fused: grpo_loss_fwd_bwd; "
                         "lmhead_logprobs: log-probs from hidden states with the LM-head "
-                        "projection on the tensor cores (the no-grad old/reference pass)")
+                        "projection on the tensor cores (the no-grad old/reference pass); "
+                        "lmhead_fwd_bwd: the loss from hidden states and its gradients with "
+                        "respect to the hidden states and the LM head, on the tensor cores")
     p.add_argument("--no-other-path", dest="also_other_path", action="store_false",
                    help="skip timing the other forward+backward path for the record")
     p.add_argument("--hidden", type=int, default=896,
-                   help="hidden size for --path lmhead_logprobs (Qwen2.5-0.5B: 896)")
+                   help="hidden size of the LM-head paths (Qwen2.5-0.5B: 896)")
     return p.parse_args()
 
 
@@ -575,62 +578,112 @@ def run_ours(args, w0: wl.Workload):
 
 
 def run_lmhead(args, w: wl.Workload):
-    """Times grpo_mask + grpo_lmhead_logprobs: log-probs of the sampled tokens
-    from hidden states [N, P+C, d] and a [V, d] LM head, logits never
-    materialised.  Roofline: tensor (2 * T_valid * V * d FLOPs per call)."""
+    """--path lmhead_logprobs: grpo_mask + grpo_lmhead_logprobs (log-probs of
+    the sampled tokens from hidden states [N, P+C, d] and a [V, d] LM head,
+    logits never materialised; 2 * T_valid * V * d FLOPs per step).
+    --path lmhead_fwd_bwd: grpo_mask + grpo_advantage + grpo_lmhead_loss_fwd +
+    grpo_lmhead_loss_bwd (the projection in the forward, its recomputation in
+    the backward, and the two gradient contractions: 4 * 2 * T_valid * V * d
+    FLOPs per step).  Roofline: tensor."""
     import torch
     from vocab_wide_logprob_gb300 import build as libbuild
     libbuild.build()
     from vocab_wide_logprob_gb300 import _native as g
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
+    train = args.path == "lmhead_fwd_bwd"
     d = args.hidden
     hidden = wl.make_hidden(w, d, "cuda")
     weight = wl.make_lm_head(w, d, "cuda")
     ids = torch.from_numpy(wl.make_ids(w)).to(dev)
+    R = torch.from_numpy(wl.make_rewards(w)).to(dev)
     mask, lens = g.grpo_mask(ids, w.P, w.C, w.eos_id)
     t_valid = int(lens.sum().item())
     lp, lse, ws = g.grpo_lmhead_logprobs(hidden, weight, w.P, ids, lens)
     stream = torch.cuda.current_stream()
+    old = ref = None
+    if train:
+        # old / reference log-probs: this policy's log-probs plus the workload's noise
+        n_old, n_ref = wl.make_noise(w)
+        if n_old is not None:
+            old = (lp + torch.from_numpy(n_old).float().to(dev)).contiguous()
+        if n_ref is not None:
+            ref = (lp + torch.from_numpy(n_ref).float().to(dev)).contiguous()
+        adv = g.grpo_advantage(R, w.G)
+        fwd = g.grpo_lmhead_loss_fwd(hidden, weight, w.P, ids, lens, adv, old, ref, w.eps, w.beta)
+        dh, dw, bws = g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"])
+
+    def step_fwd():
+        g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
+        if train:
+            g.grpo_advantage(R, w.G, adv)
+            g.grpo_lmhead_loss_fwd(hidden, weight, w.P, ids, lens, adv, old, ref, w.eps, w.beta,
+                                   out=fwd, workspace=ws)
+        else:
+            g.grpo_lmhead_logprobs(hidden, weight, w.P, ids, lens, (lp, lse), ws)
+
+    def step_bwd():
+        if train:
+            g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"],
+                                   out=(dh, dw), workspace=bws)
 
     def step():
-        g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
-        g.grpo_lmhead_logprobs(hidden, weight, w.P, ids, lens, (lp, lse), ws)
+        step_fwd()
+        step_bwd()
 
     sampler = None if args.no_clocks else ClockSampler(None)
     if sampler is not None:
         time.sleep(1.0)
     for _ in range(max(args.warmup, 3)):
         step()
-    assert g.grpo_check_error(ws) == 0
+    assert g.grpo_check_error(fwd["workspace"] if train else ws) == 0
+    if train:
+        assert g.grpo_check_error(bws) == 0
     torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
+
+    def timed(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    ms = timed(step)
     clocks = sampler.stop() if sampler is not None else None
-    ms = a.elapsed_time(b) / args.steps
-    flops = 2.0 * t_valid * w.V * d
+    ms_fwd = timed(step_fwd) if train else ms
+    ms_bwd = timed(step_bwd) if train else 0.0
+    unit_flops = 2.0 * t_valid * w.V * d
+    flops = unit_flops * (4 if train else 1)
     peaks = measured_peaks()
     peak = peaks.get("bf16_tflops") or 1900.0
     tflops = flops / (ms * 1e-3) / 1e12
     line = {
-        "metric": "completion tokens/s, log-probs from hidden states (LM head fused, no grad)",
+        "metric": ("completion tokens/s, Dr. GRPO loss fwd+bwd from hidden states (LM head "
+                   "fused: logits never materialised)") if train else
+                  "completion tokens/s, log-probs from hidden states (LM head fused, no grad)",
         "value": t_valid / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "path": "lmhead_logprobs",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "path": args.path,
         "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
-                   "hidden": d, "valid_tokens": t_valid},
-        "roofline": {"kernel": "lmhead_lse_kernel (+ gather, merge)", "bound": "tensor",
-                     "achieved": tflops, "peak": peak,
+                   "hidden": d, "valid_tokens": t_valid,
+                   "l2": "weights larger than L2 (%.2f GB); no flush" % (w.V * d * 2 / 1e9)},
+        "roofline": {"kernel": ("lmhead fwd + bwd (projection, recomputed projection, "
+                                "dhidden and dweight contractions)") if train else
+                               "lmhead_lse_kernel (+ gather, merge)",
+                     "bound": "tensor", "achieved": tflops, "peak": peak,
                      "peak_source": "measured" if peaks.get("bf16_tflops") else "fallback",
-                     "unit": "TFLOP/s", "frac": tflops / peak,
-                     "traffic": recorded_traffic("lmhead_lse_kernel", w, d)},
-        "gpu_launches": 5 * args.steps, "clocks": clocks,
+                     "unit": "TFLOP/s", "frac": tflops / peak, "flops_per_step": flops,
+                     "traffic": None if train else recorded_traffic("lmhead_lse_kernel", w, d)},
+        "gpu_launches": (13 if train else 5) * args.steps, "clocks": clocks,
     }
+    if train:
+        line["kernel_ms"] = {"fwd": ms_fwd, "bwd": ms_bwd}
+        line["fwd_tflops"] = unit_flops / (ms_fwd * 1e-3) / 1e12
+        line["bwd_tflops"] = 3 * unit_flops / (ms_bwd * 1e-3) / 1e12
     print(json.dumps(line), flush=True)
 
 
@@ -639,7 +692,7 @@ def main():
     w = wl.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
-    elif args.path == "lmhead_logprobs":
+    elif args.path in ("lmhead_logprobs", "lmhead_fwd_bwd"):
         run_lmhead(args, w)
     else:
         run_ours(args, w)

@@ -315,6 +315,48 @@ grpo_status grpo_lmhead_logprobs(const void *hidden, const void *weight, int64_t
                                  size_t workspace_bytes, grpo_stream_t stream);
 
 /*
+ * grpo_lmhead_loss_fwd -- the Dr. GRPO loss forward from hidden states:
+ * grpo_lmhead_logprobs followed by the surrogate, KL and token-sum reduction
+ * of grpo_loss_fwd ("The loss", grpo_loss).  Arguments as for those two
+ * calls; `workspace` at least grpo_lmhead_workspace_size bytes.  Outputs logp,
+ * lse, w and the device scalar loss, with grpo_loss_fwd's meaning.
+ */
+grpo_status grpo_lmhead_loss_fwd(const void *hidden, const void *weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
+                                 const int32_t *len, const float *adv, const float *old_logp,
+                                 const float *ref_logp, float eps, float beta, float norm,
+                                 float *logp, float *lse, float *w, float *loss, void *workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream);
+
+/*
+ * grpo_lmhead_loss_bwd -- gradients of g * loss with respect to the hidden
+ * states and the LM head ("loss.backward()" through "model(...).logits" =
+ * hidden x W^T; the chain rule, which the pages do not print).  Per scored
+ * row (sequence i, row P-1+t, t < len_i) the logits gradient
+ * dz = g * w[i, t] * (onehot(y) - softmax(z)) is recomputed from the logits
+ * on the tensor cores (lse and w as grpo_lmhead_loss_fwd left them), rounded
+ * to bfloat16 (the dtype of the logits), and contracted:
+ *   dhidden[i, P-1+t, :] = dz W        dweight = sum over scored rows dz^T h
+ * with float32 accumulation.  Rows that score nothing get dhidden = 0.
+ *
+ * hidden, weight, N, P, C, V, d, input_ids, len as for grpo_lmhead_logprobs;
+ * lse, w [N, C] float32 from the forward; grad_loss: device scalar (NULL: 1).
+ * dhidden [N, P+C, d] float32 and dweight [V, d] float32, 16-byte aligned,
+ * fully written (accumulate into your own buffers yourself).  workspace: at
+ * least grpo_lmhead_bwd_workspace_size bytes; it holds the dense scored
+ * hidden rows, the bfloat16 logits gradient of every possible scored row
+ * (2 * N * C * V bytes, V rounded up to 256) and the split partials of
+ * dhidden.  Results are deterministic (fixed summation orders).
+ */
+grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
+                                           size_t *bytes);
+grpo_status grpo_lmhead_loss_bwd(const void *hidden, const void *weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
+                                 const int32_t *len, const float *lse, const float *w,
+                                 const float *grad_loss, float *dhidden, float *dweight,
+                                 void *workspace, size_t workspace_bytes, grpo_stream_t stream);
+
+/*
  * grpo_check_error -- synchronises `stream`, then reports what the kernels of
  * the most recent grpo_loss_fwd on `workspace` recorded: GRPO_OK,
  * GRPO_ERR_TOKEN_RANGE (a scored id outside [0, V); its logp and lse are NaN),

@@ -1,0 +1,177 @@
+"""The loss through the LM head, forward (grpo_lmhead_loss_fwd) and backward
+(grpo_lmhead_loss_bwd: gradients with respect to the hidden states and W on
+the tensor cores) against the float64 oracle on the same bf16 inputs.
+
+Tolerances, fixed from the arithmetic before looking at results:
+* loss, w: as for the logits path (loss 1e-5 relative to max(|loss|, L1);
+  w 1e-4 of the size of its terms);
+* dhidden, dweight: the GPU rounds each logits-gradient entry dz to bf16
+  (relative error <= 2^-9) before the float32 contractions, so each output
+  element may move by at most 2^-9 times the sum of |dz| |operand| over its
+  terms (the oracle's magnitude); the check allows 2^-7 of that magnitude
+  (the rest covers float32 accumulation over up to V terms), requires exact
+  zeros where the magnitude is 0, and bounds the relative Frobenius error of
+  the whole sampled block by 1e-2.
+Inputs whose oracle ratio lies within 1e-5 of a clip boundary would let the
+two sides take different branches of min(); the seeds used here have none,
+and the test asserts it."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+import oracle
+from vocab_wide_logprob_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+GRAD_MAG = 2.0 ** -7
+GRAD_FRO = 1e-2
+
+
+def _bits16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_grad(gpu, ref, mag, what):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    err = np.abs(gpu - ref)
+    bad = err > GRAD_MAG * mag
+    assert not np.any(bad), (what, int(bad.sum()), np.argwhere(bad)[:5].tolist(),
+                             float(np.max(err / np.maximum(mag, 1e-300))))
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        assert np.linalg.norm(gpu - ref) <= GRAD_FRO * nref, (what, np.linalg.norm(gpu - ref) / nref)
+
+
+def _setup(w, d, device_gen=False):
+    n = H.g()
+    gen = "cuda" if device_gen else "cpu"
+    hidden = wl.make_hidden(w, d, gen).cuda()
+    weight = wl.make_lm_head(w, d, gen).cuda()
+    ids = wl.make_ids(w)
+    R = wl.make_rewards(w)
+    Hn, Wn = _bits16(hidden), _bits16(weight)
+    m_o, len_o = oracle.mask(ids, w.P, w.C, w.eos_id)
+    A_o = oracle.advantage(R, w.G)
+    lp_o, lse_o = oracle.lmhead_logp(Hn, Wn, w.P, w.C, ids, len_o)
+    old, ref = H.host_inputs(w, lp_o, m_o)
+    assert not H.kink_tokens(lp_o, old, w.eps).any()
+    nrm = float(w.N * w.C)
+    loss_o, w_o, ell_o = oracle.loss(lp_o, None if old is None else old.astype(np.float64),
+                                     None if ref is None else ref.astype(np.float64), A_o, len_o,
+                                     w.eps, w.beta, nrm)
+    t_ids = H.dev(ids)
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(R), w.G)
+    out = n.grpo_lmhead_loss_fwd(hidden, weight, w.P, t_ids, lens, adv, H.dev(old), H.dev(ref),
+                                 w.eps, w.beta)
+    assert n.grpo_check_error(out["workspace"]) == 0
+    host = dict(ids=ids, R=R, Hn=Hn, Wn=Wn, m=m_o, len=len_o, A=A_o, lp=lp_o, lse=lse_o, old=old,
+                ref=ref, norm=nrm, loss=loss_o, w=w_o, ell=ell_o)
+    return hidden, weight, t_ids, lens, out, host
+
+
+def _check_fwd(w, out, h):
+    lp = out["logp"].cpu().numpy().astype(np.float64)
+    lse = out["lse"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lp - h["lp"])) <= H.LOGP_ATOL["bf16"]
+    assert np.max(np.abs(lse - h["lse"])) <= H.LOGP_ATOL["bf16"]
+    H.assert_loss(float(out["loss"].item()), h["loss"], h["ell"], h["norm"])
+    wt = out["w"].cpu().numpy().astype(np.float64)
+    scale = H.w_scale(h["lp"], h["old"], h["ref"], h["A"], w.beta, h["norm"])
+    ok = h["m"] == 1
+    assert np.all(np.abs(wt - h["w"])[ok] <= 1e-4 * scale[ok] + 1e-12)
+    assert np.all(wt[~ok] == 0)
+
+
+SMALL = [
+    ("V1000_d64", wl.variant(wl.QWEN_G8, name="lmg_1000_64", B=2, G=4, P=8, C=24, V=1000,
+                             eos_id=999, seed=81), 64, 1.0),
+    ("V4099_d192_kl", wl.variant(wl.QWEN_G16_KL, name="lmg_4099_192", B=1, G=4, P=5, C=40,
+                                 V=4099, eos_id=4000, seed=82), 192, 2.5),
+    ("V300_d128_short", wl.variant(wl.QWEN_G8, name="lmg_300_128", B=1, G=2, P=3, C=6, V=300,
+                                   eos_id=299, seed=83), 128, None),
+]
+
+
+@pytest.mark.parametrize("name,w,d,g", SMALL, ids=[s[0] for s in SMALL])
+def test_lmhead_grads_small(name, w, d, g):
+    """Every element of the loss, w, dhidden and dweight against the oracle."""
+    n = H.g()
+    w = H.with_contrast(w)
+    hidden, weight, t_ids, lens, out, h = _setup(w, d)
+    _check_fwd(w, out, h)
+    gt = None if g is None else torch.tensor([g], dtype=torch.float32, device="cuda")
+    dh, dw, ws = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                                        gt)
+    assert n.grpo_check_error(ws) == 0
+    gr = oracle.lmhead_grads(h["Hn"], h["Wn"], w.P, w.C, h["ids"], h["len"], h["lse"], h["w"],
+                             1.0 if g is None else g, magnitudes=True)
+    assert_grad(dh.cpu().numpy(), gr["dhidden"], gr["dhidden_mag"], "dhidden")
+    assert_grad(dw.cpu().numpy(), gr["dweight"], gr["dweight_mag"], "dweight")
+
+
+def test_lmhead_grads_deterministic_and_scaled():
+    """Two calls give the same bits; an upstream gradient of 2 doubles every
+    output exactly (bf16 rounding commutes with a power-of-two scale)."""
+    n = H.g()
+    w = H.with_contrast(SMALL[1][1])
+    hidden, weight, t_ids, lens, out, h = _setup(w, 192)
+    one = torch.tensor([1.0], dtype=torch.float32, device="cuda")
+    two = torch.tensor([2.0], dtype=torch.float32, device="cuda")
+    a = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"], one)
+    b = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"], one)
+    c = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"], two)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    assert torch.equal(c[0], 2 * a[0]) and torch.equal(c[1], 2 * a[1])
+
+
+def test_lmhead_grads_no_scored_rows():
+    """C = 0: nothing is scored, both gradients are zero."""
+    n = H.g()
+    hidden = torch.ones((2, 4, 64), dtype=torch.bfloat16, device="cuda")
+    weight = torch.ones((300, 64), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((2, 4), dtype=torch.int64, device="cuda")
+    lens = torch.zeros((2,), dtype=torch.int32, device="cuda")
+    z = torch.zeros((2, 0), dtype=torch.float32, device="cuda")
+    dh, dw, ws = n.grpo_lmhead_loss_bwd(hidden, weight, 4, ids, lens, z, z)
+    torch.cuda.synchronize()
+    assert not dh.any() and not dw.any()
+
+
+def test_lmhead_grads_full_size_default_workload():
+    """The benchmark workload's shapes with Qwen2.5-0.5B's hidden size 896
+    (about 1,000 scored rows, V = 151,936; the first seed with reward
+    contrast): the forward against the oracle on every token; sampled rows of
+    dhidden and sampled rows of dweight (the targets of some scored tokens
+    among them) element by element; every row of dhidden that scores nothing
+    exactly zero."""
+    n = H.g()
+    w = H.with_contrast(wl.QWEN_G8)
+    hidden, weight, t_ids, lens, out, h = _setup(w, 896, device_gen=True)
+    _check_fwd(w, out, h)
+    dh, dw, ws = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"])
+    assert n.grpo_check_error(ws) == 0
+    rng = np.random.default_rng(5)
+    L = h["len"]
+    rows = []
+    for _ in range(24):
+        i = int(rng.integers(0, w.N))
+        rows.append((i, int(rng.integers(0, L[i]))))
+    rows += [(0, 0), (w.N - 1, int(L[-1]) - 1)]
+    targets = [int(h["ids"][i, w.P + t]) for i, t in rows[:16]]
+    vocab = sorted(set(targets) | set(rng.integers(0, w.V, 24).tolist()) | {0, w.V - 1})
+    gr = oracle.lmhead_grads(h["Hn"], h["Wn"], w.P, w.C, h["ids"], L, h["lse"], h["w"], 1.0,
+                             rows=rows, vocab=vocab, magnitudes=True)
+    dh_h = dh.cpu().numpy()
+    got = np.stack([dh_h[i, w.P - 1 + t] for i, t in rows])
+    assert_grad(got, gr["dhidden"], gr["dhidden_mag"], "dhidden rows")
+    assert_grad(dw.cpu().numpy()[vocab], gr["dweight"], gr["dweight_mag"], "dweight rows")
+    scored = np.zeros((w.N, w.T), bool)
+    for i in range(w.N):
+        scored[i, w.P - 1:w.P - 1 + L[i]] = True
+    assert not dh_h[~scored].any()
+    assert np.isfinite(dh_h).all() and torch.isfinite(dw).all()

@@ -67,6 +67,11 @@ def _load():
         "grpo_logprobs": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
         "grpo_lmhead_workspace_size": ([I64, I64, I64, I64, ctypes.POINTER(SZ)], INT),
         "grpo_lmhead_logprobs": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
+        "grpo_lmhead_loss_fwd": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
+                                  P, SZ, P], INT),
+        "grpo_lmhead_bwd_workspace_size": ([I64, I64, I64, I64, ctypes.POINTER(SZ)], INT),
+        "grpo_lmhead_loss_bwd": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P],
+                                 INT),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -361,6 +366,72 @@ def grpo_lmhead_logprobs(hidden, weight, P, input_ids, lens, out=None, workspace
     _check(_lib.grpo_lmhead_logprobs(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
                                      _ptr(lens), _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "grpo_lmhead_logprobs")
+    return out[0], out[1], workspace
+
+
+def grpo_lmhead_loss_fwd(hidden, weight, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
+                         eps=0.2, beta=0.0, norm=0.0, out=None, workspace=None, stream=None):
+    """The Dr. GRPO loss forward from hidden states [N, P+C, d] and the LM
+    head [V, d] (both bfloat16): the projection fused with the log-softmax on
+    the tensor cores, then the surrogate.  Returns a dict like
+    :func:`grpo_loss_fwd` (``logp``, ``lse``, ``w``, ``loss``, ``workspace``)."""
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(weight, "weight", torch.bfloat16)
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("adv", adv, torch.float32), ("old_logp", old_logp, torch.float32),
+                        ("ref_logp", ref_logp, torch.float32)):
+        _dev(t, name, dt)
+    N, T, d = hidden.shape
+    V = weight.shape[0]
+    C = T - P
+    if weight.shape[1] != d:
+        raise ValueError("weight must be [V, d]")
+    dev = hidden.device
+    if out is None:
+        out = {k: torch.empty((N, C), dtype=torch.float32, device=dev) for k in ("logp", "lse", "w")}
+        out["loss"] = torch.empty((1,), dtype=torch.float32, device=dev)
+    need = ctypes.c_size_t(0)
+    _check(_lib.grpo_lmhead_workspace_size(N, C, V, d, ctypes.byref(need)),
+           "grpo_lmhead_workspace_size")
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
+    out["workspace"] = workspace
+    _check(_lib.grpo_lmhead_loss_fwd(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
+                                     _ptr(lens), _ptr(adv), _ptr(old_logp), _ptr(ref_logp),
+                                     float(eps), float(beta), float(norm), _ptr(out["logp"]),
+                                     _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)),
+           "grpo_lmhead_loss_fwd")
+    return out
+
+
+def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=None, out=None,
+                         workspace=None, stream=None):
+    """Gradients of ``grad_loss * loss`` with respect to the hidden states and
+    the LM head.  Returns ``(dhidden [N, P+C, d], dweight [V, d], workspace)``,
+    float32; ``out`` = (dhidden, dweight) to reuse buffers."""
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(weight, "weight", torch.bfloat16)
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("lse", lse, torch.float32), ("w", w, torch.float32),
+                        ("grad_loss", grad_loss, torch.float32)):
+        _dev(t, name, dt)
+    N, T, d = hidden.shape
+    V = weight.shape[0]
+    C = T - P
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty((N, T, d), dtype=torch.float32, device=dev),
+               torch.empty((V, d), dtype=torch.float32, device=dev))
+    need = ctypes.c_size_t(0)
+    _check(_lib.grpo_lmhead_bwd_workspace_size(N, C, V, d, ctypes.byref(need)),
+           "grpo_lmhead_bwd_workspace_size")
+    if workspace is None or workspace.numel() < need.value:
+        workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
+    _check(_lib.grpo_lmhead_loss_bwd(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
+                                     _ptr(lens), _ptr(lse), _ptr(w), _ptr(grad_loss),
+                                     _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "grpo_lmhead_loss_bwd")
     return out[0], out[1], workspace
 
 

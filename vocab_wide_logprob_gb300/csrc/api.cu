@@ -398,21 +398,47 @@ grpo_status grpo_lmhead_workspace_size(int64_t N, int64_t C, int64_t V, int64_t 
   return GRPO_OK;
 }
 
-grpo_status grpo_lmhead_logprobs(const void* hidden, const void* weight, int64_t N, int64_t P,
-                                 int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
-                                 const int32_t* len, float* logp, float* lse, void* workspace,
-                                 size_t workspace_bytes, grpo_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the LM-head calls (bf16 hidden [N, P+C, d], weight [V, d]).
+grpo_status lmhead_check(const void* hidden, const void* weight, int64_t N, int64_t P, int64_t C,
+                         int64_t V, int64_t d, const int64_t* input_ids, const int32_t* len,
+                         const void* workspace) {
   grpo_status s = check_shapes(GRPO_BF16, N, P, C, V);
   if (s != GRPO_OK) return s;
   if (d < 64 || d % 64 != 0) return GRPO_ERR_UNSUPPORTED;
   if (V > (int64_t)INT32_MAX - 256 || mul3(N, P + C, d) < 0) return GRPO_ERR_UNSUPPORTED;
   if (workspace == nullptr || (N > 0 && len == nullptr)) return GRPO_ERR_INVALID_ARG;
-  if (N > 0 && C > 0 &&
-      (hidden == nullptr || weight == nullptr || input_ids == nullptr || logp == nullptr ||
-       lse == nullptr))
+  if (N > 0 && C > 0 && (hidden == nullptr || weight == nullptr || input_ids == nullptr))
     return GRPO_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(input_ids, 8) || !aligned(len, 4) ||
-      !aligned(logp, 4) || !aligned(lse, 4) || !aligned(workspace, 256))
+      !aligned(workspace, 256))
+    return GRPO_ERR_MISALIGNED;
+  return GRPO_OK;
+}
+
+// mode 0: log-probs only; 1: log-probs, then the loss.
+grpo_status lmhead_fwd_impl(const void* hidden, const void* weight, int64_t N, int64_t P, int64_t C,
+                            int64_t V, int64_t d, const int64_t* input_ids, const int32_t* len,
+                            const float* adv, const float* old_logp, const float* ref_logp,
+                            float eps, float beta, float norm, float* logp, float* lse, float* w,
+                            float* loss, void* workspace, size_t workspace_bytes,
+                            grpo_stream_t stream, int mode) {
+  grpo_status s = lmhead_check(hidden, weight, N, P, C, V, d, input_ids, len, workspace);
+  if (s != GRPO_OK) return s;
+  if (N > 0 && C > 0 && (logp == nullptr || lse == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (mode == 1) {
+    if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) ||
+        isinf(norm))
+      return GRPO_ERR_INVALID_ARG;
+    if (loss == nullptr || (N > 0 && adv == nullptr) || (N > 0 && C > 0 && w == nullptr))
+      return GRPO_ERR_INVALID_ARG;
+    if (beta != 0.f && ref_logp == nullptr && N > 0 && C > 0) return GRPO_ERR_INVALID_ARG;
+  }
+  if (!aligned(logp, 4) || !aligned(lse, 4) || !aligned(adv, 4) || !aligned(old_logp, 4) ||
+      !aligned(ref_logp, 4) || !aligned(w, 4) || !aligned(loss, 4))
     return GRPO_ERR_MISALIGNED;
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -425,13 +451,111 @@ grpo_status grpo_lmhead_logprobs(const void* hidden, const void* weight, int64_t
   a.V = V;
   a.ids = input_ids;
   a.len = len;
+  a.adv = adv;
+  a.old_logp = old_logp;
+  a.ref_logp = beta != 0.f ? ref_logp : nullptr;
+  a.eps = eps;
+  a.beta = beta;
+  a.norm = norm;
+  a.agg = 0;
   a.logp = logp;
   a.lse = lse;
+  a.w = w;
+  a.loss = loss;
   a.ws = workspace;
   const cudaStream_t st = (cudaStream_t)stream;
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
-  if (N == 0 || C == 0) return GRPO_OK;
-  return from_cuda(launch_lmhead(hidden, weight, a, d, dev, st));
+  if (N == 0 || C == 0)
+    return mode == 1 ? from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st)) : GRPO_OK;
+  cudaError_t e = launch_lmhead(hidden, weight, a, d, dev, st);
+  if (e != cudaSuccess || mode == 0) return from_cuda(e);
+  return from_cuda(launch_surrogate(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_lmhead_logprobs(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                 const int32_t* len, float* logp, float* lse, void* workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream) {
+  return lmhead_fwd_impl(hidden, weight, N, P, C, V, d, input_ids, len, nullptr, nullptr, nullptr,
+                         0.f, 0.f, 0.f, logp, lse, nullptr, nullptr, workspace, workspace_bytes,
+                         stream, 0);
+}
+
+grpo_status grpo_lmhead_loss_fwd(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                 const int32_t* len, const float* adv, const float* old_logp,
+                                 const float* ref_logp, float eps, float beta, float norm,
+                                 float* logp, float* lse, float* w, float* loss, void* workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream) {
+  return lmhead_fwd_impl(hidden, weight, N, P, C, V, d, input_ids, len, adv, old_logp, ref_logp,
+                         eps, beta, norm, logp, lse, w, loss, workspace, workspace_bytes, stream,
+                         1);
+}
+
+grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
+                                           size_t* bytes) {
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1 || d < 64 || d % 64 != 0)
+    return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
+  if (V > (int64_t)INT32_MAX - 256) return GRPO_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  *bytes = lm_bwd_layout(N, C, V, d, dev.sms).total;
+  return GRPO_OK;
+}
+
+grpo_status grpo_lmhead_loss_bwd(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                 const int32_t* len, const float* lse, const float* w,
+                                 const float* grad_loss, float* dhidden, float* dweight,
+                                 void* workspace, size_t workspace_bytes, grpo_stream_t stream) {
+  grpo_status s = lmhead_check(hidden, weight, N, P, C, V, d, input_ids, len, workspace);
+  if (s != GRPO_OK) return s;
+  if (dweight == nullptr || (N > 0 && dhidden == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (N > 0 && C > 0 && (lse == nullptr || w == nullptr)) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(w, 4) || !aligned(grad_loss, 4) || !aligned(dhidden, 16) ||
+      !aligned(dweight, 16))
+    return GRPO_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (workspace_bytes < lm_bwd_layout(N, C, V, d, dev.sms).total) return GRPO_ERR_WORKSPACE;
+  FwdArgs f = {};
+  f.N = N;
+  f.P = P;
+  f.C = C;
+  f.V = V;
+  f.len = len;
+  f.ws = workspace;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (launch_prep(f, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (N == 0 || C == 0) {  // nothing is scored: both gradients are zero
+    if (cudaMemsetAsync(dweight, 0, (size_t)V * (size_t)d * 4, st) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    const int64_t nh = mul3(N, P + C, d);
+    return nh == 0 ? GRPO_OK : from_cuda(cudaMemsetAsync(dhidden, 0, (size_t)nh * 4, st));
+  }
+  LmBwdArgs a;
+  a.hidden = hidden;
+  a.weight = weight;
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.d = d;
+  a.ids = input_ids;
+  a.lse = lse;
+  a.w = w;
+  a.grad = grad_loss;
+  a.dhidden = dhidden;
+  a.dweight = dweight;
+  a.ws = workspace;
+  cudaError_t e = launch_lmhead_dz(a, dev, st);
+  if (e != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_lmhead_grads(a, dev, st));
 }
 
 grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {

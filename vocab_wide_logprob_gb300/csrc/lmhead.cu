@@ -8,7 +8,8 @@
 //
 // Pipeline (one CTA per SM, persistent):
 //   gather_rows_kernel   copies the hidden state of every scored row into a
-//                        dense [rows, d] buffer (row r = valid token r)
+//                        dense [rows, d] buffer (row r = valid token r) and
+//                        zeroes the rows up to the next multiple of 128
 //   lmhead_lse_kernel    work items (block of 128 rows, range of vocabulary
 //                        tiles of 256).  Warp 0 issues TMA loads of a 128x64
 //                        slab of H and a 256x64 slab of W per k-step into a
@@ -22,12 +23,14 @@
 //   lmhead_merge_kernel  merges a row's partials in order (deterministic) into
 //                        lse and logp = z_y - lse, and zeroes positions past
 //                        each length.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+//
+// The backward ("loss.backward()" through the projection) recomputes the
+// logits with the same pipeline: lmhead_dz_kernel's epilogue turns each tile
+// into the logits gradient g * w_t * (onehot(y_t) - exp(z - lse_t)), rounded
+// to bf16, and stores it for the two gradient contractions (lmhead_bwd.cu).
 #include <mutex>
 
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace grpo {
 namespace {
@@ -41,41 +44,47 @@ constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB
 constexpr int kStageBytesLm = kABytes + kBBytes;
 constexpr int kLmThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kMaxSplits = 256;  // = kThreads: one candidate per thread
+constexpr uint32_t kIdescLm = umma_idesc(kBM, kBN, false, false);
 
 struct LmParams {
   int64_t N, P, C, V, d;
   const int32_t* offsets;  // prefix sums of the clamped lengths ([N+1])
-  int4* geometry;          // (row blocks, splits, tiles per split): written by the gather
-  float4* partials;        // [items][kBM] (max, sum, target logit, has target)
+  int4* geometry;          // [0] (row blocks, splits, tiles per split): written by the gather
+  float4* partials;        // forward: [items][kBM] (max, sum, target logit, has target)
   WsHeader* hdr;
   int sms;                 // CTAs in the grid: the split count is chosen from it
+  // logits-gradient pass only
+  const float* lse;        // [N, C] from the forward
+  const float* w;          // [N, C] d loss / d logp from the forward
+  const float* grad;       // upstream scalar gradient (nullable: 1)
+  uint16_t* dz;            // bf16 [rows, ldz]
+  int64_t ldz;
 };
 
-// Row blocks and vocabulary splits for t_valid rows, computed once by the
-// first CTA of gather_rows_kernel and read by the later kernels.  Candidate
-// split counts s = 1 .. 256 (one per thread) are scored by how well their work
-// items (row block, 1/s of the vocabulary tiles) fill the grid's rounds,
-// counting both the items per round and the uneven last split of tiles; the
-// smallest s within 0.01 of the best score wins (less merging, and every split
-// re-reads its row block).  items = mb * s never exceeds 4 * sms + 2 * mb, the
-// size of the partials buffer.
-__device__ float lm_split_score(int32_t mb, int32_t sp, int32_t ntiles, int sms) {
-  const int32_t items = mb * sp;
-  if (sp > ntiles || items > 4 * sms + 2 * mb) return -1.f;
+// Split `ksteps` steps of work for each of `units` independent tiles into
+// `splits` ranges so that the items (unit, range) fill the grid's rounds,
+// counting both the items per round and the uneven last range; every range
+// is non-empty and items <= max_items.  Candidate split counts 1 .. 256, one
+// per thread of the calling CTA (kThreads threads); the smallest within 0.01
+// of the best score wins (fewer partials to merge, and every range re-reads
+// its unit's operand).  Returns (splits, steps per split).
+__device__ float split_score(int32_t units, int32_t sp, int32_t ksteps, int sms,
+                             int32_t max_items) {
+  const int32_t items = units * sp;
+  if (sp > ksteps || items > max_items) return -1.f;
+  const int32_t sps = (ksteps + sp - 1) / sp;
+  if ((int64_t)sps * (sp - 1) >= ksteps) return -1.f;  // the last range would be empty
   const int32_t rounds = (items + sms - 1) / sms;
-  const int32_t tps = (ntiles + sp - 1) / sp;
-  return (float)items / (float)(rounds * sms) * (float)ntiles / (float)(tps * sp);
+  return (float)items / (float)(rounds * sms) * (float)ksteps / (float)(sps * sp);
 }
 
-// Called by all kThreads (= kMaxSplits) threads of one CTA.
-__device__ int4 lm_geometry_block(int64_t t_valid, int64_t V, int sms) {
+__device__ int2 choose_split_block(int32_t units, int32_t ksteps, int sms, int32_t max_items) {
   __shared__ float s_best[kWarps];
   __shared__ int s_pick[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t ntiles = (int32_t)((V + kBN - 1) / kBN);
-  const int32_t mb = (int32_t)((t_valid + kBM - 1) / kBM);
   const int32_t sp = tid + 1;
-  const float score = mb > 0 ? lm_split_score(mb, sp, ntiles, sms) : (sp == 1 ? 1.f : -1.f);
+  const float score =
+      units > 0 ? split_score(units, sp, ksteps, sms, max_items) : (sp == 1 ? 1.f : -1.f);
   float best = score;
   for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
   if (lane == 0) s_best[warp] = best;
@@ -89,108 +98,81 @@ __device__ int4 lm_geometry_block(int64_t t_valid, int64_t V, int sms) {
   pick = s_pick[0];
   for (int k = 1; k < kWarps; ++k) pick = min(pick, s_pick[k]);
   if (pick > kMaxSplits) pick = 1;
-  return make_int4(mb, pick, (ntiles + pick - 1) / pick, 0);
-}
-
-// ---- tensor memory and tcgen05 helpers ----------------------------------------
-
-__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr) {
-  uint64_t dsc = 0;
-  dsc |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
-  dsc |= (uint64_t)1 << 16;                   // leading byte offset (unused: 128-byte swizzle)
-  dsc |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 bytes
-  dsc |= (uint64_t)1 << 46;                   // descriptor version
-  dsc |= (uint64_t)2 << 61;                   // layout: 128-byte swizzle, K-major
-  return dsc;
-}
-
-// D (f32) += A (bf16, K-major) * B (bf16, K-major)^T, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
-
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t ad, uint64_t bd, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(ad), "l"(bd), "r"(kIdesc), "r"(acc)
-      : "memory");
-}
-// Arrive on the mbarrier once every tcgen05 operation issued so far is done.
-__device__ __forceinline__ void umma_commit(uint32_t mbar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
-      "%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* map, int x, int y,
-                                            uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(sdst),
-      "l"(map), "r"(x), "r"(y), "r"(mbar)
-      : "memory");
+  return make_int2(pick, (ksteps + pick - 1) / pick);
 }
 
 // ---- gather: dense [rows, d] copy of the scored rows' hidden states ----------
 
+// geometry[0]: the projection pass (row blocks, vocabulary splits, tiles per
+// split, 0).  With `grad_gemm`, geometry[1]: the hidden-state gradient
+// contraction (row blocks, 256-wide d tiles, vocabulary splits, 64-wide
+// k-steps per split).
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                                                uint16_t* __restrict__ dense,
                                                                const int32_t* __restrict__ off,
                                                                int64_t N, int64_t T, int64_t P,
                                                                int64_t d, int64_t V, int sms,
-                                                               int4* __restrict__ geometry) {
+                                                               int4* __restrict__ geometry,
+                                                               int grad_gemm) {
   pdl_wait();
   pdl_trigger();
   const int64_t tv = off[N];
+  const int32_t mb = (int32_t)((tv + kBM - 1) / kBM);
   if (blockIdx.x == 0) {
-    const int4 g = lm_geometry_block(tv, V, sms);
-    if (threadIdx.x == 0) *geometry = g;
+    const int32_t ntiles = (int32_t)((V + kBN - 1) / kBN);
+    const int2 s = choose_split_block(mb, ntiles, sms, 4 * sms + 2 * mb);
+    if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
+  }
+  if (grad_gemm && blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
+    const int32_t nb = (int32_t)((d + 255) / 256);
+    const int32_t ksteps = (int32_t)((V + kBN - 1) / kBN) * (kBN / kBK);
+    const int2 s = choose_split_block(mb * nb, ksteps, sms, 2 * sms + mb * nb);
+    if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
   }
   const int64_t vec_per_row = d / 8;  // 16-byte vectors
-  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < tv * vec_per_row;
+  const int64_t rows_pad = (int64_t)mb * kBM;
+  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < rows_pad * vec_per_row;
        k += (int64_t)gridDim.x * kThreads) {
     const int64_t r = k / vec_per_row, c = k - r * vec_per_row;
-    int lo = 0, hi = (int)N;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (off[mid] <= r)
-        lo = mid;
-      else
-        hi = mid;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);  // rows past the last scored one read as zeros
+    if (r < tv) {
+      int lo = 0, hi = (int)N;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= r)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      const int64_t t = r - off[lo];
+      const uint4* src =
+          reinterpret_cast<const uint4*>(hidden + ((int64_t)lo * T + P - 1 + t) * d);
+      v = ld_stream(src + c);
     }
-    const int64_t t = r - off[lo];
-    const uint4* src = reinterpret_cast<const uint4*>(hidden + ((int64_t)lo * T + P - 1 + t) * d);
-    reinterpret_cast<uint4*>(dense + r * d)[c] = ld_stream(src + c);
+    reinterpret_cast<uint4*>(dense + r * d)[c] = v;
   }
 }
 
-// ---- the tensor-core kernel -----------------------------------------------------
+// ---- the tensor-core pipeline ----------------------------------------------------
 
-__global__ void __launch_bounds__(kLmThreads, 1)
-    lmhead_lse_kernel(const __grid_constant__ CUtensorMap map_h,
-                      const __grid_constant__ CUtensorMap map_w, const int64_t* __restrict__ ids,
-                      const LmParams p) {
+// Completion of the valid token r (binary search over the offsets).
+__device__ __forceinline__ int completion_of(const int32_t* off, int64_t N, int64_t r) {
+  int lo = 0, hi = (int)N;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= r)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// kMode 0: log-sum-exp partials per row; kMode 1: the bf16 logits gradient.
+template <int kMode>
+__device__ __forceinline__ void lm_tile_pipeline(const CUtensorMap* map_h, const CUtensorMap* map_w,
+                                                 const int64_t* __restrict__ ids,
+                                                 const LmParams& p) {
   extern __shared__ __align__(1024) unsigned char lm_smem[];
   __shared__ __align__(8) uint64_t s_full[kLmStages];
   __shared__ __align__(8) uint64_t s_empty[kLmStages];
@@ -215,12 +197,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
     mbar_init_fence();
   }
-  if (warp == 1) {  // two 256-column fp32 accumulators: all 512 TMEM columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                     smem_u32(&s_tmem))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc(&s_tmem, 512);  // two 256-column fp32 accumulators
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
@@ -229,7 +206,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   pdl_trigger();
 
   const int64_t tv = p.offsets[p.N];
-  const int4 geo = *p.geometry;
+  const int4 geo = p.geometry[0];
   const int64_t mb = geo.x, splits = geo.y, tps = geo.z;
   const int64_t ntiles = (p.V + kBN - 1) / kBN;
   const int64_t items = mb * splits;
@@ -253,8 +230,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const uint32_t full = smem_u32(&s_full[stage]);
             const uint32_t sa = ring_u32 + stage * kStageBytesLm;
             mbar_arrive_expect_tx(full, kStageBytesLm);
-            tma_load_2d(sa, &map_h, kb * kBK, (int)(rb * kBM), full);
-            tma_load_2d(sa + kABytes, &map_w, kb * kBK, (int)(n * kBN), full);
+            tma_load_2d(sa, map_h, kb * kBK, (int)(rb * kBM), full);
+            tma_load_2d(sa + kABytes, map_w, kb * kBK, (int)(n * kBN), full);
             if (++stage == kLmStages) {
               stage = 0;
               phase ^= 1u;
@@ -294,8 +271,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const uint32_t sa = ring_u32 + stage * kStageBytesLm;
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
-              umma(dacc, umma_sdesc(sa + j * 32), umma_sdesc(sa + kABytes + j * 32),
-                   (kb | j) ? 1u : 0u);
+              umma_bf16(dacc, umma_desc_k(sa + j * 32), umma_desc_k(sa + kABytes + j * 32),
+                        kIdescLm, (kb | j) ? 1u : 0u);
             umma_commit(smem_u32(&s_empty[stage]));  // the stage is free once these finish
             if (++stage == kLmStages) {
               stage = 0;
@@ -318,21 +295,21 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     int buf = 0;
     uint32_t aphase = 0;
     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const float g = (kMode == 1 && p.grad != nullptr) ? __ldg(p.grad) : 1.f;
     for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
       const int64_t rb = it / splits, sp = it - rb * splits;
       const int64_t n0 = sp * tps, n1 = min(ntiles, n0 + tps);
       const int64_t r = rb * kBM + row_in_block;  // valid token of this thread
       int64_t y = -1;
+      float lse_r = 0.f, coef = 0.f;
       if (r < tv) {
-        int lo = 0, hi = (int)p.N;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.offsets[mid] <= r)
-            lo = mid;
-          else
-            hi = mid;
+        const int i = completion_of(p.offsets, p.N, r);
+        const int64_t t = r - p.offsets[i];
+        y = __ldg(ids + (int64_t)i * (p.P + p.C) + p.P + t);
+        if (kMode == 1) {
+          lse_r = __ldg(p.lse + (int64_t)i * p.C + t);
+          coef = g * __ldg(p.w + (int64_t)i * p.C + t);
         }
-        y = __ldg(ids + (int64_t)lo * (p.P + p.C) + p.P + (r - p.offsets[lo]));
       }
       float m = -INFINITY, s_extra = 0.f, zy = 0.f;
       uint64_t acc01 = f2_pack(0.f, 0.f), acc23 = f2_pack(0.f, 0.f);
@@ -353,36 +330,79 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           float v[32];
           tmem_ld32(tbase + (uint32_t)c, v);
           const int64_t v0 = vbase + c;
-          if (v0 + 32 > p.V) {  // the vocabulary's last tile: columns past V do not exist
+          if constexpr (kMode == 0) {
+            if (v0 + 32 > p.V) {  // the vocabulary's last tile: columns past V do not exist
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (v0 + j >= p.V) v[j] = -INFINITY;
-          }
-          if (y >= v0 && y < v0 + 32) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (v0 + j == y) zy = v[j];
-            has = true;
-          }
-          float bm = v[0];
-#pragma unroll
-          for (int j = 1; j < 32; ++j) bm = fmaxf(bm, v[j]);
-          if (bm > m) {
-            const float sc = ex2((m - bm) * kLog2e);
-            const uint64_t sc2 = f2_pack(sc, sc);
-            acc01 = f2_mul(acc01, sc2);
-            acc23 = f2_mul(acc23, sc2);
-            s_extra *= sc;
-            m = bm;
-          }
-          if (m != -INFINITY) {
-            const float mL = m * kLog2e;
-            const uint64_t nmL2 = f2_pack(-mL, -mL);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              acc01 = f2_add(acc01, f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nmL2)));
-              acc23 = f2_add(acc23, f2_ex2(f2_fma(f2_pack(v[j + 2], v[j + 3]), L2, nmL2)));
+              for (int j = 0; j < 32; ++j)
+                if (v0 + j >= p.V) v[j] = -INFINITY;
             }
+            if (y >= v0 && y < v0 + 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (v0 + j == y) zy = v[j];
+              has = true;
+            }
+            float bm = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) bm = fmaxf(bm, v[j]);
+            if (bm > m) {
+              const float sc = ex2((m - bm) * kLog2e);
+              const uint64_t sc2 = f2_pack(sc, sc);
+              acc01 = f2_mul(acc01, sc2);
+              acc23 = f2_mul(acc23, sc2);
+              s_extra *= sc;
+              m = bm;
+            }
+            if (m != -INFINITY) {
+              const float mL = m * kLog2e;
+              const uint64_t nmL2 = f2_pack(-mL, -mL);
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                acc01 = f2_add(acc01, f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nmL2)));
+                acc23 = f2_add(acc23, f2_ex2(f2_fma(f2_pack(v[j + 2], v[j + 3]), L2, nmL2)));
+              }
+            }
+          } else {
+            // dz = coef * (onehot(y) - 2^(z log2 e - lse log2 e)), bf16 (round to nearest even)
+            const float lL = lse_r * kLog2e;
+            const uint64_t nlL2 = f2_pack(-lL, -lL);
+            const uint64_t nc2 = f2_pack(-coef, -coef);
+            uint32_t pk[16];
+            if (y >= v0 && y < v0 + 32) {
+              // the target column: coef * (1 - p_y) without cancellation, -expm1(z_y - lse)
+              float zy_ = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (v0 + j == y) zy_ = v[j];
+              const float dy = coef * -expm1f(zy_ - lse_r);
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float a, b;
+                f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
+                a = (v0 + j == y) ? dy : a;
+                b = (v0 + j + 1 == y) ? dy : b;
+                pk[j / 2] = pack_bf16x2(a, b);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float a, b;
+                f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
+                pk[j / 2] = pack_bf16x2(a, b);
+              }
+            }
+            if (r >= tv) {  // padding rows of the last block: zeros
+#pragma unroll
+              for (int j = 0; j < 16; ++j) pk[j] = 0u;
+            } else if (v0 + 32 > p.V) {  // columns past V: zeros
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (v0 + j >= p.V) pk[j >> 1] &= (j & 1) ? 0x0000ffffu : 0xffff0000u;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.dz + r * p.ldz + v0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
         }
         tmem_fence_before();
@@ -394,11 +414,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
       }
       if (!ok) break;
-      float a0, a1, a2, a3;
-      f2_unpack(acc01, a0, a1);
-      f2_unpack(acc23, a2, a3);
-      const float s = ((a0 + a1) + (a2 + a3)) + s_extra;
-      if (r < tv) p.partials[it * kBM + row_in_block] = make_float4(m, s, zy, has ? 1.f : 0.f);
+      if constexpr (kMode == 0) {
+        float a0, a1, a2, a3;
+        f2_unpack(acc01, a0, a1);
+        f2_unpack(acc23, a2, a3);
+        const float s = ((a0 + a1) + (a2 + a3)) + s_extra;
+        if (r < tv) p.partials[it * kBM + row_in_block] = make_float4(m, s, zy, has ? 1.f : 0.f);
+      }
     }
   }
 
@@ -408,8 +430,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tmem_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    tmem_dealloc(tmem, 512);
   }
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_lse_kernel(const __grid_constant__ CUtensorMap map_h,
+                      const __grid_constant__ CUtensorMap map_w, const int64_t* __restrict__ ids,
+                      const LmParams p) {
+  lm_tile_pipeline<0>(&map_h, &map_w, ids, p);
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_dz_kernel(const __grid_constant__ CUtensorMap map_h,
+                     const __grid_constant__ CUtensorMap map_w, const int64_t* __restrict__ ids,
+                     const LmParams p) {
+  lm_tile_pipeline<1>(&map_h, &map_w, ids, p);
 }
 
 // ---- merge: partials of a row in split order -> lse, logp ----------------------
@@ -476,15 +512,50 @@ cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
   return cudaSuccess;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, d] matrix, box 64 x box_rows,
-// 128-byte swizzle (rows past `rows` read as zeros).
-cudaError_t encode_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t d, int box_rows) {
+LmParams lm_params(const int32_t* off, int4* geometry, WsHeader* hdr, int64_t N, int64_t P,
+                   int64_t C, int64_t V, int64_t d, int sms) {
+  LmParams p = {};
+  p.N = N;
+  p.P = P;
+  p.C = C;
+  p.V = V;
+  p.d = d;
+  p.offsets = off;
+  p.geometry = geometry;
+  p.hdr = hdr;
+  p.sms = sms;
+  return p;
+}
+
+template <typename K>
+cudaError_t launch_tiles(K kern, const void* dense, const void* weight, int64_t rows, int64_t d,
+                         int64_t V, const int64_t* ids, const LmParams& p, const DeviceInfo& dev,
+                         cudaStream_t st, bool* attr_done) {
+  CUtensorMap map_h, map_w;
+  cudaError_t e;
+  if ((e = encode_bf16_2d(&map_h, dense, d, rows, d, kBM)) != cudaSuccess) return e;
+  if ((e = encode_bf16_2d(&map_w, weight, d, V, d, kBN)) != cudaSuccess) return e;
+  const int smem = kLmStages * kStageBytesLm + 1024;
+  if (!*attr_done) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+      return e;
+    *attr_done = true;
+  }
+  return launch_pdl(kern, dim3((unsigned)dev.sms), dim3(kLmThreads), (size_t)smem, st, 1, map_h,
+                    map_w, ids, p);
+}
+
+}  // namespace
+
+cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                           int64_t pitch, int box_outer) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   cudaError_t e = get_encoder(&enc);
   if (e != cudaSuccess) return e;
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -492,18 +563,32 @@ cudaError_t encode_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-}  // namespace
-
 LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms) {
   LmLayout l;
   const WsLayout base = ws_layout(N);
   const int64_t rows = N * C;
-  l.geometry = base.total;  // 16 bytes
-  l.dense = align_up(base.total + 16, 1024);
-  l.partials = align_up(l.dense + (size_t)rows * (size_t)d * 2, 256);
   const int64_t mb_max = (rows + kBM - 1) / kBM;
+  l.geometry = base.total;  // 2 x int4
+  l.dense = align_up(base.total + 32, 1024);
+  l.partials = align_up(l.dense + (size_t)(mb_max * kBM) * (size_t)d * 2, 256);
   const int64_t items_max = 4 * (int64_t)sms + 2 * mb_max;  // mb * splits bound
   l.total = align_up(l.partials + (size_t)items_max * kBM * sizeof(float4), 256);
+  return l;
+}
+
+LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms) {
+  LmBwdLayout l;
+  const WsLayout base = ws_layout(N);
+  const int64_t mb_max = (N * C + kBM - 1) / kBM;
+  l.rows_cap = mb_max * kBM;
+  l.ldz = (V + kBN - 1) / kBN * kBN;
+  const int64_t nb = (d + 255) / 256;
+  l.items_max = 2 * (int64_t)sms + mb_max * nb;
+  l.geometry = base.total;
+  l.dense = align_up(base.total + 32, 1024);
+  l.dz = align_up(l.dense + (size_t)l.rows_cap * (size_t)d * 2, 1024);
+  l.dh_partials = align_up(l.dz + (size_t)l.rows_cap * (size_t)l.ldz * 2, 1024);
+  l.total = align_up(l.dh_partials + (size_t)l.items_max * kBM * 256 * sizeof(float), 256);
   return l;
 }
 
@@ -514,46 +599,49 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   char* ws = static_cast<char*>(a.ws);
   const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
   uint16_t* dense = reinterpret_cast<uint16_t*>(ws + ll.dense);
-  const int64_t rows = a.N * a.C;
+  const int64_t rows = (a.N * a.C + kBM - 1) / kBM * kBM;
 
   int4* geometry = reinterpret_cast<int4*>(ws + ll.geometry);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(hidden), dense, off, a.N,
-                             a.P + a.C, a.P, d, a.V, dev.sms, geometry);
+                             a.P + a.C, a.P, d, a.V, dev.sms, geometry, 0);
   if (e != cudaSuccess) return e;
 
-  CUtensorMap map_h, map_w;
-  if ((e = encode_2d(&map_h, dense, rows, d, kBM)) != cudaSuccess) return e;
-  if ((e = encode_2d(&map_w, weight, a.V, d, kBN)) != cudaSuccess) return e;
-
-  LmParams p;
-  p.N = a.N;
-  p.P = a.P;
-  p.C = a.C;
-  p.V = a.V;
-  p.d = d;
-  p.offsets = off;
-  p.geometry = geometry;
+  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, d,
+                         dev.sms);
   p.partials = reinterpret_cast<float4*>(ws + ll.partials);
-  p.hdr = reinterpret_cast<WsHeader*>(ws);
-  p.sms = dev.sms;
-
-  const int smem = kLmStages * kStageBytesLm + 1024;
   static bool attr_done = false;
-  if (!attr_done) {
-    if ((e = cudaFuncSetAttribute(lmhead_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  smem)) != cudaSuccess)
-      return e;
-    attr_done = true;
-  }
-  e = launch_pdl(lmhead_lse_kernel, dim3((unsigned)dev.sms), dim3(kLmThreads), (size_t)smem, st, 1,
-                 map_h, map_w, a.ids, p);
-  if (e != cudaSuccess) return e;
-  int64_t blocks = (rows + kThreads - 1) / kThreads;
+  if ((e = launch_tiles(lmhead_lse_kernel, dense, weight, rows, d, a.V, a.ids, p, dev, st,
+                        &attr_done)) != cudaSuccess)
+    return e;
+  int64_t blocks = (a.N * a.C + kThreads - 1) / kThreads;
   if (blocks > 1024) blocks = 1024;
   if (blocks < 1) blocks = 1;
   return launch_pdl(lmhead_merge_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1, p,
                     a.ids, a.logp, a.lse, reinterpret_cast<const int32_t*>(ws + wl.lens));
+}
+
+cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {
+  const WsLayout wl = ws_layout(a.N);
+  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms);
+  char* ws = static_cast<char*>(a.ws);
+  const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
+  uint16_t* dense = reinterpret_cast<uint16_t*>(ws + bl.dense);
+  int4* geometry = reinterpret_cast<int4*>(ws + bl.geometry);
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
+                             st, 1, static_cast<const uint16_t*>(a.hidden), dense, off, a.N,
+                             a.P + a.C, a.P, a.d, a.V, dev.sms, geometry, 1);
+  if (e != cudaSuccess) return e;
+  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, a.d,
+                         dev.sms);
+  p.lse = a.lse;
+  p.w = a.w;
+  p.grad = a.grad;
+  p.dz = reinterpret_cast<uint16_t*>(ws + bl.dz);
+  p.ldz = bl.ldz;
+  static bool attr_done = false;
+  return launch_tiles(lmhead_dz_kernel, dense, a.weight, bl.rows_cap, a.d, a.V, a.ids, p, dev,
+                      st, &attr_done);
 }
 
 }  // namespace grpo
