@@ -302,7 +302,7 @@ grpo_status grpo_loss_fwd_bwd_ex(const void *logits, grpo_dtype dtype, int64_t N
  *
  * hidden [N, P+C, d] bfloat16 (row P-1+t of sequence i scores token t);
  * weight [V, d] bfloat16 (the LM head, row v = the output embedding of token
- * v); both 16-byte aligned; d a multiple of 64.  input_ids, len, logp, lse as
+ * v); both 16-byte aligned; d a multiple of 128.  input_ids, len, logp, lse as
  * for grpo_logprobs (0 past each length).  workspace: at least
  * grpo_lmhead_workspace_size bytes (it holds a dense copy of the scored rows'
  * hidden states, 2*d bytes per completion token, and a few KB of partials).

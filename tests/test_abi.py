@@ -164,9 +164,11 @@ def test_extended_entry_validation(lib):
     assert lib.grpo_loss_fwd_ex(a, 1, 8, 4, 8, 64, A(0x20000), A(0x30000), A(0x40000), None, None,
                                 0.2, 0.0, 0.0, 5, A(0x50000), A(0x60000), A(0x70000), A(0x80000),
                                 A(0x100000), 1 << 20, None) == UNSUPPORTED
-    # LM head: hidden size a multiple of 64, 16-byte aligned operands
+    # LM head: hidden size a multiple of 128, 16-byte aligned operands
     args = [a, A(0x200000), 8, 4, 8, 1000, 96, A(0x20000), A(0x30000), A(0x40000), A(0x50000),
             A(0x100000), 1 << 30, None]
+    assert lib.grpo_lmhead_logprobs(*args) == UNSUPPORTED
+    args[6] = 192
     assert lib.grpo_lmhead_logprobs(*args) == UNSUPPORTED
     args[6] = 128
     args[0] = A(0x10008)

@@ -31,7 +31,7 @@ def _run(w, d, device_gen=False):
     return hidden, weight, ids, lens.cpu().numpy(), lp.cpu().numpy(), lse.cpu().numpy(), status
 
 
-@pytest.mark.parametrize("V,d", [(1000, 64), (1000, 128), (4099, 192), (151936, 896)])
+@pytest.mark.parametrize("V,d", [(1000, 128), (1000, 256), (4099, 384), (151936, 896)])
 def test_lmhead_small(V, d):
     w = wl.variant(wl.QWEN_G8, name=f"lm_{V}_{d}", B=1, G=4, P=8, C=24, V=V, seed=60 + d,
                    eos_id=min(wl.QWEN25_EOS, V - 1))
@@ -86,8 +86,8 @@ def test_lmhead_many_row_blocks_sampled():
 def test_lmhead_bad_token_reported():
     w = wl.variant(wl.QWEN_G8, name="lm_bad", B=1, G=4, P=8, C=24, V=1000, eos_id=999, seed=5)
     g = H.g()
-    hidden = wl.make_hidden(w, 64).cuda()
-    weight = wl.make_lm_head(w, 64).cuda()
+    hidden = wl.make_hidden(w, 128).cuda()
+    weight = wl.make_lm_head(w, 128).cuda()
     ids = wl.make_ids(w)
     ids[0, w.P + 2] = 5000
     t_ids = torch.from_numpy(ids).cuda()
@@ -97,7 +97,7 @@ def test_lmhead_bad_token_reported():
     assert np.isnan(lp[0, 2].item())
 
 
-@pytest.mark.parametrize("V,d,B,G,C", [(200, 64, 1, 2, 3), (256, 128, 1, 1, 1), (257, 64, 2, 2, 5)],
+@pytest.mark.parametrize("V,d,B,G,C", [(200, 128, 1, 2, 3), (256, 128, 1, 1, 1), (257, 256, 2, 2, 5)],
                          ids=["V_below_tile", "one_row", "V_tile_plus_one"])
 def test_lmhead_edge_shapes(V, d, B, G, C):
     w = wl.variant(wl.QWEN_G8, name=f"lm_edge_{V}", B=B, G=G, P=3, C=C, V=V, eos_id=V - 1,
@@ -110,8 +110,8 @@ def test_lmhead_edge_shapes(V, d, B, G, C):
 
 def test_lmhead_empty_batch():
     g = H.g()
-    hidden = torch.zeros((0, 6, 64), dtype=torch.bfloat16, device="cuda")
-    weight = torch.zeros((300, 64), dtype=torch.bfloat16, device="cuda")
+    hidden = torch.zeros((0, 6, 128), dtype=torch.bfloat16, device="cuda")
+    weight = torch.zeros((300, 128), dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros((0, 6), dtype=torch.int64, device="cuda")
     lens = torch.zeros((0,), dtype=torch.int32, device="cuda")
     lp, lse, ws = g.grpo_lmhead_logprobs(hidden, weight, 2, ids, lens)

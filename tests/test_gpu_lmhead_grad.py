@@ -86,10 +86,10 @@ def _check_fwd(w, out, h):
 
 
 SMALL = [
-    ("V1000_d64", wl.variant(wl.QWEN_G8, name="lmg_1000_64", B=2, G=4, P=8, C=24, V=1000,
-                             eos_id=999, seed=81), 64, 1.0),
-    ("V4099_d192_kl", wl.variant(wl.QWEN_G16_KL, name="lmg_4099_192", B=1, G=4, P=5, C=40,
-                                 V=4099, eos_id=4000, seed=82), 192, 2.5),
+    ("V1000_d128", wl.variant(wl.QWEN_G8, name="lmg_1000_128", B=2, G=4, P=8, C=24, V=1000,
+                              eos_id=999, seed=81), 128, 1.0),
+    ("V4099_d384_kl", wl.variant(wl.QWEN_G16_KL, name="lmg_4099_384", B=1, G=4, P=5, C=40,
+                                 V=4099, eos_id=4000, seed=82), 384, 2.5),
     ("V300_d128_short", wl.variant(wl.QWEN_G8, name="lmg_300_128", B=1, G=2, P=3, C=6, V=300,
                                    eos_id=299, seed=83), 128, None),
 ]
@@ -117,7 +117,7 @@ def test_lmhead_grads_deterministic_and_scaled():
     output exactly (bf16 rounding commutes with a power-of-two scale)."""
     n = H.g()
     w = H.with_contrast(SMALL[1][1])
-    hidden, weight, t_ids, lens, out, h = _setup(w, 192)
+    hidden, weight, t_ids, lens, out, h = _setup(w, 384)
     one = torch.tensor([1.0], dtype=torch.float32, device="cuda")
     two = torch.tensor([2.0], dtype=torch.float32, device="cuda")
     a = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"], one)
@@ -132,8 +132,8 @@ def test_lmhead_grads_deterministic_and_scaled():
 def test_lmhead_grads_no_scored_rows():
     """C = 0: nothing is scored, both gradients are zero."""
     n = H.g()
-    hidden = torch.ones((2, 4, 64), dtype=torch.bfloat16, device="cuda")
-    weight = torch.ones((300, 64), dtype=torch.bfloat16, device="cuda")
+    hidden = torch.ones((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    weight = torch.ones((300, 128), dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros((2, 4), dtype=torch.int64, device="cuda")
     lens = torch.zeros((2,), dtype=torch.int32, device="cuda")
     z = torch.zeros((2, 0), dtype=torch.float32, device="cuda")

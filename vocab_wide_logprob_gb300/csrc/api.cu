@@ -389,8 +389,8 @@ grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, i
 
 grpo_status grpo_lmhead_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
                                        size_t* bytes) {
-  if (bytes == nullptr || N < 0 || C < 0 || V < 1 || d < 64 || d % 64 != 0)
-    return GRPO_ERR_INVALID_ARG;
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+  if (d < 128 || d % 128 != 0) return GRPO_ERR_UNSUPPORTED;
   if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -408,7 +408,7 @@ grpo_status lmhead_check(const void* hidden, const void* weight, int64_t N, int6
                          const void* workspace) {
   grpo_status s = check_shapes(GRPO_BF16, N, P, C, V);
   if (s != GRPO_OK) return s;
-  if (d < 64 || d % 64 != 0) return GRPO_ERR_UNSUPPORTED;
+  if (d < 128 || d % 128 != 0) return GRPO_ERR_UNSUPPORTED;
   if (V > (int64_t)INT32_MAX - 256 || mul3(N, P + C, d) < 0) return GRPO_ERR_UNSUPPORTED;
   if (workspace == nullptr || (N > 0 && len == nullptr)) return GRPO_ERR_INVALID_ARG;
   if (N > 0 && C > 0 && (hidden == nullptr || weight == nullptr || input_ids == nullptr))
@@ -498,8 +498,8 @@ grpo_status grpo_lmhead_loss_fwd(const void* hidden, const void* weight, int64_t
 
 grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
                                            size_t* bytes) {
-  if (bytes == nullptr || N < 0 || C < 0 || V < 1 || d < 64 || d % 64 != 0)
-    return GRPO_ERR_INVALID_ARG;
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+  if (d < 128 || d % 128 != 0) return GRPO_ERR_UNSUPPORTED;
   if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
   if (V > (int64_t)INT32_MAX - 256) return GRPO_ERR_UNSUPPORTED;
   DeviceInfo dev;

@@ -508,7 +508,7 @@ cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceIn
 // dense copy of the scored rows' hidden states and the per-item partials.
 struct LmLayout {
   size_t geometry;  // int4: row blocks, vocabulary splits, tiles per split
-  size_t dense;     // bf16 [N*C rounded up to 128, d]
+  size_t dense;     // bf16 [N*C rounded up to 256, d]
   size_t partials;  // float4 [items][128]
   size_t total;
 };
@@ -523,10 +523,10 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
 struct LmBwdLayout {
   size_t geometry;     // int4[2]: projection pass; hidden-gradient contraction
   size_t dense;        // bf16 [rows_cap, d]
-  size_t dz;           // bf16 [rows_cap, ldz]
-  size_t dh_partials;  // fp32 [items_max][128][256]
+  size_t dz;           // bf16 [ldz / 64][rows_cap][64] (vocabulary slabs)
+  size_t dh_partials;  // fp32 [items_max][256][256]
   size_t total;
-  int64_t rows_cap;    // N*C rounded up to 128
+  int64_t rows_cap;    // N*C rounded up to 256
   int64_t ldz;         // V rounded up to 256
   int64_t items_max;
 };
@@ -543,6 +543,8 @@ struct LmBwdArgs {
   float* dweight;       // fp32 [V, d]
   void* ws;
 };
+// CTA pairs of the tensor-core kernels on this device.
+int lm_pairs(const DeviceInfo& dev);
 // After launch_prep: gather (+ both geometries) and the logits-gradient pass.
 cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st);
 // After launch_lmhead_dz: the hidden-state and weight gradient contractions.

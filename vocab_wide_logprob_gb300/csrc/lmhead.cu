@@ -3,23 +3,19 @@
 // "compute_logprobs" in "Making Dr GRPO go brrr", salahadawi.com) fused with
 // the shifted log-softmax and gather, so the [rows, V] logits never reach
 // HBM.  This is a dense contraction, so it runs on the 5th-generation tensor
-// cores: tcgen05.mma with operands staged in shared memory by TMA and the
-// fp32 accumulator in tensor memory (TMEM).
+// cores: tcgen05.mma on CTA pairs (2-SM MMA, M = 256) with operands staged in
+// shared memory by TMA and the fp32 accumulator in tensor memory (TMEM).
 //
-// Pipeline (one CTA per SM, persistent):
 //   gather_rows_kernel   copies the hidden state of every scored row into a
 //                        dense [rows, d] buffer (row r = valid token r) and
-//                        zeroes the rows up to the next multiple of 128
-//   lmhead_lse_kernel    work items (block of 128 rows, range of vocabulary
-//                        tiles of 256).  Warp 0 issues TMA loads of a 128x64
-//                        slab of H and a 256x64 slab of W per k-step into a
-//                        4-stage ring (128-byte swizzle); warp 1 issues
-//                        tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into
-//                        one of two TMEM accumulators; warps 2-5 read the
-//                        finished 128x256 tile from TMEM (one row per thread)
-//                        and fold it into a running (max, sum of exp) and the
-//                        target logit, while the MMAs fill the other buffer.
-//                        Each item writes one partial per row.
+//                        zeroes the rows up to the next multiple of 256
+//   lmhead_lse_kernel    work items (block of 256 rows, range of vocabulary
+//                        tiles of 256) on the pair pipeline (pair_pipeline.cuh):
+//                        each CTA loads 128 rows of H and 128 vocabulary rows
+//                        of W per 64-wide k-step; the epilogue folds each
+//                        finished 256-column tile of its 128 rows into a
+//                        running (max, sum of exp) and the target logit.  Each
+//                        item writes one partial per row.
 //   lmhead_merge_kernel  merges a row's partials in order (deterministic) into
 //                        lse and logp = z_y - lse, and zeroes positions past
 //                        each length.
@@ -27,38 +23,33 @@
 // The backward ("loss.backward()" through the projection) recomputes the
 // logits with the same pipeline: lmhead_dz_kernel's epilogue turns each tile
 // into the logits gradient g * w_t * (onehot(y_t) - exp(z - lse_t)), rounded
-// to bf16, and stores it for the two gradient contractions (lmhead_bwd.cu).
+// to bf16, and stores it by TMA, in 64-column vocabulary slabs, for the two
+// gradient contractions (lmhead_bwd.cu).
 #include <mutex>
 
-#include "tc.cuh"
+#include "pair_pipeline.cuh"
 
 namespace grpo {
 namespace {
 
-constexpr int kBM = 128;          // rows per tile (TMEM lanes)
-constexpr int kBN = 256;          // vocabulary columns per tile
-constexpr int kBK = 64;           // k per stage: one 128-byte swizzle atom of bf16
-constexpr int kLmStages = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KiB
-constexpr int kStageBytesLm = kABytes + kBBytes;
-constexpr int kLmThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kMaxSplits = 256;  // = kThreads: one candidate per thread
-constexpr uint32_t kIdescLm = umma_idesc(kBM, kBN, false, false);
+constexpr int kRows = 256;        // rows per pair tile (128 per CTA)
+constexpr int kVTile = 256;       // vocabulary columns per tile
+constexpr int kK = 64;            // k per stage: one 128-byte swizzle atom of bf16
+constexpr int kMaxSplits = 256;   // = kThreads: one candidate per thread
+constexpr uint32_t kIdescLm = umma_idesc(256, kVTile, false, false);
+constexpr int kLmSmem = kPairRingBytes + 1024;
+constexpr int kDzSmem = kLmSmem + 4 * 4096;  // + the epilogue's TMA-store boxes
 
 struct LmParams {
   int64_t N, P, C, V, d;
   const int32_t* offsets;  // prefix sums of the clamped lengths ([N+1])
   int4* geometry;          // [0] (row blocks, splits, tiles per split): written by the gather
-  float4* partials;        // forward: [items][kBM] (max, sum, target logit, has target)
+  float4* partials;        // forward: [items][256] (max, sum, target logit, has target)
   WsHeader* hdr;
-  int sms;                 // CTAs in the grid: the split count is chosen from it
   // logits-gradient pass only
   const float* lse;        // [N, C] from the forward
   const float* w;          // [N, C] d loss / d logp from the forward
   const float* grad;       // upstream scalar gradient (nullable: 1)
-  uint16_t* dz;            // bf16 [rows, ldz]
-  int64_t ldz;
 };
 
 // Split `ksteps` steps of work for each of `units` independent tiles into
@@ -68,23 +59,23 @@ struct LmParams {
 // per thread of the calling CTA (kThreads threads); the smallest within 0.01
 // of the best score wins (fewer partials to merge, and every range re-reads
 // its unit's operand).  Returns (splits, steps per split).
-__device__ float split_score(int32_t units, int32_t sp, int32_t ksteps, int sms,
+__device__ float split_score(int32_t units, int32_t sp, int32_t ksteps, int slots,
                              int32_t max_items) {
   const int32_t items = units * sp;
   if (sp > ksteps || items > max_items) return -1.f;
   const int32_t sps = (ksteps + sp - 1) / sp;
   if ((int64_t)sps * (sp - 1) >= ksteps) return -1.f;  // the last range would be empty
-  const int32_t rounds = (items + sms - 1) / sms;
-  return (float)items / (float)(rounds * sms) * (float)ksteps / (float)(sps * sp);
+  const int32_t rounds = (items + slots - 1) / slots;
+  return (float)items / (float)(rounds * slots) * (float)ksteps / (float)(sps * sp);
 }
 
-__device__ int2 choose_split_block(int32_t units, int32_t ksteps, int sms, int32_t max_items) {
+__device__ int2 choose_split_block(int32_t units, int32_t ksteps, int slots, int32_t max_items) {
   __shared__ float s_best[kWarps];
   __shared__ int s_pick[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t sp = tid + 1;
   const float score =
-      units > 0 ? split_score(units, sp, ksteps, sms, max_items) : (sp == 1 ? 1.f : -1.f);
+      units > 0 ? split_score(units, sp, ksteps, slots, max_items) : (sp == 1 ? 1.f : -1.f);
   float best = score;
   for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
   if (lane == 0) s_best[warp] = best;
@@ -103,34 +94,34 @@ __device__ int2 choose_split_block(int32_t units, int32_t ksteps, int sms, int32
 
 // ---- gather: dense [rows, d] copy of the scored rows' hidden states ----------
 
-// geometry[0]: the projection pass (row blocks, vocabulary splits, tiles per
-// split, 0).  With `grad_gemm`, geometry[1]: the hidden-state gradient
-// contraction (row blocks, 256-wide d tiles, vocabulary splits, 64-wide
-// k-steps per split).
+// geometry[0]: the projection pass (256-row blocks, vocabulary splits, tiles
+// per split, 0).  With `grad_gemm`, geometry[1]: the hidden-state gradient
+// contraction (256-row blocks, 256-wide d tiles, vocabulary splits, 64-wide
+// k-steps per split).  `pairs`: CTA pairs of the tensor-core kernels.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                                                uint16_t* __restrict__ dense,
                                                                const int32_t* __restrict__ off,
                                                                int64_t N, int64_t T, int64_t P,
-                                                               int64_t d, int64_t V, int sms,
+                                                               int64_t d, int64_t V, int pairs,
                                                                int4* __restrict__ geometry,
                                                                int grad_gemm) {
   pdl_wait();
   pdl_trigger();
   const int64_t tv = off[N];
-  const int32_t mb = (int32_t)((tv + kBM - 1) / kBM);
+  const int32_t mb = (int32_t)((tv + kRows - 1) / kRows);
   if (blockIdx.x == 0) {
-    const int32_t ntiles = (int32_t)((V + kBN - 1) / kBN);
-    const int2 s = choose_split_block(mb, ntiles, sms, 4 * sms + 2 * mb);
+    const int32_t ntiles = (int32_t)((V + kVTile - 1) / kVTile);
+    const int2 s = choose_split_block(mb, ntiles, pairs, 4 * pairs + 2 * mb);
     if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
   }
   if (grad_gemm && blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
     const int32_t nb = (int32_t)((d + 255) / 256);
-    const int32_t ksteps = (int32_t)((V + kBN - 1) / kBN) * (kBN / kBK);
-    const int2 s = choose_split_block(mb * nb, ksteps, sms, 2 * sms + mb * nb);
+    const int32_t ksteps = (int32_t)((V + kVTile - 1) / kVTile) * (kVTile / kK);
+    const int2 s = choose_split_block(mb * nb, ksteps, pairs, 2 * pairs + mb * nb);
     if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
   }
   const int64_t vec_per_row = d / 8;  // 16-byte vectors
-  const int64_t rows_pad = (int64_t)mb * kBM;
+  const int64_t rows_pad = (int64_t)mb * kRows;
   for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < rows_pad * vec_per_row;
        k += (int64_t)gridDim.x * kThreads) {
     const int64_t r = k / vec_per_row, c = k - r * vec_per_row;
@@ -153,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
   }
 }
 
-// ---- the tensor-core pipeline ----------------------------------------------------
+// ---- the projection on the pair pipeline -------------------------------------------
 
 // Completion of the valid token r (binary search over the offsets).
 __device__ __forceinline__ int completion_of(const int32_t* off, int64_t N, int64_t r) {
@@ -168,284 +159,225 @@ __device__ __forceinline__ int completion_of(const int32_t* off, int64_t N, int6
   return lo;
 }
 
-// kMode 0: log-sum-exp partials per row; kMode 1: the bf16 logits gradient.
+// Items (256-row block, range of vocabulary tiles); a tile is 256 rows x 256
+// vocabulary columns reduced over d.  kMode 0: log-sum-exp partials per row;
+// kMode 1: the bf16 logits gradient, stored by TMA.
 template <int kMode>
-__device__ __forceinline__ void lm_tile_pipeline(const CUtensorMap* map_h, const CUtensorMap* map_w,
-                                                 const int64_t* __restrict__ ids,
-                                                 const LmParams& p) {
-  extern __shared__ __align__(1024) unsigned char lm_smem[];
-  __shared__ __align__(8) uint64_t s_full[kLmStages];
-  __shared__ __align__(8) uint64_t s_empty[kLmStages];
-  __shared__ __align__(8) uint64_t s_acc_full[2];
-  __shared__ __align__(8) uint64_t s_acc_empty[2];
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
+struct LmOp {
+  const LmParams& p;
+  const CUtensorMap* map_h;
+  const CUtensorMap* map_w;
+  const CUtensorMap* map_dz;
+  const int64_t* ids;
+  uint32_t rank, stg;
+  int64_t tv, mb, splits, tps, ntiles;
+  int kblocks;
+  // epilogue state of this thread's row
+  int64_t r, y;
+  float lse_r, coef, g, m, s_extra, zy;
+  uint64_t acc01, acc23;
+  bool has;
+  uint32_t chunk;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  unsigned char* ring = lm_smem + ((1024 - (smem_u32(lm_smem) & 1023)) & 1023);
-  const uint32_t ring_u32 = smem_u32(ring);
-
-  if (tid == 0) {
-    s_abort = 0;
-    for (int k = 0; k < kLmStages; ++k) {
-      mbar_init(smem_u32(&s_full[k]), 1);
-      mbar_init(smem_u32(&s_empty[k]), 1);  // one tcgen05.commit per use
-    }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&s_acc_full[k]), 1);   // tcgen05.commit after a tile's MMAs
-      mbar_init(smem_u32(&s_acc_empty[k]), 4);  // one arrive per epilogue warp
-    }
-    mbar_init_fence();
+  __device__ void setup() {
+    tv = p.offsets[p.N];
+    const int4 geo = p.geometry[0];
+    mb = geo.x;
+    splits = geo.y;
+    tps = geo.z;
+    ntiles = (p.V + kVTile - 1) / kVTile;
+    kblocks = (int)(p.d / kK);
+    g = (kMode == 1 && p.grad != nullptr) ? __ldg(p.grad) : 1.f;
+    chunk = 0;
   }
-  if (warp == 1) tmem_alloc(&s_tmem, 512);  // two 256-column fp32 accumulators
-  tmem_fence_before();
-  __syncthreads();
-  tmem_fence_after();
-  const uint32_t tmem = s_tmem;
-  pdl_wait();
-  pdl_trigger();
-
-  const int64_t tv = p.offsets[p.N];
-  const int4 geo = p.geometry[0];
-  const int64_t mb = geo.x, splits = geo.y, tps = geo.z;
-  const int64_t ntiles = (p.V + kBN - 1) / kBN;
-  const int64_t items = mb * splits;
-  const int kblocks = (int)(p.d / kBK);
-
-  if (warp == 0) {
-    // ---------------- TMA producer -----------------------------------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-        const int64_t rb = it / splits, sp = it - rb * splits;
-        const int64_t n0 = sp * tps, n1 = min(ntiles, n0 + tps);
-        for (int64_t n = n0; n < n1; ++n) {
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u)) {
-              atomicOr(&p.hdr->flags, kFlagTimeout);
-              *(volatile int*)&s_abort = 1;
-              break;
-            }
-            const uint32_t full = smem_u32(&s_full[stage]);
-            const uint32_t sa = ring_u32 + stage * kStageBytesLm;
-            mbar_arrive_expect_tx(full, kStageBytesLm);
-            tma_load_2d(sa, map_h, kb * kBK, (int)(rb * kBM), full);
-            tma_load_2d(sa + kABytes, map_w, kb * kBK, (int)(n * kBN), full);
-            if (++stage == kLmStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (*(volatile int*)&s_abort) break;
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ---------------------------------------------
-    if (lane == 0) {
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, aphase = 0;
-      for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-        const int64_t rb = it / splits, sp = it - rb * splits;
-        const int64_t n0 = sp * tps, n1 = min(ntiles, n0 + tps);
-        (void)rb;
-        for (int64_t n = n0; n < n1; ++n) {
-          // the epilogue has drained this accumulator
-          if (!mbar_wait(smem_u32(&s_acc_empty[buf]), aphase ^ 1u)) {
-            atomicOr(&p.hdr->flags, kFlagTimeout);
-            *(volatile int*)&s_abort = 1;
-            break;
-          }
-          tmem_fence_after();
-          const uint32_t dacc = tmem + (uint32_t)(buf * kBN);
-          bool ok = true;
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(smem_u32(&s_full[stage]), phase)) {
-              atomicOr(&p.hdr->flags, kFlagTimeout);
-              *(volatile int*)&s_abort = 1;
-              ok = false;
-              break;
-            }
-            tmem_fence_after();
-            const uint32_t sa = ring_u32 + stage * kStageBytesLm;
+  __device__ int64_t items() const { return mb * splits; }
+  __device__ int64_t first_tile(int64_t it) const { return (it % splits) * tps; }
+  __device__ int tiles(int64_t it) const {
+    const int64_t n0 = first_tile(it);
+    return (int)(min(ntiles, n0 + tps) - n0);
+  }
+  __device__ void krange(int64_t, int, int64_t* k0, int64_t* k1) const {
+    *k0 = 0;
+    *k1 = kblocks;
+  }
+  __device__ uint32_t bytes(int64_t, int) const { return kPairStageBytes; }
+  __device__ void load(uint32_t sa, int64_t it, int t, int64_t ks, uint32_t rk,
+                       uint32_t mbar) const {
+    const int64_t rb = it / splits, n = first_tile(it) + t;
+    tma_load_2d_pair(sa, map_h, (int)(ks * kK), (int)(rb * kRows + rk * 128), mbar);
+    tma_load_2d_pair(sa + kPairBOffset, map_w, (int)(ks * kK), (int)(n * kVTile + rk * 128),
+                     mbar);
+  }
+  __device__ void mma(uint32_t dacc, uint32_t sa, int64_t, int, bool first) const {
 #pragma unroll
-            for (int j = 0; j < kBK / 16; ++j)
-              umma_bf16(dacc, umma_desc_k(sa + j * 32), umma_desc_k(sa + kABytes + j * 32),
-                        kIdescLm, (kb | j) ? 1u : 0u);
-            umma_commit(smem_u32(&s_empty[stage]));  // the stage is free once these finish
-            if (++stage == kLmStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (!ok) break;
-          umma_commit(smem_u32(&s_acc_full[buf]));  // the tile is complete in TMEM
-          if (++buf == 2) {
-            buf = 0;
-            aphase ^= 1u;
-          }
-        }
+    for (int j = 0; j < kK / 16; ++j)
+      umma_bf16_pair(dacc, umma_desc_k(sa + j * 32), umma_desc_k(sa + kPairBOffset + j * 32),
+                     kIdescLm, (first && j == 0) ? 0u : 1u);
+  }
+
+  __device__ void epi_begin(int64_t it) {
+    const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
+    r = (it / splits) * kRows + rank * 128 + quarter * 32 + lane;
+    y = -1;
+    lse_r = 0.f;
+    coef = 0.f;
+    if (r < tv) {
+      const int i = completion_of(p.offsets, p.N, r);
+      const int64_t t = r - p.offsets[i];
+      y = __ldg(ids + (int64_t)i * (p.P + p.C) + p.P + t);
+      if (kMode == 1) {
+        lse_r = __ldg(p.lse + (int64_t)i * p.C + t);
+        coef = g * __ldg(p.w + (int64_t)i * p.C + t);
       }
     }
-  } else {
-    // ---------------- epilogue: warps 2..5, one accumulator row per thread ----
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 of this warp
-    const int row_in_block = quarter * 32 + lane;
-    int buf = 0;
-    uint32_t aphase = 0;
+    m = -INFINITY;
+    s_extra = 0.f;
+    zy = 0.f;
+    acc01 = f2_pack(0.f, 0.f);
+    acc23 = f2_pack(0.f, 0.f);
+    has = false;
+  }
+
+  __device__ void epi_tile(int64_t it, int t, uint32_t tbase, bool) {
+    const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
-    const float g = (kMode == 1 && p.grad != nullptr) ? __ldg(p.grad) : 1.f;
-    for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-      const int64_t rb = it / splits, sp = it - rb * splits;
-      const int64_t n0 = sp * tps, n1 = min(ntiles, n0 + tps);
-      const int64_t r = rb * kBM + row_in_block;  // valid token of this thread
-      int64_t y = -1;
-      float lse_r = 0.f, coef = 0.f;
-      if (r < tv) {
-        const int i = completion_of(p.offsets, p.N, r);
-        const int64_t t = r - p.offsets[i];
-        y = __ldg(ids + (int64_t)i * (p.P + p.C) + p.P + t);
-        if (kMode == 1) {
-          lse_r = __ldg(p.lse + (int64_t)i * p.C + t);
-          coef = g * __ldg(p.w + (int64_t)i * p.C + t);
-        }
-      }
-      float m = -INFINITY, s_extra = 0.f, zy = 0.f;
-      uint64_t acc01 = f2_pack(0.f, 0.f), acc23 = f2_pack(0.f, 0.f);
-      bool has = false;
-      bool ok = true;
-      for (int64_t n = n0; n < n1; ++n) {
-        if (!mbar_wait(smem_u32(&s_acc_full[buf]), aphase)) {
-          atomicOr(&p.hdr->flags, kFlagTimeout);
-          *(volatile int*)&s_abort = 1;
-          ok = false;
-          break;
-        }
-        tmem_fence_after();
-        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBN);
-        const int64_t vbase = n * kBN;
+    const int64_t vbase = (first_tile(it) + t) * kVTile;
 #pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
-          float v[32];
-          tmem_ld32(tbase + (uint32_t)c, v);
-          const int64_t v0 = vbase + c;
-          if constexpr (kMode == 0) {
-            if (v0 + 32 > p.V) {  // the vocabulary's last tile: columns past V do not exist
+    for (int c = 0; c < kVTile; c += 32) {
+      float v[32];
+      tmem_ld32(tbase + (uint32_t)c, v);
+      const int64_t v0 = vbase + c;
+      if constexpr (kMode == 0) {
+        if (v0 + 32 > p.V) {  // the vocabulary's last tile: columns past V do not exist
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (v0 + j >= p.V) v[j] = -INFINITY;
-            }
-            if (y >= v0 && y < v0 + 32) {
+          for (int j = 0; j < 32; ++j)
+            if (v0 + j >= p.V) v[j] = -INFINITY;
+        }
+        if (y >= v0 && y < v0 + 32) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (v0 + j == y) zy = v[j];
-              has = true;
-            }
-            float bm = v[0];
+          for (int j = 0; j < 32; ++j)
+            if (v0 + j == y) zy = v[j];
+          has = true;
+        }
+        float bm = v[0];
 #pragma unroll
-            for (int j = 1; j < 32; ++j) bm = fmaxf(bm, v[j]);
-            if (bm > m) {
-              const float sc = ex2((m - bm) * kLog2e);
-              const uint64_t sc2 = f2_pack(sc, sc);
-              acc01 = f2_mul(acc01, sc2);
-              acc23 = f2_mul(acc23, sc2);
-              s_extra *= sc;
-              m = bm;
-            }
-            if (m != -INFINITY) {
-              const float mL = m * kLog2e;
-              const uint64_t nmL2 = f2_pack(-mL, -mL);
+        for (int j = 1; j < 32; ++j) bm = fmaxf(bm, v[j]);
+        if (bm > m) {
+          const float sc = ex2((m - bm) * kLog2e);
+          const uint64_t sc2 = f2_pack(sc, sc);
+          acc01 = f2_mul(acc01, sc2);
+          acc23 = f2_mul(acc23, sc2);
+          s_extra *= sc;
+          m = bm;
+        }
+        if (m != -INFINITY) {
+          const float mL = m * kLog2e;
+          const uint64_t nmL2 = f2_pack(-mL, -mL);
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) {
-                acc01 = f2_add(acc01, f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nmL2)));
-                acc23 = f2_add(acc23, f2_ex2(f2_fma(f2_pack(v[j + 2], v[j + 3]), L2, nmL2)));
-              }
-            }
-          } else {
-            // dz = coef * (onehot(y) - 2^(z log2 e - lse log2 e)), bf16 (round to nearest even)
-            const float lL = lse_r * kLog2e;
-            const uint64_t nlL2 = f2_pack(-lL, -lL);
-            const uint64_t nc2 = f2_pack(-coef, -coef);
-            uint32_t pk[16];
-            if (y >= v0 && y < v0 + 32) {
-              // the target column: coef * (1 - p_y) without cancellation, -expm1(z_y - lse)
-              float zy_ = 0.f;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (v0 + j == y) zy_ = v[j];
-              const float dy = coef * -expm1f(zy_ - lse_r);
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                float a, b;
-                f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
-                a = (v0 + j == y) ? dy : a;
-                b = (v0 + j + 1 == y) ? dy : b;
-                pk[j / 2] = pack_bf16x2(a, b);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                float a, b;
-                f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
-                pk[j / 2] = pack_bf16x2(a, b);
-              }
-            }
-            if (r >= tv) {  // padding rows of the last block: zeros
-#pragma unroll
-              for (int j = 0; j < 16; ++j) pk[j] = 0u;
-            } else if (v0 + 32 > p.V) {  // columns past V: zeros
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (v0 + j >= p.V) pk[j >> 1] &= (j & 1) ? 0x0000ffffu : 0xffff0000u;
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.dz + r * p.ldz + v0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int j = 0; j < 32; j += 4) {
+            acc01 = f2_add(acc01, f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nmL2)));
+            acc23 = f2_add(acc23, f2_ex2(f2_fma(f2_pack(v[j + 2], v[j + 3]), L2, nmL2)));
           }
         }
-        tmem_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_acc_empty[buf]));  // accumulator may be reused
-        if (++buf == 2) {
-          buf = 0;
-          aphase ^= 1u;
+      } else {
+        // dz = coef * (onehot(y) - 2^(z log2 e - lse log2 e)), bf16 (round to nearest even)
+        const float lL = lse_r * kLog2e;
+        const uint64_t nlL2 = f2_pack(-lL, -lL);
+        const uint64_t nc2 = f2_pack(-coef, -coef);
+        uint32_t pk[16];
+        if (y >= v0 && y < v0 + 32) {
+          // the target column: coef * (1 - p_y) without cancellation, -expm1(z_y - lse)
+          float zy_ = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (v0 + j == y) zy_ = v[j];
+          const float dy = coef * -expm1f(zy_ - lse_r);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float a, b;
+            f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
+            a = (v0 + j == y) ? dy : a;
+            b = (v0 + j + 1 == y) ? dy : b;
+            pk[j / 2] = pack_bf16x2(a, b);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float a, b;
+            f2_unpack(f2_mul(f2_ex2(f2_fma(f2_pack(v[j], v[j + 1]), L2, nlL2)), nc2), a, b);
+            pk[j / 2] = pack_bf16x2(a, b);
+          }
         }
-      }
-      if (!ok) break;
-      if constexpr (kMode == 0) {
-        float a0, a1, a2, a3;
-        f2_unpack(acc01, a0, a1);
-        f2_unpack(acc23, a2, a3);
-        const float s = ((a0 + a1) + (a2 + a3)) + s_extra;
-        if (r < tv) p.partials[it * kBM + row_in_block] = make_float4(m, s, zy, has ? 1.f : 0.f);
+        if (r >= tv) {  // padding rows of the last block: zeros
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        } else if (v0 + 32 > p.V) {  // columns past V: zeros
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (v0 + j >= p.V) pk[j >> 1] &= (j & 1) ? 0x0000ffffu : 0xffff0000u;
+        }
+        // row `lane` of this warp's 32 x 32 box; 16-byte chunk q sits at q ^ ((lane >> 1) & 3)
+        const uint32_t box = stg + (chunk & 1u) * 2048u;
+        if (lane == 0) bulk_wait_read<1>();  // the store that last used this box has read it
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(box + (uint32_t)lane * 64u + ((uint32_t)(q ^ ((lane >> 1) & 3)) << 4),
+                       pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(map_dz, box, (int)(v0 & 63),
+                       (int)((it / splits) * kRows + rank * 128 + quarter * 32), (int)(v0 >> 6));
+          bulk_commit();
+        }
+        ++chunk;
       }
     }
   }
 
-  // release tensor memory: every MMA this CTA issued has completed once the
-  // epilogue consumed its tile (or, after a timeout, once the last commit lands)
-  tmem_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tmem_fence_after();
-    tmem_dealloc(tmem, 512);
+  __device__ void epi_end(int64_t it) {
+    if constexpr (kMode == 0) {
+      const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
+      float a0, a1, a2, a3;
+      f2_unpack(acc01, a0, a1);
+      f2_unpack(acc23, a2, a3);
+      const float s = ((a0 + a1) + (a2 + a3)) + s_extra;
+      if (r < tv)
+        p.partials[it * kRows + rank * 128 + quarter * 32 + lane] =
+            make_float4(m, s, zy, has ? 1.f : 0.f);
+    }
   }
+  __device__ void epi_finish() {
+    if (kMode == 1 && (threadIdx.x & 31) == 0) bulk_wait<0>();  // the gradient stores are done
+  }
+};
+
+template <int kMode>
+__device__ __forceinline__ void lm_kernel_body(const CUtensorMap* map_h, const CUtensorMap* map_w,
+                                               const CUtensorMap* map_dz, const int64_t* ids,
+                                               const LmParams& p) {
+  extern __shared__ __align__(1024) unsigned char lm_smem[];
+  const uint32_t ring = smem_u32(lm_smem + ((1024 - (smem_u32(lm_smem) & 1023)) & 1023));
+  LmOp<kMode> op{p, map_h, map_w, map_dz, ids};
+  op.rank = cluster_rank();
+  op.stg = ring + kPairRingBytes + (uint32_t)((threadIdx.x >> 5) & 3) * 4096u;
+  pair_pipeline(op, ring, p.hdr);
 }
 
-__global__ void __launch_bounds__(kLmThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     lmhead_lse_kernel(const __grid_constant__ CUtensorMap map_h,
                       const __grid_constant__ CUtensorMap map_w, const int64_t* __restrict__ ids,
                       const LmParams p) {
-  lm_tile_pipeline<0>(&map_h, &map_w, ids, p);
+  lm_kernel_body<0>(&map_h, &map_w, nullptr, ids, p);
 }
 
-__global__ void __launch_bounds__(kLmThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     lmhead_dz_kernel(const __grid_constant__ CUtensorMap map_h,
-                     const __grid_constant__ CUtensorMap map_w, const int64_t* __restrict__ ids,
+                     const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_dz, const int64_t* __restrict__ ids,
                      const LmParams p) {
-  lm_tile_pipeline<1>(&map_h, &map_w, ids, p);
+  lm_kernel_body<1>(&map_h, &map_w, &map_dz, ids, p);
 }
 
 // ---- merge: partials of a row in split order -> lse, logp ----------------------
@@ -468,12 +400,12 @@ __global__ void __launch_bounds__(kThreads) lmhead_merge_kernel(const LmParams p
       continue;
     }
     const int64_t r = p.offsets[i] + t;
-    const int64_t rb = r / kBM, rr = r - rb * kBM;
-    float4 pk = p.partials[(rb * splits) * kBM + rr];
+    const int64_t rb = r / kRows, rr = r - rb * kRows;
+    float4 pk = p.partials[(rb * splits) * kRows + rr];
     float cm = pk.x, cs = pk.y, z = pk.z;
     bool has = pk.w != 0.f;
     for (int64_t sp = 1; sp < splits; ++sp) {
-      pk = p.partials[(rb * splits + sp) * kBM + rr];
+      pk = p.partials[(rb * splits + sp) * kRows + rr];
       lse_merge(cm, cs, pk.x, pk.y);
       if (pk.w != 0.f) {
         z = pk.z;
@@ -513,7 +445,7 @@ cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 }
 
 LmParams lm_params(const int32_t* off, int4* geometry, WsHeader* hdr, int64_t N, int64_t P,
-                   int64_t C, int64_t V, int64_t d, int sms) {
+                   int64_t C, int64_t V, int64_t d) {
   LmParams p = {};
   p.N = N;
   p.P = P;
@@ -523,30 +455,19 @@ LmParams lm_params(const int32_t* off, int4* geometry, WsHeader* hdr, int64_t N,
   p.offsets = off;
   p.geometry = geometry;
   p.hdr = hdr;
-  p.sms = sms;
   return p;
 }
 
-template <typename K>
-cudaError_t launch_tiles(K kern, const void* dense, const void* weight, int64_t rows, int64_t d,
-                         int64_t V, const int64_t* ids, const LmParams& p, const DeviceInfo& dev,
-                         cudaStream_t st, bool* attr_done) {
-  CUtensorMap map_h, map_w;
-  cudaError_t e;
-  if ((e = encode_bf16_2d(&map_h, dense, d, rows, d, kBM)) != cudaSuccess) return e;
-  if ((e = encode_bf16_2d(&map_w, weight, d, V, d, kBN)) != cudaSuccess) return e;
-  const int smem = kLmStages * kStageBytesLm + 1024;
-  if (!*attr_done) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-        cudaSuccess)
-      return e;
-    *attr_done = true;
-  }
-  return launch_pdl(kern, dim3((unsigned)dev.sms), dim3(kLmThreads), (size_t)smem, st, 1, map_h,
-                    map_w, ids, p);
+cudaError_t set_smem(const void* kern, int bytes, bool* done) {
+  if (*done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *done = true;
+  return e;
 }
 
 }  // namespace
+
+int lm_pairs(const DeviceInfo& dev) { return dev.sms / 2 > 0 ? dev.sms / 2 : 1; }
 
 cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
                            int64_t pitch, int box_outer) {
@@ -555,7 +476,7 @@ cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, in
   if (e != cudaSuccess) return e;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
   cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_outer};
+  cuuint32_t box[2] = {(cuuint32_t)kK, (cuuint32_t)box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -563,32 +484,67 @@ cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_store_32x32(CUtensorMap* map, void* base, bool fp32, int64_t inner,
+                               int64_t outer, int64_t pitch) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const int64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch * es)};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_dz_slabs(CUtensorMap* map, void* base, int64_t rows, int64_t ldz, int box_rows,
+                            bool store) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  cudaError_t e = get_encoder(&enc);
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(ldz / 64)};
+  cuuint64_t strides[2] = {128u, (cuuint64_t)rows * 128u};
+  cuuint32_t box[3] = {store ? 32u : 64u, store ? 32u : (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   store ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   store ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms) {
   LmLayout l;
   const WsLayout base = ws_layout(N);
-  const int64_t rows = N * C;
-  const int64_t mb_max = (rows + kBM - 1) / kBM;
+  const int64_t mb_max = (N * C + kRows - 1) / kRows;
+  const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
   l.geometry = base.total;  // 2 x int4
   l.dense = align_up(base.total + 32, 1024);
-  l.partials = align_up(l.dense + (size_t)(mb_max * kBM) * (size_t)d * 2, 256);
-  const int64_t items_max = 4 * (int64_t)sms + 2 * mb_max;  // mb * splits bound
-  l.total = align_up(l.partials + (size_t)items_max * kBM * sizeof(float4), 256);
+  l.partials = align_up(l.dense + (size_t)(mb_max * kRows) * (size_t)d * 2, 256);
+  const int64_t items_max = 4 * pairs + 2 * mb_max;  // mb * splits bound
+  l.total = align_up(l.partials + (size_t)items_max * kRows * sizeof(float4), 256);
   return l;
 }
 
 LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms) {
   LmBwdLayout l;
   const WsLayout base = ws_layout(N);
-  const int64_t mb_max = (N * C + kBM - 1) / kBM;
-  l.rows_cap = mb_max * kBM;
-  l.ldz = (V + kBN - 1) / kBN * kBN;
+  const int64_t mb_max = (N * C + kRows - 1) / kRows;
+  const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
+  l.rows_cap = mb_max * kRows;
+  l.ldz = (V + kVTile - 1) / kVTile * kVTile;
   const int64_t nb = (d + 255) / 256;
-  l.items_max = 2 * (int64_t)sms + mb_max * nb;
+  l.items_max = 2 * pairs + mb_max * nb;
   l.geometry = base.total;
   l.dense = align_up(base.total + 32, 1024);
   l.dz = align_up(l.dense + (size_t)l.rows_cap * (size_t)d * 2, 1024);
   l.dh_partials = align_up(l.dz + (size_t)l.rows_cap * (size_t)l.ldz * 2, 1024);
-  l.total = align_up(l.dh_partials + (size_t)l.items_max * kBM * 256 * sizeof(float), 256);
+  l.total = align_up(l.dh_partials + (size_t)l.items_max * kRows * 256 * sizeof(float), 256);
   return l;
 }
 
@@ -599,20 +555,24 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   char* ws = static_cast<char*>(a.ws);
   const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
   uint16_t* dense = reinterpret_cast<uint16_t*>(ws + ll.dense);
-  const int64_t rows = (a.N * a.C + kBM - 1) / kBM * kBM;
+  const int64_t rows = (a.N * a.C + kRows - 1) / kRows * kRows;
+  const int pairs = lm_pairs(dev);
 
   int4* geometry = reinterpret_cast<int4*>(ws + ll.geometry);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(hidden), dense, off, a.N,
-                             a.P + a.C, a.P, d, a.V, dev.sms, geometry, 0);
+                             a.P + a.C, a.P, d, a.V, pairs, geometry, 0);
   if (e != cudaSuccess) return e;
 
-  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, d,
-                         dev.sms);
+  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, d);
   p.partials = reinterpret_cast<float4*>(ws + ll.partials);
+  CUtensorMap map_h, map_w;
+  if ((e = encode_bf16_2d(&map_h, dense, d, rows, d, 128)) != cudaSuccess) return e;
+  if ((e = encode_bf16_2d(&map_w, weight, d, a.V, d, 128)) != cudaSuccess) return e;
   static bool attr_done = false;
-  if ((e = launch_tiles(lmhead_lse_kernel, dense, weight, rows, d, a.V, a.ids, p, dev, st,
-                        &attr_done)) != cudaSuccess)
+  if ((e = set_smem((const void*)lmhead_lse_kernel, kLmSmem, &attr_done)) != cudaSuccess) return e;
+  if ((e = launch_pdl(lmhead_lse_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
+                      (size_t)kLmSmem, st, 2, map_h, map_w, a.ids, p)) != cudaSuccess)
     return e;
   int64_t blocks = (a.N * a.C + kThreads - 1) / kThreads;
   if (blocks > 1024) blocks = 1024;
@@ -628,20 +588,24 @@ cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStre
   const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
   uint16_t* dense = reinterpret_cast<uint16_t*>(ws + bl.dense);
   int4* geometry = reinterpret_cast<int4*>(ws + bl.geometry);
+  const int pairs = lm_pairs(dev);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(a.hidden), dense, off, a.N,
-                             a.P + a.C, a.P, a.d, a.V, dev.sms, geometry, 1);
+                             a.P + a.C, a.P, a.d, a.V, pairs, geometry, 1);
   if (e != cudaSuccess) return e;
-  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, a.d,
-                         dev.sms);
+  LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, a.d);
   p.lse = a.lse;
   p.w = a.w;
   p.grad = a.grad;
-  p.dz = reinterpret_cast<uint16_t*>(ws + bl.dz);
-  p.ldz = bl.ldz;
+  uint16_t* dz = reinterpret_cast<uint16_t*>(ws + bl.dz);
+  CUtensorMap map_h, map_w, map_dz;
+  if ((e = encode_bf16_2d(&map_h, dense, a.d, bl.rows_cap, a.d, 128)) != cudaSuccess) return e;
+  if ((e = encode_bf16_2d(&map_w, a.weight, a.d, a.V, a.d, 128)) != cudaSuccess) return e;
+  if ((e = encode_dz_slabs(&map_dz, dz, bl.rows_cap, bl.ldz, 32, true)) != cudaSuccess) return e;
   static bool attr_done = false;
-  return launch_tiles(lmhead_dz_kernel, dense, a.weight, bl.rows_cap, a.d, a.V, a.ids, p, dev,
-                      st, &attr_done);
+  if ((e = set_smem((const void*)lmhead_dz_kernel, kDzSmem, &attr_done)) != cudaSuccess) return e;
+  return launch_pdl(lmhead_dz_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
+                    (size_t)kDzSmem, st, 2, map_h, map_w, map_dz, a.ids, p);
 }
 
 }  // namespace grpo

@@ -6,269 +6,172 @@
 //   dhidden[row] = dz[row] W        (rows x V) (V x d): K = vocabulary
 //   dweight      = dz^T H_scored    (V x rows) (rows x d): K = scored rows
 //
-// Both are dense contractions on the tcgen05 tensor cores with the fp32
-// accumulator in TMEM.  The operands are read in their natural row-major
-// layouts: W [V, d], the dense scored hidden rows [rows, d] and dz
-// [rows, ldz] enter as MN-major (transposed) shared-memory operands where the
-// contraction runs over their row index, so nothing is transposed in memory.
+// Both are dense contractions on the tcgen05 tensor cores (CTA pairs, 2-SM
+// MMA with M = 256, pair_pipeline.cuh) with the fp32 accumulator in TMEM.  The
+// operands are read where they lie: W [V, d] and the dense scored hidden rows
+// [rows, d] (row-major), and dz in 64-column vocabulary slabs
+// [ldz / 64][rows][64]; each enters as an MN-major (transposed) shared-memory
+// operand where the contraction runs over its row index, so nothing is
+// transposed in memory.
 //
-// lmhead_grad_gemm_kernel<false>  dhidden partials: items (128 rows, 256
-//     columns of d, range of vocabulary k-steps), fp32 tiles in the workspace
+// lmhead_grad_gemm_kernel<false>  dhidden partials: items (range of
+//     vocabulary k-steps, 256 rows, 256 columns of d), fp32 tiles in the
+//     workspace
 // lmhead_dh_reduce_kernel         sums a row's partials in split order
 //     (deterministic) into dhidden [N, P+C, d]; rows that score nothing get 0
-// lmhead_grad_gemm_kernel<true>   dweight: items (128 vocabulary rows, 256
+// lmhead_grad_gemm_kernel<true>   dweight: items (256 vocabulary rows, 256
 //     columns of d), K = every scored row, fp32 straight to dweight [V, d]
 //
-// Warp roles as in the projection kernel: warp 0 TMA, warp 1 MMA, warps 2-5
-// drain TMEM through a shared-memory transpose into coalesced 16-byte stores.
-#include "tc.cuh"
+// The epilogue warps drain TMEM into 32 x 32 shared-memory boxes (128-byte
+// swizzle, two per warp) that TMA stores write out while the next box fills.
+// d must be a multiple of 128: each CTA of a pair holds half of a d tile of
+// 256 (or 128) columns as whole 64-column MN-major atoms.
+#include "pair_pipeline.cuh"
 
 namespace grpo {
 namespace {
 
-constexpr int kGM = 128;                  // output rows per tile (TMEM lanes)
-constexpr int kGN = 256;                  // output columns per tile (the last d tile may be narrower)
-constexpr int kGK = 64;                   // k per stage
-constexpr int kGStages = 4;
-constexpr int kGABytes = kGM * kGK * 2;   // 16 KiB
-constexpr int kGBBytes = kGN * kGK * 2;   // 32 KiB (at the full tile width)
-constexpr int kGStageBytes = kGABytes + kGBBytes;
-constexpr int kGThreads = 192;
-constexpr uint32_t kMnAtomStride = 8192;  // 64 M/N elements x 64 K rows x 2 bytes (one TMA box)
-constexpr int kStagePitch = 36;           // floats per staged row: 16-byte aligned, no bank conflicts
-constexpr int kEpiFloats = 4 * 32 * kStagePitch;
-constexpr int kGSmem = kGStages * kGStageBytes + kEpiFloats * 4 + 1024;
-constexpr int kTileFloats = kGM * kGN;
+constexpr int kRows = 256;                 // output rows per pair tile (128 per CTA)
+constexpr int kGN = 256;                   // output columns per tile (the last d tile may be 128)
+constexpr int kGK = 64;                    // k per stage
+constexpr int kGABytes = 128 * kGK * 2;    // this CTA's A: 16 KiB
+constexpr uint32_t kMnAtomStride = 8192;   // 64 M/N elements x 64 K rows x 2 bytes (one TMA box)
+constexpr int kEpiBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA-store box
+constexpr int kGSmem = kPairRingBytes + 4 * 2 * kEpiBoxBytes + 1024;
+constexpr int64_t kTileFloats = (int64_t)kRows * kGN;
 
 struct GradParams {
   int64_t N, V, d;
   const int32_t* offsets;  // [N+1]: offsets[N] = scored rows
   const int4* geometry;    // [1]: (row blocks, d tiles, splits, k-steps per split)
   int64_t ksteps_v;        // vocabulary k-steps of the hidden-state gradient (ldz / 64)
-  float* out;              // <false>: partial tiles [items][128][256]; <true>: dweight [V, d]
   WsHeader* hdr;
 };
 
-struct GradItem {
-  int64_t m_tile, n_tile, k0, k1;
+// kDW false: dhidden partial tiles; true: dweight.
+template <bool kDW>
+struct GradOp {
+  const GradParams& p;
+  const CUtensorMap* map_a;
+  const CUtensorMap* map_b;
+  const CUtensorMap* map_out;
+  uint32_t rank, stg;
+  int64_t nb, mb, sps, ksteps, n_items;
+  uint32_t chunk;
+
+  __device__ void setup() {
+    nb = (p.d + kGN - 1) / kGN;
+    const int64_t tv = p.offsets[p.N];
+    if (kDW) {
+      ksteps = (tv + kGK - 1) / kGK;  // rows past tv are zero in both operands
+      sps = ksteps;
+      mb = (p.V + kRows - 1) / kRows;
+      n_items = mb * nb;
+    } else {
+      const int4 g = p.geometry[1];
+      mb = g.x;
+      sps = g.w;
+      ksteps = p.ksteps_v;
+      n_items = (int64_t)g.x * g.y * g.z;
+    }
+    chunk = 0;
+  }
+  // dweight: it = m tile * nb + d tile.  dhidden: it = (split * mb + m tile) * nb + d tile,
+  // so the items running at the same time share their vocabulary range in L2.
+  __device__ int64_t m_tile(int64_t it) const { return kDW ? it / nb : (it / nb) % mb; }
+  __device__ int64_t n_tile(int64_t it) const { return it % nb; }
+  __device__ int width(int64_t it) const { return (int)min((int64_t)kGN, p.d - n_tile(it) * kGN); }
+  __device__ int64_t items() const { return n_items; }
+  __device__ int tiles(int64_t) const { return 1; }
+  __device__ void krange(int64_t it, int, int64_t* k0, int64_t* k1) const {
+    if (kDW) {
+      *k0 = 0;
+      *k1 = ksteps;
+    } else {
+      *k0 = (it / nb / mb) * sps;
+      *k1 = min(ksteps, *k0 + sps);
+    }
+  }
+  __device__ uint32_t bytes(int64_t it, int) const {
+    return (uint32_t)(kGABytes + (width(it) / 2) * kGK * 2);
+  }
+  __device__ void load(uint32_t sa, int64_t it, int, int64_t ks, uint32_t rk,
+                       uint32_t mbar) const {
+    const int64_t mt = m_tile(it), nt = n_tile(it);
+    const int half = width(it) / 2;
+    if (kDW) {  // dz^T: two {64 vocabulary, 64 rows} slab boxes (MN-major A)
+      for (int j = 0; j < 2; ++j)
+        tma_load_3d_pair(sa + j * kMnAtomStride, map_a, 0, (int)(ks * kGK),
+                         (int)(mt * (kRows / 64) + rk * 2 + j), mbar);
+    } else {    // dz: one {64 vocabulary, 128 rows} slab box (K-major A)
+      tma_load_3d_pair(sa, map_a, 0, (int)(mt * kRows + rk * 128), (int)ks, mbar);
+    }
+    for (int j = 0; j < half / 64; ++j)  // B: this CTA's half of the d tile, {64 of d, 64 k rows}
+      tma_load_2d_pair(sa + kPairBOffset + j * kMnAtomStride, map_b,
+                       (int)(nt * kGN + rk * half + 64 * j), (int)(ks * kGK), mbar);
+  }
+  __device__ void mma(uint32_t dacc, uint32_t sa, int64_t it, int, bool first) const {
+    const uint32_t idesc = umma_idesc(256, width(it), kDW, true);
+#pragma unroll
+    for (int j = 0; j < kGK / 16; ++j) {
+      const uint64_t ad = kDW ? umma_desc_mn(sa + j * 2048, kMnAtomStride)
+                              : umma_desc_k(sa + j * 32);
+      const uint64_t bd = umma_desc_mn(sa + kPairBOffset + j * 2048, kMnAtomStride);
+      umma_bf16_pair(dacc, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+    }
+  }
+  __device__ void epi_begin(int64_t) {}
+  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty) {
+    const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
+    const int nw = width(it);
+    // box origin: dweight [V, d] at (vocabulary row, d column); partial tile `it` as rows
+    // it*256 .. of an [items*256, 256] matrix
+    const int y = kDW ? (int)(m_tile(it) * kRows + rank * 128 + quarter * 32)
+                      : (int)(it * kRows + rank * 128 + quarter * 32);
+    const int x0 = kDW ? (int)(n_tile(it) * kGN) : 0;
+    for (int c = 0; c < nw; c += 32) {
+      float v[32];
+      if (!empty) {
+        tmem_ld32(tbase + (uint32_t)c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      // row `lane` of the box; 16-byte chunk q sits at q ^ (lane & 7)
+      const uint32_t box = stg + (chunk & 1u) * (uint32_t)kEpiBoxBytes;
+      if (lane == 0) bulk_wait_read<1>();  // the store that last used this box has read it
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(box + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4),
+                     __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                     __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map_out, box, x0 + c, y);
+        bulk_commit();
+      }
+      ++chunk;
+    }
+  }
+  __device__ void epi_end(int64_t) {}
+  __device__ void epi_finish() {
+    if ((threadIdx.x & 31) == 0) bulk_wait<0>();  // every store has completed
+  }
 };
 
 template <bool kDW>
-__device__ __forceinline__ GradItem grad_item(int64_t it, int64_t nb, int64_t splits, int64_t sps,
-                                              int64_t ksteps) {
-  GradItem g;
-  if (kDW) {
-    g.m_tile = it / nb;
-    g.n_tile = it - g.m_tile * nb;
-    g.k0 = 0;
-    g.k1 = ksteps;
-  } else {
-    const int64_t s = it % splits, t = it / splits;
-    g.n_tile = t % nb;
-    g.m_tile = t / nb;
-    g.k0 = s * sps;
-    g.k1 = min(ksteps, g.k0 + sps);
-  }
-  return g;
-}
-
-template <bool kDW>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     lmhead_grad_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                            const __grid_constant__ CUtensorMap map_b, const GradParams p) {
+                            const __grid_constant__ CUtensorMap map_b,
+                            const __grid_constant__ CUtensorMap map_out, const GradParams p) {
   extern __shared__ __align__(1024) unsigned char g_smem[];
-  __shared__ __align__(8) uint64_t s_full[kGStages];
-  __shared__ __align__(8) uint64_t s_empty[kGStages];
-  __shared__ __align__(8) uint64_t s_acc_full[2];
-  __shared__ __align__(8) uint64_t s_acc_empty[2];
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  unsigned char* ring = g_smem + ((1024 - (smem_u32(g_smem) & 1023)) & 1023);
-  const uint32_t ring_u32 = smem_u32(ring);
-  float* staging = reinterpret_cast<float*>(ring + kGStages * kGStageBytes);
-
-  if (tid == 0) {
-    s_abort = 0;
-    for (int k = 0; k < kGStages; ++k) {
-      mbar_init(smem_u32(&s_full[k]), 1);
-      mbar_init(smem_u32(&s_empty[k]), 1);
-    }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&s_acc_full[k]), 1);
-      mbar_init(smem_u32(&s_acc_empty[k]), 4);
-    }
-    mbar_init_fence();
-  }
-  if (warp == 1) tmem_alloc(&s_tmem, 512);  // two 256-column fp32 accumulators
-  tmem_fence_before();
-  __syncthreads();
-  tmem_fence_after();
-  const uint32_t tmem = s_tmem;
-  pdl_wait();
-  pdl_trigger();
-
-  const int64_t tv = p.offsets[p.N];
-  const int64_t nb = (p.d + kGN - 1) / kGN;
-  int64_t items, splits = 1, sps, ksteps;
-  if (kDW) {
-    ksteps = (tv + kGK - 1) / kGK;  // rows past tv are zero in both operands
-    sps = ksteps;
-    items = (p.V + kGM - 1) / kGM * nb;
-  } else {
-    const int4 g = p.geometry[1];
-    splits = g.z;
-    sps = g.w;
-    ksteps = p.ksteps_v;
-    items = (int64_t)g.x * g.y * splits;
-  }
-
-  if (warp == 0) {
-    // ---------------- TMA producer -----------------------------------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-        const GradItem gi = grad_item<kDW>(it, nb, splits, sps, ksteps);
-        const int nw = (int)min((int64_t)kGN, p.d - gi.n_tile * kGN);
-        const uint32_t bytes = (uint32_t)(kGABytes + nw * kGK * 2);
-        for (int64_t ks = gi.k0; ks < gi.k1; ++ks) {
-          if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u)) {
-            atomicOr(&p.hdr->flags, kFlagTimeout);
-            *(volatile int*)&s_abort = 1;
-            break;
-          }
-          const uint32_t full = smem_u32(&s_full[stage]);
-          const uint32_t sa = ring_u32 + stage * kGStageBytes;
-          mbar_arrive_expect_tx(full, bytes);
-          if (kDW) {  // dz^T: two {64 vocabulary, 64 rows} boxes (MN-major A)
-            tma_load_2d(sa, &map_a, (int)(gi.m_tile * kGM), (int)(ks * kGK), full);
-            tma_load_2d(sa + kMnAtomStride, &map_a, (int)(gi.m_tile * kGM + 64), (int)(ks * kGK),
-                        full);
-          } else {    // dz: one {64 vocabulary, 128 rows} box (K-major A)
-            tma_load_2d(sa, &map_a, (int)(ks * kGK), (int)(gi.m_tile * kGM), full);
-          }
-          for (int j = 0; j < nw / 64; ++j)  // B: {64 of d, 64 k rows} boxes (MN-major)
-            tma_load_2d(sa + kGABytes + j * kMnAtomStride, &map_b, (int)(gi.n_tile * kGN + 64 * j),
-                        (int)(ks * kGK), full);
-          if (++stage == kGStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ---------------------------------------------
-    if (lane == 0) {
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, aphase = 0;
-      for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-        const GradItem gi = grad_item<kDW>(it, nb, splits, sps, ksteps);
-        const int nw = (int)min((int64_t)kGN, p.d - gi.n_tile * kGN);
-        const uint32_t idesc = umma_idesc(kGM, nw, kDW, true);
-        if (!mbar_wait(smem_u32(&s_acc_empty[buf]), aphase ^ 1u)) {
-          atomicOr(&p.hdr->flags, kFlagTimeout);
-          *(volatile int*)&s_abort = 1;
-          break;
-        }
-        tmem_fence_after();
-        const uint32_t dacc = tmem + (uint32_t)(buf * kGN);
-        bool ok = true;
-        for (int64_t ks = gi.k0; ks < gi.k1; ++ks) {
-          if (!mbar_wait(smem_u32(&s_full[stage]), phase)) {
-            atomicOr(&p.hdr->flags, kFlagTimeout);
-            *(volatile int*)&s_abort = 1;
-            ok = false;
-            break;
-          }
-          tmem_fence_after();
-          const uint32_t sa = ring_u32 + stage * kGStageBytes;
-#pragma unroll
-          for (int j = 0; j < kGK / 16; ++j) {
-            const uint64_t ad = kDW ? umma_desc_mn(sa + j * 2048, kMnAtomStride)
-                                    : umma_desc_k(sa + j * 32);
-            const uint64_t bd = umma_desc_mn(sa + kGABytes + j * 2048, kMnAtomStride);
-            umma_bf16(dacc, ad, bd, idesc, (ks > gi.k0 || j > 0) ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&s_empty[stage]));
-          if (++stage == kGStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(smem_u32(&s_acc_full[buf]));  // (no MMAs for an empty range: arrives at once)
-        if (++buf == 2) {
-          buf = 0;
-          aphase ^= 1u;
-        }
-      }
-    }
-  } else {
-    // ---------------- epilogue: warps 2..5 ------------------------------------
-    const int quarter = warp & 3;  // TMEM lanes (tile rows) 32*quarter .. +31
-    float* stg = staging + quarter * 32 * kStagePitch;
-    const int sub = lane >> 3, c4 = (lane & 7) * 4;
-    int buf = 0;
-    uint32_t aphase = 0;
-    for (int64_t it = blockIdx.x; it < items && !*(volatile int*)&s_abort; it += gridDim.x) {
-      const GradItem gi = grad_item<kDW>(it, nb, splits, sps, ksteps);
-      const int nw = (int)min((int64_t)kGN, p.d - gi.n_tile * kGN);
-      if (!mbar_wait(smem_u32(&s_acc_full[buf]), aphase)) {
-        atomicOr(&p.hdr->flags, kFlagTimeout);
-        *(volatile int*)&s_abort = 1;
-        break;
-      }
-      tmem_fence_after();
-      const bool empty = gi.k1 <= gi.k0;  // nothing accumulated: the tile is zero
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kGN);
-      for (int c = 0; c < nw; c += 32) {
-        float v[32];
-        if (!empty) {
-          tmem_ld32(tbase + (uint32_t)c, v);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        // transpose through shared memory: thread = row -> 8 threads per row segment
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(stg + lane * kStagePitch + 4 * q) =
-              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = 4 * k + sub;  // row of this warp's 32
-          const float4 x = *reinterpret_cast<const float4*>(stg + row * kStagePitch + c4);
-          const int64_t tr = quarter * 32 + row;  // row inside the 128-row tile
-          if (kDW) {
-            const int64_t v = gi.m_tile * kGM + tr;
-            if (v < p.V)
-              *reinterpret_cast<float4*>(p.out + v * p.d + gi.n_tile * kGN + c + c4) = x;
-          } else {
-            *reinterpret_cast<float4*>(p.out + it * kTileFloats + tr * kGN + c + c4) = x;
-          }
-        }
-        __syncwarp();
-      }
-      tmem_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_acc_empty[buf]));
-      if (++buf == 2) {
-        buf = 0;
-        aphase ^= 1u;
-      }
-    }
-  }
-
-  tmem_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tmem_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  const uint32_t ring = smem_u32(g_smem + ((1024 - (smem_u32(g_smem) & 1023)) & 1023));
+  GradOp<kDW> op{p, &map_a, &map_b, &map_out};
+  op.rank = cluster_rank();
+  op.stg = ring + kPairRingBytes + (uint32_t)((threadIdx.x >> 5) & 3) * 2u * kEpiBoxBytes;
+  pair_pipeline(op, ring, p.hdr);
 }
 
 // dhidden [N, P+C, d]: the scored row (i, P-1+t), t < len_i, is valid token
@@ -280,7 +183,7 @@ __global__ void __launch_bounds__(kThreads)
   pdl_wait();
   pdl_trigger();
   const int4 g = geometry[1];
-  const int64_t nb = g.y, splits = g.z;
+  const int64_t mb = g.x, nb = g.y, splits = g.z;
   const int64_t T = P + C;
   const int64_t total4 = N * T * d / 4;
   for (int64_t e4 = (int64_t)blockIdx.x * kThreads + threadIdx.x; e4 < total4;
@@ -291,11 +194,12 @@ __global__ void __launch_bounds__(kThreads)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (t >= 0 && t < lens[i]) {
       const int64_t r = off[i] + t;
-      const int64_t rb = r / kGM, rr = r - rb * kGM;
+      const int64_t rb = r / kRows, rr = r - rb * kRows;
       const int64_t nt = k / kGN, kk = k - nt * kGN;
-      const float* src = partials + ((rb * nb + nt) * splits) * kTileFloats + rr * kGN + kk;
+      // partial tile of split s: item (s * mb + rb) * nb + nt
+      const float* src = partials + (rb * nb + nt) * kTileFloats + rr * kGN + kk;
       for (int64_t s = 0; s < splits; ++s) {
-        const float4 x = *reinterpret_cast<const float4*>(src + s * kTileFloats);
+        const float4 x = *reinterpret_cast<const float4*>(src + s * mb * nb * kTileFloats);
         acc.x += x.x;
         acc.y += x.y;
         acc.z += x.z;
@@ -307,8 +211,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <bool kDW>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GradParams& p,
-                        const DeviceInfo& dev, cudaStream_t st) {
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                        const GradParams& p, const DeviceInfo& dev, cudaStream_t st) {
   static bool attr_done = false;
   cudaError_t e;
   if (!attr_done) {
@@ -318,8 +222,8 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GradPa
       return e;
     attr_done = true;
   }
-  return launch_pdl(lmhead_grad_gemm_kernel<kDW>, dim3((unsigned)dev.sms), dim3(kGThreads),
-                    (size_t)kGSmem, st, 1, a, b, p);
+  return launch_pdl(lmhead_grad_gemm_kernel<kDW>, dim3((unsigned)(2 * lm_pairs(dev))),
+                    dim3(kPairThreads), (size_t)kGSmem, st, 2, a, b, out, p);
 }
 
 }  // namespace
@@ -345,12 +249,16 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
   // dhidden = dz W: A = dz (K-major, K = vocabulary), B = W (MN-major)
-  CUtensorMap a_dh, b_dh, a_dw, b_dw;
+  CUtensorMap a_dh, b_dh, o_dh, a_dw, b_dw, o_dw;
   cudaError_t e;
-  if ((e = encode_bf16_2d(&a_dh, dz, bl.ldz, bl.rows_cap, bl.ldz, kGM)) != cudaSuccess) return e;
+  if ((e = encode_dz_slabs(&a_dh, const_cast<uint16_t*>(dz), bl.rows_cap, bl.ldz, 128, false)) !=
+      cudaSuccess)
+    return e;
   if ((e = encode_bf16_2d(&b_dh, a.weight, a.d, a.V, a.d, kGK)) != cudaSuccess) return e;
-  p.out = partials;
-  if ((e = launch_gemm<false>(a_dh, b_dh, p, dev, st)) != cudaSuccess) return e;
+  if ((e = encode_store_32x32(&o_dh, partials, true, kGN, bl.items_max * kRows, kGN)) !=
+      cudaSuccess)
+    return e;
+  if ((e = launch_gemm<false>(a_dh, b_dh, o_dh, p, dev, st)) != cudaSuccess) return e;
   int64_t blocks = (a.N * (a.P + a.C) * a.d / 4 + kThreads - 1) / kThreads;
   if (blocks > 4 * (int64_t)dev.sms) blocks = 4 * (int64_t)dev.sms;
   if (blocks < 1) blocks = 1;
@@ -360,10 +268,12 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
     return e;
 
   // dweight = dz^T H: A = dz (MN-major, K = scored rows), B = H (MN-major)
-  if ((e = encode_bf16_2d(&a_dw, dz, bl.ldz, bl.rows_cap, bl.ldz, kGK)) != cudaSuccess) return e;
+  if ((e = encode_dz_slabs(&a_dw, const_cast<uint16_t*>(dz), bl.rows_cap, bl.ldz, 64, false)) !=
+      cudaSuccess)
+    return e;
   if ((e = encode_bf16_2d(&b_dw, dense, a.d, bl.rows_cap, a.d, kGK)) != cudaSuccess) return e;
-  p.out = a.dweight;
-  return launch_gemm<true>(a_dw, b_dw, p, dev, st);
+  if ((e = encode_store_32x32(&o_dw, a.dweight, true, a.d, a.V, a.d)) != cudaSuccess) return e;
+  return launch_gemm<true>(a_dw, b_dw, o_dw, p, dev, st);
 }
 
 }  // namespace grpo

@@ -107,10 +107,132 @@ __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* ma
       : "memory");
 }
 
+// 3-D variant (coordinates x inner, y, z outer).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t sdst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sdst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(mbar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t ssrc, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+      "r"(x), "r"(y), "r"(z), "r"(ssrc)
+      : "memory");
+}
+
+// 2-D TMA store of a shared-memory box to global memory (bulk async group of
+// this thread); x is the inner coordinate.  Parts outside the tensor are not
+// written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t ssrc, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   map),
+               "r"(x), "r"(y), "r"(ssrc)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most N of this thread's bulk groups still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// At most N of this thread's bulk groups not yet complete.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Generic-proxy writes to shared memory become visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ---- CTA pairs (2-SM MMA, .cta_group::2) ----------------------------------------
+// A cluster of two CTAs on two SMs computes one M = 256 tile: CTA r holds rows
+// [128 r, 128 r + 128) of A and half of B's N rows in its own shared memory;
+// one thread of the even CTA (the leader) issues the MMAs, which read both
+// CTAs' operands and write each CTA's 128 rows of D into its own TMEM.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// (map_to_rank: the shared::cluster address of a shared::cta offset in CTA
+// `rank`; cluster_sync: a barrier over both CTAs; both in common.cuh.)
+__device__ __forceinline__ void pair_sync() { cluster_sync(); }
+// Whole warp in each CTA of the pair: allocate / free the same TMEM columns in both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t tmem, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(cols)
+               : "memory");
+}
+// Leader only: D (both CTAs' TMEM, M = 256) (+)= A * B^T.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t tmem_d, uint64_t ad, uint64_t bd,
+                                               uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Leader only: once the MMAs issued so far are done, arrive on the mbarrier at
+// this shared::cta offset in both CTAs of the pair.
+__device__ __forceinline__ void umma_commit_pair(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(mbar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+// TMA load into this CTA's shared memory completing on an mbarrier of either
+// CTA of the pair (`mbar_cluster` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t sdst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(sdst),
+      "l"(map), "r"(x), "r"(y), "r"(mbar_cluster)
+      : "memory");
+}
+// Arrive on an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster)
+               : "memory");
+}
+
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with row pitch
 // `pitch` elements, box {64, box_outer}, 128-byte swizzle; reads outside the
 // extents return zeros.
 cudaError_t encode_bf16_2d(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
                            int64_t pitch, int box_outer);
+// The logits gradient dz of the scored rows is kept in vocabulary slabs:
+// [ldz / 64][rows][64] bf16, so that a TMA box of 64 vocabulary columns by
+// 64 or 128 rows is one contiguous 8 or 16 KiB block.  Tensor map of that
+// layout with box {64, box_rows, 1} (128-byte swizzle, loads) or, with
+// `store`, box {32, 32, 1} (64-byte swizzle, the epilogue's stores).
+cudaError_t encode_dz_slabs(CUtensorMap* map, void* base, int64_t rows, int64_t ldz, int box_rows,
+                            bool store);
+// Tensor map of a row-major [outer, inner] matrix for the epilogues' 32 x 32
+// TMA stores: bf16 (64-byte rows, 64-byte swizzle) or fp32 (128-byte rows,
+// 128-byte swizzle); pitch in elements.
+cudaError_t encode_store_32x32(CUtensorMap* map, void* base, bool fp32, int64_t inner,
+                               int64_t outer, int64_t pitch);
 
 }  // namespace grpo
