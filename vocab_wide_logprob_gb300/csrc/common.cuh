@@ -524,7 +524,7 @@ struct LmBwdLayout {
   size_t geometry;     // int4[2]: projection pass; hidden-gradient contraction
   size_t dense;        // bf16 [rows_cap, d]
   size_t dz;           // bf16 [ldz / 64][rows_cap][64] (vocabulary slabs)
-  size_t dh_partials;  // fp32 [items_max][256][256]
+  size_t dh_partials;  // fp32 [items_max][256][512]
   size_t total;
   int64_t rows_cap;    // N*C rounded up to 256
   int64_t ldz;         // V rounded up to 256

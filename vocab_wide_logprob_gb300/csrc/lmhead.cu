@@ -96,7 +96,7 @@ __device__ int2 choose_split_block(int32_t units, int32_t ksteps, int slots, int
 
 // geometry[0]: the projection pass (256-row blocks, vocabulary splits, tiles
 // per split, 0).  With `grad_gemm`, geometry[1]: the hidden-state gradient
-// contraction (256-row blocks, 256-wide d tiles, vocabulary splits, 64-wide
+// contraction (256-row blocks, 512-wide d tiles, vocabulary splits, 64-wide
 // k-steps per split).  `pairs`: CTA pairs of the tensor-core kernels.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                                                uint16_t* __restrict__ dense,
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
     if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
   }
   if (grad_gemm && blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
-    const int32_t nb = (int32_t)((d + 255) / 256);
+    const int32_t nb = (int32_t)((d + 511) / 512);
     const int32_t ksteps = (int32_t)((V + kVTile - 1) / kVTile) * (kVTile / kK);
     const int2 s = choose_split_block(mb * nb, ksteps, pairs, 2 * pairs + mb * nb);
     if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
@@ -164,6 +164,9 @@ __device__ __forceinline__ int completion_of(const int32_t* off, int64_t N, int6
 // kMode 1: the bf16 logits gradient, stored by TMA.
 template <int kMode>
 struct LmOp {
+  static constexpr int kStages = kPairStages;
+  static constexpr int kStageBytes = kPairStageBytes;
+  static constexpr int kAccCols = 256;
   const LmParams& p;
   const CUtensorMap* map_h;
   const CUtensorMap* map_w;
@@ -538,13 +541,13 @@ LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms) {
   const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
   l.rows_cap = mb_max * kRows;
   l.ldz = (V + kVTile - 1) / kVTile * kVTile;
-  const int64_t nb = (d + 255) / 256;
+  const int64_t nb = (d + 511) / 512;  // d tiles of the hidden-state gradient
   l.items_max = 2 * pairs + mb_max * nb;
   l.geometry = base.total;
   l.dense = align_up(base.total + 32, 1024);
   l.dz = align_up(l.dense + (size_t)l.rows_cap * (size_t)d * 2, 1024);
   l.dh_partials = align_up(l.dz + (size_t)l.rows_cap * (size_t)l.ldz * 2, 1024);
-  l.total = align_up(l.dh_partials + (size_t)l.items_max * kRows * 256 * sizeof(float), 256);
+  l.total = align_up(l.dh_partials + (size_t)l.items_max * kRows * 512 * sizeof(float), 256);
   return l;
 }
 

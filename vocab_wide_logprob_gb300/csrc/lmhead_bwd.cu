@@ -14,43 +14,84 @@
 // operand where the contraction runs over its row index, so nothing is
 // transposed in memory.
 //
-// lmhead_grad_gemm_kernel<false>  dhidden partials: items (range of
-//     vocabulary k-steps, 256 rows, 256 columns of d), fp32 tiles in the
+// lmhead_grad_gemm_kernel<DhOp>   dhidden partials: items (range of
+//     vocabulary k-steps, 256 rows, up to 512 columns of d), fp32 tiles in the
 //     workspace
 // lmhead_dh_reduce_kernel         sums a row's partials in split order
 //     (deterministic) into dhidden [N, P+C, d]; rows that score nothing get 0
-// lmhead_grad_gemm_kernel<true>   dweight: items (256 vocabulary rows, 256
+// lmhead_grad_gemm_kernel<DwOp>   dweight: items (256 vocabulary rows, 512
 //     columns of d), K = every scored row, fp32 straight to dweight [V, d]
 //
 // The epilogue warps drain TMEM into 32 x 32 shared-memory boxes (128-byte
 // swizzle, two per warp) that TMA stores write out while the next box fills.
-// d must be a multiple of 128: each CTA of a pair holds half of a d tile of
-// 256 (or 128) columns as whole 64-column MN-major atoms.
+// d must be a multiple of 128: each CTA of a pair holds half of every MMA's
+// N columns (256 or 128) as whole 64-column MN-major atoms.
 #include "pair_pipeline.cuh"
 
 namespace grpo {
 namespace {
 
 constexpr int kRows = 256;                 // output rows per pair tile (128 per CTA)
-constexpr int kGN = 256;                   // output columns per tile (the last d tile may be 128)
 constexpr int kGK = 64;                    // k per stage
 constexpr int kGABytes = 128 * kGK * 2;    // this CTA's A: 16 KiB
 constexpr uint32_t kMnAtomStride = 8192;   // 64 M/N elements x 64 K rows x 2 bytes (one TMA box)
 constexpr int kEpiBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA-store box
-constexpr int kGSmem = kPairRingBytes + 4 * 2 * kEpiBoxBytes + 1024;
-constexpr int64_t kTileFloats = (int64_t)kRows * kGN;
+constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;
+constexpr int kDhN = 512;                  // dhidden: d columns per item (two MMAs of <= 256)
+constexpr int64_t kDhTileFloats = (int64_t)kRows * kDhN;
 
 struct GradParams {
   int64_t N, V, d;
   const int32_t* offsets;  // [N+1]: offsets[N] = scored rows
-  const int4* geometry;    // [1]: (row blocks, d tiles, splits, k-steps per split)
+  const int4* geometry;    // [1]: (row blocks, d tiles of 512, splits, k-steps per split)
   int64_t ksteps_v;        // vocabulary k-steps of the hidden-state gradient (ldz / 64)
   WsHeader* hdr;
 };
 
-// kDW false: dhidden partial tiles; true: dweight.
-template <bool kDW>
-struct GradOp {
+// Drains `nw` accumulator columns of this warp's 32 TMEM lanes through two
+// 32 x 32 fp32 boxes (128-byte swizzle) into TMA stores at (x0 + c, y).
+__device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t stg,
+                                           uint32_t& chunk, uint32_t tbase, int nw, bool empty,
+                                           int x0, int y) {
+  const int lane = threadIdx.x & 31;
+  for (int c = 0; c < nw; c += 32) {
+    float v[32];
+    if (!empty) {
+      tmem_ld32(tbase + (uint32_t)c, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    }
+    // row `lane` of the box; 16-byte chunk q sits at q ^ (lane & 7)
+    const uint32_t box = stg + (chunk & 1u) * (uint32_t)kEpiBoxBytes;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last used this box has read it
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(box + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4),
+                   __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                   __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map_out, box, x0 + c, y);
+      bulk_commit();
+    }
+    ++chunk;
+  }
+}
+
+// dhidden = dz W.  Items (vocabulary split, 256-row block, d tile of up to
+// 512): A = dz (K-major, one {64 vocabulary, 128 rows} slab box per CTA), B =
+// W (MN-major): the d tile is two MMAs of N0 <= 256 and N1 = width - N0
+// columns sharing A, each split over the pair (N / 2 columns per CTA, whole
+// 64-column atoms), accumulating into TMEM columns [0, N0) and [256, 256 + N1).
+// Fewer operand bytes per FLOP than 256-column tiles: the kernel is bound by
+// how fast operands arrive from L2, and its epilogue runs once per long item.
+struct DhOp {
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = kGABytes + 2 * 16384;  // A + up to 256 B columns
+  static constexpr int kAccCols = 512;
   const GradParams& p;
   const CUtensorMap* map_a;
   const CUtensorMap* map_b;
@@ -60,100 +101,62 @@ struct GradOp {
   uint32_t chunk;
 
   __device__ void setup() {
-    nb = (p.d + kGN - 1) / kGN;
-    const int64_t tv = p.offsets[p.N];
-    if (kDW) {
-      ksteps = (tv + kGK - 1) / kGK;  // rows past tv are zero in both operands
-      sps = ksteps;
-      mb = (p.V + kRows - 1) / kRows;
-      n_items = mb * nb;
-    } else {
-      const int4 g = p.geometry[1];
-      mb = g.x;
-      sps = g.w;
-      ksteps = p.ksteps_v;
-      n_items = (int64_t)g.x * g.y * g.z;
-    }
+    nb = (p.d + kDhN - 1) / kDhN;
+    const int4 g = p.geometry[1];
+    mb = g.x;
+    sps = g.w;
+    ksteps = p.ksteps_v;
+    n_items = (int64_t)g.x * g.y * g.z;
     chunk = 0;
   }
-  // dweight: it = m tile * nb + d tile.  dhidden: it = (split * mb + m tile) * nb + d tile,
-  // so the items running at the same time share their vocabulary range in L2.
-  __device__ int64_t m_tile(int64_t it) const { return kDW ? it / nb : (it / nb) % mb; }
+  // it = (split * mb + row block) * nb + d tile: the items running at the same
+  // time share their vocabulary range in L2.
+  __device__ int64_t m_tile(int64_t it) const { return (it / nb) % mb; }
   __device__ int64_t n_tile(int64_t it) const { return it % nb; }
-  __device__ int width(int64_t it) const { return (int)min((int64_t)kGN, p.d - n_tile(it) * kGN); }
+  __device__ int width(int64_t it) const { return (int)min((int64_t)kDhN, p.d - n_tile(it) * kDhN); }
   __device__ int64_t items() const { return n_items; }
   __device__ int tiles(int64_t) const { return 1; }
   __device__ void krange(int64_t it, int, int64_t* k0, int64_t* k1) const {
-    if (kDW) {
-      *k0 = 0;
-      *k1 = ksteps;
-    } else {
-      *k0 = (it / nb / mb) * sps;
-      *k1 = min(ksteps, *k0 + sps);
-    }
+    *k0 = (it / nb / mb) * sps;
+    *k1 = min(ksteps, *k0 + sps);
   }
   __device__ uint32_t bytes(int64_t it, int) const {
     return (uint32_t)(kGABytes + (width(it) / 2) * kGK * 2);
   }
   __device__ void load(uint32_t sa, int64_t it, int, int64_t ks, uint32_t rk,
                        uint32_t mbar) const {
-    const int64_t mt = m_tile(it), nt = n_tile(it);
-    const int half = width(it) / 2;
-    if (kDW) {  // dz^T: two {64 vocabulary, 64 rows} slab boxes (MN-major A)
-      for (int j = 0; j < 2; ++j)
-        tma_load_3d_pair(sa + j * kMnAtomStride, map_a, 0, (int)(ks * kGK),
-                         (int)(mt * (kRows / 64) + rk * 2 + j), mbar);
-    } else {    // dz: one {64 vocabulary, 128 rows} slab box (K-major A)
-      tma_load_3d_pair(sa, map_a, 0, (int)(mt * kRows + rk * 128), (int)ks, mbar);
-    }
-    for (int j = 0; j < half / 64; ++j)  // B: this CTA's half of the d tile, {64 of d, 64 k rows}
-      tma_load_2d_pair(sa + kPairBOffset + j * kMnAtomStride, map_b,
-                       (int)(nt * kGN + rk * half + 64 * j), (int)(ks * kGK), mbar);
+    const int64_t d0 = n_tile(it) * kDhN;
+    const int w = width(it), n0 = min(w, 256), n1 = w - n0;
+    tma_load_3d_pair(sa, map_a, 0, (int)(m_tile(it) * kRows + rk * 128), (int)ks, mbar);
+    const uint32_t sb = sa + kGABytes;
+    for (int j = 0; j < n0 / 128; ++j)  // first MMA: this CTA's n0 / 2 columns
+      tma_load_2d_pair(sb + j * kMnAtomStride, map_b, (int)(d0 + rk * (n0 / 2) + 64 * j),
+                       (int)(ks * kGK), mbar);
+    for (int j = 0; j < n1 / 128; ++j)  // second MMA: this CTA's n1 / 2 columns
+      tma_load_2d_pair(sb + 16384 + j * kMnAtomStride, map_b,
+                       (int)(d0 + 256 + rk * (n1 / 2) + 64 * j), (int)(ks * kGK), mbar);
   }
   __device__ void mma(uint32_t dacc, uint32_t sa, int64_t it, int, bool first) const {
-    const uint32_t idesc = umma_idesc(256, width(it), kDW, true);
+    const int w = width(it), n0 = min(w, 256), n1 = w - n0;
+    const uint32_t id0 = umma_idesc(256, n0, false, true);
+    const uint32_t id1 = umma_idesc(256, n1 > 0 ? n1 : 16, false, true);
+    const uint32_t sb = sa + kGABytes;
 #pragma unroll
     for (int j = 0; j < kGK / 16; ++j) {
-      const uint64_t ad = kDW ? umma_desc_mn(sa + j * 2048, kMnAtomStride)
-                              : umma_desc_k(sa + j * 32);
-      const uint64_t bd = umma_desc_mn(sa + kPairBOffset + j * 2048, kMnAtomStride);
-      umma_bf16_pair(dacc, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+      const uint64_t ad = umma_desc_k(sa + j * 32);
+      const uint32_t acc = (first && j == 0) ? 0u : 1u;
+      umma_bf16_pair(dacc, ad, umma_desc_mn(sb + j * 2048, kMnAtomStride), id0, acc);
+      if (n1 > 0)
+        umma_bf16_pair(dacc + 256, ad, umma_desc_mn(sb + 16384 + j * 2048, kMnAtomStride), id1,
+                       acc);
     }
   }
   __device__ void epi_begin(int64_t) {}
   __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty) {
-    const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
-    const int nw = width(it);
-    // box origin: dweight [V, d] at (vocabulary row, d column); partial tile `it` as rows
-    // it*256 .. of an [items*256, 256] matrix
-    const int y = kDW ? (int)(m_tile(it) * kRows + rank * 128 + quarter * 32)
-                      : (int)(it * kRows + rank * 128 + quarter * 32);
-    const int x0 = kDW ? (int)(n_tile(it) * kGN) : 0;
-    for (int c = 0; c < nw; c += 32) {
-      float v[32];
-      if (!empty) {
-        tmem_ld32(tbase + (uint32_t)c, v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      }
-      // row `lane` of the box; 16-byte chunk q sits at q ^ (lane & 7)
-      const uint32_t box = stg + (chunk & 1u) * (uint32_t)kEpiBoxBytes;
-      if (lane == 0) bulk_wait_read<1>();  // the store that last used this box has read it
-      __syncwarp();
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(box + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4),
-                     __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                     __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(map_out, box, x0 + c, y);
-        bulk_commit();
-      }
-      ++chunk;
-    }
+    // partial tile `it`: rows it*256 .. of an [items*256, 512] matrix
+    const int quarter = (threadIdx.x >> 5) & 3;
+    drain_fp32(map_out, stg, chunk, tbase, width(it), empty, 0,
+               (int)(it * kRows + rank * 128 + quarter * 32));
   }
   __device__ void epi_end(int64_t) {}
   __device__ void epi_finish() {
@@ -161,69 +164,162 @@ struct GradOp {
   }
 };
 
-template <bool kDW>
+// dweight = dz^T H.  Items (256-vocabulary block, d tile of kN), K = every
+// scored row: A = dz^T (MN-major, two {64 vocabulary, 64 rows} slab boxes per
+// CTA), B = H (MN-major, each CTA holding half of every MMA's N columns).
+// kN = 256: two accumulators, so the epilogue of one item (128 KiB of fp32 per
+// CTA) overlaps the next item's MMAs.  kN = 512: two MMAs share A (fewer
+// operand bytes per FLOP), one accumulator.
+template <int kN>
+struct DwOp {
+  static constexpr int kStages = kN == 512 ? 4 : kPairStages;
+  static constexpr int kStageBytes = kGABytes + (kN / 2) * kGK * 2;
+  static constexpr int kAccCols = kN;
+  const GradParams& p;
+  const CUtensorMap* map_a;
+  const CUtensorMap* map_b;
+  const CUtensorMap* map_out;
+  uint32_t rank, stg;
+  int64_t nb, ksteps, n_items;
+  uint32_t chunk;
+
+  __device__ void setup() {
+    nb = (p.d + kN - 1) / kN;
+    ksteps = (p.offsets[p.N] + kGK - 1) / kGK;  // rows past the last scored one are zero
+    n_items = (p.V + kRows - 1) / kRows * nb;
+    chunk = 0;
+  }
+  __device__ int64_t m_tile(int64_t it) const { return it / nb; }
+  __device__ int64_t n_tile(int64_t it) const { return it % nb; }
+  __device__ int width(int64_t it) const { return (int)min((int64_t)kN, p.d - n_tile(it) * kN); }
+  __device__ int64_t items() const { return n_items; }
+  __device__ int tiles(int64_t) const { return 1; }
+  __device__ void krange(int64_t, int, int64_t* k0, int64_t* k1) const {
+    *k0 = 0;
+    *k1 = ksteps;
+  }
+  __device__ uint32_t bytes(int64_t it, int) const {
+    return (uint32_t)(kGABytes + (width(it) / 2) * kGK * 2);
+  }
+  __device__ void load(uint32_t sa, int64_t it, int, int64_t ks, uint32_t rk,
+                       uint32_t mbar) const {
+    const int64_t mt = m_tile(it), d0 = n_tile(it) * kN;
+    const int w = width(it), n0 = min(w, 256), n1 = w - n0;
+    for (int j = 0; j < 2; ++j)
+      tma_load_3d_pair(sa + j * kMnAtomStride, map_a, 0, (int)(ks * kGK),
+                       (int)(mt * (kRows / 64) + rk * 2 + j), mbar);
+    const uint32_t sb = sa + kGABytes;
+    for (int j = 0; j < n0 / 128; ++j)
+      tma_load_2d_pair(sb + j * kMnAtomStride, map_b, (int)(d0 + rk * (n0 / 2) + 64 * j),
+                       (int)(ks * kGK), mbar);
+    for (int j = 0; j < n1 / 128; ++j)
+      tma_load_2d_pair(sb + 16384 + j * kMnAtomStride, map_b,
+                       (int)(d0 + 256 + rk * (n1 / 2) + 64 * j), (int)(ks * kGK), mbar);
+  }
+  __device__ void mma(uint32_t dacc, uint32_t sa, int64_t it, int, bool first) const {
+    const int w = width(it), n0 = min(w, 256), n1 = w - n0;
+    const uint32_t id0 = umma_idesc(256, n0, true, true);
+    const uint32_t id1 = umma_idesc(256, n1 > 0 ? n1 : 16, true, true);
+    const uint32_t sb = sa + kGABytes;
+#pragma unroll
+    for (int j = 0; j < kGK / 16; ++j) {
+      const uint64_t ad = umma_desc_mn(sa + j * 2048, kMnAtomStride);
+      const uint32_t acc = (first && j == 0) ? 0u : 1u;
+      umma_bf16_pair(dacc, ad, umma_desc_mn(sb + j * 2048, kMnAtomStride), id0, acc);
+      if (n1 > 0)
+        umma_bf16_pair(dacc + 256, ad, umma_desc_mn(sb + 16384 + j * 2048, kMnAtomStride), id1,
+                       acc);
+    }
+  }
+  __device__ void epi_begin(int64_t) {}
+  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty) {
+    // dweight [V, d] at (vocabulary row, d column); rows past V are not stored
+    const int quarter = (threadIdx.x >> 5) & 3;
+    drain_fp32(map_out, stg, chunk, tbase, width(it), empty, (int)(n_tile(it) * kN),
+               (int)(m_tile(it) * kRows + rank * 128 + quarter * 32));
+  }
+  __device__ void epi_end(int64_t) {}
+  __device__ void epi_finish() {
+    if ((threadIdx.x & 31) == 0) bulk_wait<0>();  // every store has completed
+  }
+};
+
+constexpr int kDwN = 512;  // dweight: d columns per item (measured faster than 256)
+
+template <class Op>
 __global__ void __launch_bounds__(kPairThreads, 1)
     lmhead_grad_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_out, const GradParams p) {
   extern __shared__ __align__(1024) unsigned char g_smem[];
   const uint32_t ring = smem_u32(g_smem + ((1024 - (smem_u32(g_smem) & 1023)) & 1023));
-  GradOp<kDW> op{p, &map_a, &map_b, &map_out};
+  Op op{p, &map_a, &map_b, &map_out};
   op.rank = cluster_rank();
-  op.stg = ring + kPairRingBytes + (uint32_t)((threadIdx.x >> 5) & 3) * 2u * kEpiBoxBytes;
+  op.stg = ring + Op::kStages * Op::kStageBytes +
+           (uint32_t)((threadIdx.x >> 5) & 3) * 2u * kEpiBoxBytes;
   pair_pipeline(op, ring, p.hdr);
 }
 
 // dhidden [N, P+C, d]: the scored row (i, P-1+t), t < len_i, is valid token
 // r = offsets[i] + t; its value is the sum of its split partials in order.
-__global__ void __launch_bounds__(kThreads)
+// A CTA per output row (index arithmetic once per row), 16-byte accesses.
+constexpr int kReduceThreads = 128;
+
+__global__ void __launch_bounds__(kReduceThreads)
     lmhead_dh_reduce_kernel(const float* __restrict__ partials, const int4* __restrict__ geometry,
                             const int32_t* __restrict__ off, const int32_t* __restrict__ lens,
                             int64_t N, int64_t P, int64_t C, int64_t d, float* __restrict__ dh) {
   pdl_wait();
   pdl_trigger();
   const int4 g = geometry[1];
-  const int64_t mb = g.x, nb = g.y, splits = g.z;
-  const int64_t T = P + C;
-  const int64_t total4 = N * T * d / 4;
-  for (int64_t e4 = (int64_t)blockIdx.x * kThreads + threadIdx.x; e4 < total4;
-       e4 += (int64_t)gridDim.x * kThreads) {
-    const int64_t e = e4 * 4;
-    const int64_t row_all = e / d, k = e - row_all * d;
-    const int64_t i = row_all / T, t = row_all - i * T - (P - 1);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t >= 0 && t < lens[i]) {
-      const int64_t r = off[i] + t;
-      const int64_t rb = r / kRows, rr = r - rb * kRows;
-      const int64_t nt = k / kGN, kk = k - nt * kGN;
+  const int64_t mb = g.x, nb = g.y;
+  const int splits = g.z;
+  const int64_t T = P + C, rows = N * T;
+  const int d4 = (int)(d / 4);
+  const int64_t split_stride = mb * nb * kDhTileFloats;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int64_t i = row / T, t = row - i * T - (P - 1);
+    float4* dst = reinterpret_cast<float4*>(dh + row * d);
+    if (t < 0 || t >= lens[i]) {
+      for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads)
+        dst[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
+    const int64_t r = off[i] + t;
+    const int64_t rb = r / kRows, rr = r - rb * kRows;
+    for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads) {
+      const int k = 4 * k4, nt = k / kDhN, kk = k - nt * kDhN;
       // partial tile of split s: item (s * mb + rb) * nb + nt
-      const float* src = partials + (rb * nb + nt) * kTileFloats + rr * kGN + kk;
-      for (int64_t s = 0; s < splits; ++s) {
-        const float4 x = *reinterpret_cast<const float4*>(src + s * mb * nb * kTileFloats);
+      const float* src = partials + (rb * nb + nt) * kDhTileFloats + rr * kDhN + kk;
+      float4 acc = *reinterpret_cast<const float4*>(src);
+#pragma unroll 4
+      for (int s = 1; s < splits; ++s) {
+        const float4 x = *reinterpret_cast<const float4*>(src + s * split_stride);
         acc.x += x.x;
         acc.y += x.y;
         acc.z += x.z;
         acc.w += x.w;
       }
+      dst[k4] = acc;
     }
-    reinterpret_cast<float4*>(dh)[e4] = acc;
   }
 }
 
-template <bool kDW>
+template <class Op>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GradParams& p, const DeviceInfo& dev, cudaStream_t st) {
+  constexpr int smem = Op::kStages * Op::kStageBytes + kEpiBytes + 1024;
   static bool attr_done = false;
   cudaError_t e;
   if (!attr_done) {
-    if ((e = cudaFuncSetAttribute(lmhead_grad_gemm_kernel<kDW>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) !=
+    if ((e = cudaFuncSetAttribute(lmhead_grad_gemm_kernel<Op>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
       return e;
     attr_done = true;
   }
-  return launch_pdl(lmhead_grad_gemm_kernel<kDW>, dim3((unsigned)(2 * lm_pairs(dev))),
-                    dim3(kPairThreads), (size_t)kGSmem, st, 2, a, b, out, p);
+  return launch_pdl(lmhead_grad_gemm_kernel<Op>, dim3((unsigned)(2 * lm_pairs(dev))),
+                    dim3(kPairThreads), (size_t)smem, st, 2, a, b, out, p);
 }
 
 }  // namespace
@@ -255,14 +351,15 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
       cudaSuccess)
     return e;
   if ((e = encode_bf16_2d(&b_dh, a.weight, a.d, a.V, a.d, kGK)) != cudaSuccess) return e;
-  if ((e = encode_store_32x32(&o_dh, partials, true, kGN, bl.items_max * kRows, kGN)) !=
+  if ((e = encode_store_32x32(&o_dh, partials, true, kDhN, bl.items_max * kRows, kDhN)) !=
       cudaSuccess)
     return e;
-  if ((e = launch_gemm<false>(a_dh, b_dh, o_dh, p, dev, st)) != cudaSuccess) return e;
-  int64_t blocks = (a.N * (a.P + a.C) * a.d / 4 + kThreads - 1) / kThreads;
-  if (blocks > 4 * (int64_t)dev.sms) blocks = 4 * (int64_t)dev.sms;
+  if ((e = launch_gemm<DhOp>(a_dh, b_dh, o_dh, p, dev, st)) != cudaSuccess) return e;
+  int64_t blocks = a.N * (a.P + a.C);  // a CTA per row
+  if (blocks > 16 * (int64_t)dev.sms) blocks = 16 * (int64_t)dev.sms;
   if (blocks < 1) blocks = 1;
-  if ((e = launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1,
+  if ((e = launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0,
+                      st, 1,
                       (const float*)partials, geometry, off, lens, a.N, a.P, a.C, a.d,
                       a.dhidden)) != cudaSuccess)
     return e;
@@ -273,7 +370,7 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
     return e;
   if ((e = encode_bf16_2d(&b_dw, dense, a.d, bl.rows_cap, a.d, kGK)) != cudaSuccess) return e;
   if ((e = encode_store_32x32(&o_dw, a.dweight, true, a.d, a.V, a.d)) != cudaSuccess) return e;
-  return launch_gemm<true>(a_dw, b_dw, o_dw, p, dev, st);
+  return launch_gemm<DwOp<kDwN>>(a_dw, b_dw, o_dw, p, dev, st);
 }
 
 }  // namespace grpo

@@ -7,12 +7,13 @@
 // 64-wide k-steps.  Per CTA:
 //   warp 0 (one lane)  TMA producer: loads this CTA's 128 rows of A and its half
 //                      of B's N rows for each k-step into a ring of
-//                      kPairStages 32 KiB stages; the loads of both CTAs
+//                      Op::kStages stages; the loads of both CTAs
 //                      complete on the leader's `full` barrier.
 //   warp 1 (one lane)  on the leader only: issues tcgen05.mma.cta_group::2
 //                      (M = 256, K = 16) into one of two 256-column TMEM
-//                      accumulators; commits free the stage (`empty`) and
-//                      publish the tile (`acc_full`) in both CTAs at once.
+//                      accumulators (or one of up to 512 columns); commits
+//                      free the stage (`empty`) and publish the tile
+//                      (`acc_full`) in both CTAs at once.
 //   warps 2-5          epilogue: each reads this CTA's 128 TMEM lanes of the
 //                      finished tile (warp w owns lanes 32 (w % 4) ..) and
 //                      hands the accumulator back (`acc_empty` on the leader,
@@ -31,12 +32,17 @@
 namespace grpo {
 
 constexpr int kPairThreads = 192;
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 6;          // the default ring: 6 stages of 32 KiB
 constexpr int kPairStageBytes = 32768;  // A 16 KiB + B half <= 16 KiB per CTA
 constexpr int kPairBOffset = 16384;     // B half inside a stage
 constexpr int kPairRingBytes = kPairStages * kPairStageBytes;
 
 // Op:
+//   static constexpr int kStages, kStageBytes   the ring (kStages * kStageBytes <= the
+//                                               dynamic shared memory before `ring` + ...)
+//   static constexpr int kAccCols               256: two accumulators, the epilogue of one
+//                                               tile overlaps the MMAs of the next; 512:
+//                                               one accumulator of up to 512 columns
 //   int64_t items() const;  int tiles(int64_t it) const;
 //   void krange(int64_t it, int t, int64_t* k0, int64_t* k1) const;
 //   uint32_t bytes(int64_t it, int t) const;            this CTA's bytes per k-step
@@ -47,8 +53,12 @@ constexpr int kPairRingBytes = kPairStages * kPairStageBytes;
 //                  bool empty); void epi_end(int64_t it); void epi_finish();
 template <class Op>
 __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* hdr) {
-  __shared__ __align__(8) uint64_t s_full[kPairStages];
-  __shared__ __align__(8) uint64_t s_empty[kPairStages];
+  constexpr int kStages = Op::kStages;
+  constexpr uint32_t kStageBytes = Op::kStageBytes;
+  constexpr int kBufs = Op::kAccCols == 512 ? 1 : 2;
+  constexpr uint32_t kAccCols = Op::kAccCols;
+  __shared__ __align__(8) uint64_t s_full[kStages];
+  __shared__ __align__(8) uint64_t s_empty[kStages];
   __shared__ __align__(8) uint64_t s_acc_full[2];
   __shared__ __align__(8) uint64_t s_acc_empty[2];
   __shared__ uint32_t s_tmem;
@@ -60,7 +70,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
 
   if (tid == 0) {
     s_abort = 0;
-    for (int k = 0; k < kPairStages; ++k) {
+    for (int k = 0; k < kStages; ++k) {
       mbar_init(smem_u32(&s_full[k]), 1);   // leader: its producer's arrive (+ both CTAs' bytes)
       mbar_init(smem_u32(&s_empty[k]), 1);  // the leader's multicast commit
     }
@@ -70,7 +80,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
     }
     mbar_init_fence();
   }
-  if (warp == 1) tmem_alloc_pair(&s_tmem, 512);  // two 256-column fp32 accumulators
+  if (warp == 1) tmem_alloc_pair(&s_tmem, 512);  // all 512 columns: kBufs accumulators
   tmem_fence_before();
   pair_sync();  // barriers and TMEM exist in both CTAs before any cross-CTA use
   tmem_fence_after();
@@ -102,9 +112,8 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
             }
             const uint32_t full = smem_u32(&s_full[stage]);
             if (rank == 0) mbar_arrive_expect_tx(full, 2u * bytes);
-            op.load(ring + (uint32_t)stage * kPairStageBytes, it, t, ks, rank,
-                    map_to_rank(full, 0));
-            if (++stage == kPairStages) {
+            op.load(ring + (uint32_t)stage * kStageBytes, it, t, ks, rank, map_to_rank(full, 0));
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
@@ -124,7 +133,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
             break;
           }
           tmem_fence_after();
-          const uint32_t dacc = tmem + (uint32_t)(buf * 256);
+          const uint32_t dacc = tmem + (uint32_t)buf * kAccCols;
           int64_t k0, k1;
           op.krange(it, t, &k0, &k1);
           bool ok = true;
@@ -135,16 +144,16 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
               break;
             }
             tmem_fence_after();
-            op.mma(dacc, ring + (uint32_t)stage * kPairStageBytes, it, t, ks == k0);
+            op.mma(dacc, ring + (uint32_t)stage * kStageBytes, it, t, ks == k0);
             umma_commit_pair(smem_u32(&s_empty[stage]));  // the stage is free in both CTAs
-            if (++stage == kPairStages) {
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
           umma_commit_pair(smem_u32(&s_acc_full[buf]));  // (an empty range: arrives at once)
-          if (++buf == 2) {
+          if (++buf == kBufs) {
             buf = 0;
             aphase ^= 1u;
           }
@@ -170,12 +179,12 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
         tmem_fence_after();
         int64_t k0, k1;
         op.krange(it, t, &k0, &k1);
-        op.epi_tile(it, t, tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 256),
+        op.epi_tile(it, t, tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * kAccCols,
                     k1 <= k0);
         tmem_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
-        if (++buf == 2) {
+        if (++buf == kBufs) {
           buf = 0;
           aphase ^= 1u;
         }
