@@ -111,7 +111,9 @@ KERNEL_SOURCES = {
     "dlogits_kernel": ("dlogits.cu", "common.cuh"),
     "lse_gather_kernel": ("lse_gather.cu", "common.cuh"),
     "grpo_loss_fwd_bwd": ("fused.cu", "dlogits.cu", "lse_gather.cu", "common.cuh"),
-    "lmhead_lse_kernel": ("lmhead.cu", "common.cuh"),
+    "lmhead_lse_kernel": ("lmhead.cu", "lmhead.cuh", "pair_pipeline.cuh", "tc.cuh", "common.cuh"),
+    "lmhead_fwd_bwd": ("lmhead.cu", "lmhead_bwd.cu", "lmhead.cuh", "pair_pipeline.cuh", "tc.cuh",
+                       "common.cuh", "mask_advantage.cu", "lse_gather.cu", "surrogate.cu"),
 }
 
 
@@ -677,7 +679,8 @@ def run_lmhead(args, w: wl.Workload):
                      "bound": "tensor", "achieved": tflops, "peak": peak,
                      "peak_source": "measured" if peaks.get("bf16_tflops") else "fallback",
                      "unit": "TFLOP/s", "frac": tflops / peak, "flops_per_step": flops,
-                     "traffic": None if train else recorded_traffic("lmhead_lse_kernel", w, d)},
+                     "traffic": recorded_traffic("lmhead_fwd_bwd" if train else
+                                                 "lmhead_lse_kernel", w, d)},
         "gpu_launches": (13 if train else 5) * args.steps, "clocks": clocks,
     }
     if train:

@@ -5,6 +5,7 @@
 #include <stdlib.h>
 
 #include "common.cuh"
+#include "lmhead.cuh"
 #include "grpo.h"
 
 namespace grpo {

@@ -504,50 +504,4 @@ cudaError_t launch_lse_grad(const FwdArgs& a, const BwdArgs& b, const DeviceInfo
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, const DeviceInfo& d,
                         cudaStream_t st);
 
-// LM-head log-probs (tensor cores): workspace beyond the base layout holds a
-// dense copy of the scored rows' hidden states and the per-item partials.
-struct LmLayout {
-  size_t geometry;  // int4: row blocks, vocabulary splits, tiles per split
-  size_t dense;     // bf16 [N*C rounded up to 256, d]
-  size_t partials;  // float4 [items][128]
-  size_t total;
-};
-LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms);
-// After launch_prep: gather, tensor-core log-sum-exp, merge.
-cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs& a, int64_t d,
-                          const DeviceInfo& dev, cudaStream_t st);
-
-// Gradients through the LM head.  Workspace beyond the base layout: the two
-// geometries, the dense scored hidden rows, the bf16 logits gradient of the
-// scored rows, and the split partials of the hidden-state gradient.
-struct LmBwdLayout {
-  size_t geometry;     // int4[2]: projection pass; hidden-gradient contraction
-  size_t dense;        // bf16 [rows_cap, d]
-  size_t dz;           // bf16 [ldz / 64][rows_cap][64] (vocabulary slabs)
-  size_t dh_partials;  // fp32 [items_max][256][512]
-  size_t total;
-  int64_t rows_cap;    // N*C rounded up to 256
-  int64_t ldz;         // V rounded up to 256
-  int64_t items_max;
-};
-LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms);
-struct LmBwdArgs {
-  const void* hidden;   // bf16 [N, P+C, d]
-  const void* weight;   // bf16 [V, d]
-  int64_t N, P, C, V, d;
-  const int64_t* ids;
-  const float* lse;     // [N, C]
-  const float* w;       // [N, C]
-  const float* grad;    // nullable: 1
-  float* dhidden;       // fp32 [N, P+C, d]
-  float* dweight;       // fp32 [V, d]
-  void* ws;
-};
-// CTA pairs of the tensor-core kernels on this device.
-int lm_pairs(const DeviceInfo& dev);
-// After launch_prep: gather (+ both geometries) and the logits-gradient pass.
-cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st);
-// After launch_lmhead_dz: the hidden-state and weight gradient contractions.
-cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st);
-
 }  // namespace grpo

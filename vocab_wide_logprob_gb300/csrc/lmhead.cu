@@ -28,6 +28,7 @@
 #include <mutex>
 
 #include "pair_pipeline.cuh"
+#include "lmhead.cuh"
 
 namespace grpo {
 namespace {
@@ -38,7 +39,7 @@ constexpr int kK = 64;            // k per stage: one 128-byte swizzle atom of b
 constexpr int kMaxSplits = 256;   // = kThreads: one candidate per thread
 constexpr uint32_t kIdescLm = umma_idesc(256, kVTile, false, false);
 constexpr int kLmSmem = kPairRingBytes + 1024;
-constexpr int kDzSmem = kLmSmem + 4 * 4096;  // + the epilogue's TMA-store boxes
+constexpr int kDzSmem = kLmSmem + 8 * 4096;  // + two 2 KiB TMA-store boxes per epilogue warp
 
 struct LmParams {
   int64_t N, P, C, V, d;
@@ -167,6 +168,9 @@ struct LmOp {
   static constexpr int kStages = kPairStages;
   static constexpr int kStageBytes = kPairStageBytes;
   static constexpr int kAccCols = 256;
+  // the gradient epilogue (exp, scale, round, store per element) is the heavier
+  // one: two warps per TMEM lane quarter, 128 columns each
+  static constexpr int kEpiWarps = kMode == 1 ? 8 : 4;
   const LmParams& p;
   const CUtensorMap* map_h;
   const CUtensorMap* map_w;
@@ -241,12 +245,13 @@ struct LmOp {
     has = false;
   }
 
-  __device__ void epi_tile(int64_t it, int t, uint32_t tbase, bool) {
+  __device__ void epi_tile(int64_t it, int t, uint32_t tbase, bool, int slice) {
     const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
     const int64_t vbase = (first_tile(it) + t) * kVTile;
+    constexpr int kCols = kVTile * 4 / kEpiWarps;  // this warp's columns of the tile
 #pragma unroll 1
-    for (int c = 0; c < kVTile; c += 32) {
+    for (int c = slice * kCols; c < (slice + 1) * kCols; c += 32) {
       float v[32];
       tmem_ld32(tbase + (uint32_t)c, v);
       const int64_t v0 = vbase + c;
@@ -364,7 +369,7 @@ __device__ __forceinline__ void lm_kernel_body(const CUtensorMap* map_h, const C
   const uint32_t ring = smem_u32(lm_smem + ((1024 - (smem_u32(lm_smem) & 1023)) & 1023));
   LmOp<kMode> op{p, map_h, map_w, map_dz, ids};
   op.rank = cluster_rank();
-  op.stg = ring + kPairRingBytes + (uint32_t)((threadIdx.x >> 5) & 3) * 4096u;
+  op.stg = ring + kPairRingBytes + (uint32_t)((threadIdx.x >> 5) - 2) * 4096u;  // epilogue warps
   pair_pipeline(op, ring, p.hdr);
 }
 
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   lm_kernel_body<0>(&map_h, &map_w, nullptr, ids, p);
 }
 
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(64 + 32 * LmOp<1>::kEpiWarps, 1)
     lmhead_dz_kernel(const __grid_constant__ CUtensorMap map_h,
                      const __grid_constant__ CUtensorMap map_w,
                      const __grid_constant__ CUtensorMap map_dz, const int64_t* __restrict__ ids,
@@ -607,8 +612,9 @@ cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStre
   if ((e = encode_dz_slabs(&map_dz, dz, bl.rows_cap, bl.ldz, 32, true)) != cudaSuccess) return e;
   static bool attr_done = false;
   if ((e = set_smem((const void*)lmhead_dz_kernel, kDzSmem, &attr_done)) != cudaSuccess) return e;
-  return launch_pdl(lmhead_dz_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
-                    (size_t)kDzSmem, st, 2, map_h, map_w, map_dz, a.ids, p);
+  return launch_pdl(lmhead_dz_kernel, dim3((unsigned)(2 * pairs)),
+                    dim3(64 + 32 * LmOp<1>::kEpiWarps), (size_t)kDzSmem, st, 2, map_h, map_w,
+                    map_dz, a.ids, p);
 }
 
 }  // namespace grpo

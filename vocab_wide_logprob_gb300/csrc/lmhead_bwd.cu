@@ -27,6 +27,7 @@
 // d must be a multiple of 128: each CTA of a pair holds half of every MMA's
 // N columns (256 or 128) as whole 64-column MN-major atoms.
 #include "pair_pipeline.cuh"
+#include "lmhead.cuh"
 
 namespace grpo {
 namespace {
@@ -36,7 +37,6 @@ constexpr int kGK = 64;                    // k per stage
 constexpr int kGABytes = 128 * kGK * 2;    // this CTA's A: 16 KiB
 constexpr uint32_t kMnAtomStride = 8192;   // 64 M/N elements x 64 K rows x 2 bytes (one TMA box)
 constexpr int kEpiBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA-store box
-constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;
 constexpr int kDhN = 512;                  // dhidden: d columns per item (two MMAs of <= 256)
 constexpr int64_t kDhTileFloats = (int64_t)kRows * kDhN;
 
@@ -48,13 +48,14 @@ struct GradParams {
   WsHeader* hdr;
 };
 
-// Drains `nw` accumulator columns of this warp's 32 TMEM lanes through two
-// 32 x 32 fp32 boxes (128-byte swizzle) into TMA stores at (x0 + c, y).
+// Drains accumulator columns [c0, c1) of this warp's 32 TMEM lanes through
+// kBoxes 32 x 32 fp32 boxes (128-byte swizzle) into TMA stores at (x0 + c, y).
+template <int kBoxes>
 __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t stg,
-                                           uint32_t& chunk, uint32_t tbase, int nw, bool empty,
-                                           int x0, int y) {
+                                           uint32_t& chunk, uint32_t tbase, int c0, int c1,
+                                           bool empty, int x0, int y) {
   const int lane = threadIdx.x & 31;
-  for (int c = 0; c < nw; c += 32) {
+  for (int c = c0; c < c1; c += 32) {
     float v[32];
     if (!empty) {
       tmem_ld32(tbase + (uint32_t)c, v);
@@ -63,8 +64,8 @@ __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t 
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
     }
     // row `lane` of the box; 16-byte chunk q sits at q ^ (lane & 7)
-    const uint32_t box = stg + (chunk & 1u) * (uint32_t)kEpiBoxBytes;
-    if (lane == 0) bulk_wait_read<1>();  // the store that last used this box has read it
+    const uint32_t box = stg + (chunk % kBoxes) * (uint32_t)kEpiBoxBytes;
+    if (lane == 0) bulk_wait_read<kBoxes - 1>();  // the store that last used this box has read it
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -92,6 +93,8 @@ struct DhOp {
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = kGABytes + 2 * 16384;  // A + up to 256 B columns
   static constexpr int kAccCols = 512;
+  static constexpr int kEpiWarps = 4;  // the epilogue runs once per long item
+  static constexpr int kBoxes = 2;
   const GradParams& p;
   const CUtensorMap* map_a;
   const CUtensorMap* map_b;
@@ -152,11 +155,11 @@ struct DhOp {
     }
   }
   __device__ void epi_begin(int64_t) {}
-  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty) {
+  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty, int) {
     // partial tile `it`: rows it*256 .. of an [items*256, 512] matrix
     const int quarter = (threadIdx.x >> 5) & 3;
-    drain_fp32(map_out, stg, chunk, tbase, width(it), empty, 0,
-               (int)(it * kRows + rank * 128 + quarter * 32));
+    drain_fp32<kBoxes>(map_out, stg, chunk, tbase, 0, width(it), empty, 0,
+                       (int)(it * kRows + rank * 128 + quarter * 32));
   }
   __device__ void epi_end(int64_t) {}
   __device__ void epi_finish() {
@@ -175,6 +178,10 @@ struct DwOp {
   static constexpr int kStages = kN == 512 ? 4 : kPairStages;
   static constexpr int kStageBytes = kGABytes + (kN / 2) * kGK * 2;
   static constexpr int kAccCols = kN;
+  // the epilogue (kN fp32 columns per row per item) is as long as a good part
+  // of the item's MMAs: two warps per TMEM lane quarter drain half each
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kBoxes = 1;
   const GradParams& p;
   const CUtensorMap* map_a;
   const CUtensorMap* map_b;
@@ -232,11 +239,12 @@ struct DwOp {
     }
   }
   __device__ void epi_begin(int64_t) {}
-  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty) {
+  __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty, int slice) {
     // dweight [V, d] at (vocabulary row, d column); rows past V are not stored
     const int quarter = (threadIdx.x >> 5) & 3;
-    drain_fp32(map_out, stg, chunk, tbase, width(it), empty, (int)(n_tile(it) * kN),
-               (int)(m_tile(it) * kRows + rank * 128 + quarter * 32));
+    const int half = width(it) / 2;
+    drain_fp32<kBoxes>(map_out, stg, chunk, tbase, slice * half, (slice + 1) * half, empty,
+                       (int)(n_tile(it) * kN), (int)(m_tile(it) * kRows + rank * 128 + quarter * 32));
   }
   __device__ void epi_end(int64_t) {}
   __device__ void epi_finish() {
@@ -247,7 +255,7 @@ struct DwOp {
 constexpr int kDwN = 512;  // dweight: d columns per item (measured faster than 256)
 
 template <class Op>
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(64 + 32 * Op::kEpiWarps, 1)
     lmhead_grad_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_out, const GradParams p) {
@@ -255,8 +263,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t ring = smem_u32(g_smem + ((1024 - (smem_u32(g_smem) & 1023)) & 1023));
   Op op{p, &map_a, &map_b, &map_out};
   op.rank = cluster_rank();
-  op.stg = ring + Op::kStages * Op::kStageBytes +
-           (uint32_t)((threadIdx.x >> 5) & 3) * 2u * kEpiBoxBytes;
+  op.stg = ring + Op::kStages * Op::kStageBytes +  // this epilogue warp's boxes
+           (uint32_t)((threadIdx.x >> 5) - 2) * Op::kBoxes * kEpiBoxBytes;
   pair_pipeline(op, ring, p.hdr);
 }
 
@@ -308,7 +316,8 @@ __global__ void __launch_bounds__(kReduceThreads)
 template <class Op>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
                         const GradParams& p, const DeviceInfo& dev, cudaStream_t st) {
-  constexpr int smem = Op::kStages * Op::kStageBytes + kEpiBytes + 1024;
+  constexpr int smem = Op::kStages * Op::kStageBytes + Op::kEpiWarps * Op::kBoxes * kEpiBoxBytes +
+                       1024;
   static bool attr_done = false;
   cudaError_t e;
   if (!attr_done) {
@@ -319,7 +328,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
     attr_done = true;
   }
   return launch_pdl(lmhead_grad_gemm_kernel<Op>, dim3((unsigned)(2 * lm_pairs(dev))),
-                    dim3(kPairThreads), (size_t)smem, st, 2, a, b, out, p);
+                    dim3(64 + 32 * Op::kEpiWarps), (size_t)smem, st, 2, a, b, out, p);
 }
 
 }  // namespace

@@ -14,10 +14,11 @@
 //                      accumulators (or one of up to 512 columns); commits
 //                      free the stage (`empty`) and publish the tile
 //                      (`acc_full`) in both CTAs at once.
-//   warps 2-5          epilogue: each reads this CTA's 128 TMEM lanes of the
-//                      finished tile (warp w owns lanes 32 (w % 4) ..) and
-//                      hands the accumulator back (`acc_empty` on the leader,
-//                      8 arrivals: 4 warps x 2 CTAs).
+//   warps 2 ..         epilogue (Op::kEpiWarps = 4 or 8): each reads this CTA's
+//                      TMEM lanes 32 (w % 4) .. + 31 of the finished tile (with
+//                      8 warps, half of its columns each) and hands the
+//                      accumulator back (`acc_empty` on the leader, one
+//                      arrival per epilogue warp of both CTAs).
 // Per CTA, A and B stage operands sit at the same shared-memory offsets, which
 // is how the leader's descriptors address both CTAs' halves.  Every wait is
 // bounded (one second); a timeout sets kFlagTimeout in the workspace header
@@ -31,7 +32,7 @@
 
 namespace grpo {
 
-constexpr int kPairThreads = 192;
+constexpr int kPairThreads = 192;  // with 4 epilogue warps
 constexpr int kPairStages = 6;          // the default ring: 6 stages of 32 KiB
 constexpr int kPairStageBytes = 32768;  // A 16 KiB + B half <= 16 KiB per CTA
 constexpr int kPairBOffset = 16384;     // B half inside a stage
@@ -40,6 +41,8 @@ constexpr int kPairRingBytes = kPairStages * kPairStageBytes;
 // Op:
 //   static constexpr int kStages, kStageBytes   the ring (kStages * kStageBytes <= the
 //                                               dynamic shared memory before `ring` + ...)
+//   static constexpr int kEpiWarps              4 or 8 epilogue warps (kernel threads:
+//                                               64 + 32 * kEpiWarps)
 //   static constexpr int kAccCols               256: two accumulators, the epilogue of one
 //                                               tile overlaps the MMAs of the next; 512:
 //                                               one accumulator of up to 512 columns
@@ -50,13 +53,14 @@ constexpr int kPairRingBytes = kPairStages * kPairStageBytes;
 //             uint32_t mbar_cluster) const;             this CTA's TMA loads
 //   void mma(uint32_t dacc, uint32_t sa, int64_t it, int t, bool first) const;  4 MMAs
 //   void epi_begin(int64_t it); void epi_tile(int64_t it, int t, uint32_t tmem_lane_base,
-//                  bool empty); void epi_end(int64_t it); void epi_finish();
+//                  bool empty, int slice); void epi_end(int64_t it); void epi_finish();
 template <class Op>
 __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* hdr) {
   constexpr int kStages = Op::kStages;
   constexpr uint32_t kStageBytes = Op::kStageBytes;
   constexpr int kBufs = Op::kAccCols == 512 ? 1 : 2;
   constexpr uint32_t kAccCols = Op::kAccCols;
+  constexpr int kEpi = Op::kEpiWarps;  // 4 or 8: one or two warps per TMEM lane quarter
   __shared__ __align__(8) uint64_t s_full[kStages];
   __shared__ __align__(8) uint64_t s_empty[kStages];
   __shared__ __align__(8) uint64_t s_acc_full[2];
@@ -76,7 +80,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(smem_u32(&s_acc_full[k]), 1);   // the leader's multicast commit
-      mbar_init(smem_u32(&s_acc_empty[k]), 8);  // leader: 4 epilogue warps x 2 CTAs
+      mbar_init(smem_u32(&s_acc_empty[k]), 2 * kEpi);  // leader: the epilogue warps of 2 CTAs
     }
     mbar_init_fence();
   }
@@ -160,8 +164,9 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
         }
       }
     }
-  } else {  // ---------------- epilogue: warps 2..5 of both CTAs ------------------
-    const int quarter = warp & 3;
+  } else {  // ---------------- epilogue: warps 2 .. 2 + kEpi - 1 of both CTAs -----
+    const int quarter = warp & 3;  // TMEM lanes 32 * quarter .. + 31
+    const int slice = (warp - 2) >> 2;  // with 8 warps: which half of the columns
     int buf = 0;
     uint32_t aphase = 0;
     const uint32_t acc_empty_leader0 = map_to_rank(smem_u32(&s_acc_empty[0]), 0);
@@ -180,7 +185,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
         int64_t k0, k1;
         op.krange(it, t, &k0, &k1);
         op.epi_tile(it, t, tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)buf * kAccCols,
-                    k1 <= k0);
+                    k1 <= k0, slice);
         tmem_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
