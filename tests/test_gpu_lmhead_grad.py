@@ -12,9 +12,10 @@ Tolerances, fixed from the arithmetic before looking at results:
   (the rest covers float32 accumulation over up to V terms), requires exact
   zeros where the magnitude is 0, and bounds the relative Frobenius error of
   the whole sampled block by 1e-2.
-Inputs whose oracle ratio lies within 1e-5 of a clip boundary would let the
-two sides take different branches of min(); the seeds used here have none,
-and the test asserts it."""
+Inputs whose oracle ratio lies near a clip boundary would let the two sides
+take different branches of min() (and a dweight row sums over every token);
+the old log-probs of such tokens are moved 2e-3 away on the host, for both
+sides, before anything runs."""
 import numpy as np
 import pytest
 import torch
@@ -56,6 +57,11 @@ def _setup(w, d, device_gen=False):
     A_o = oracle.advantage(R, w.G)
     lp_o, lse_o = oracle.lmhead_logp(Hn, Wn, w.P, w.C, ids, len_o)
     old, ref = H.host_inputs(w, lp_o, m_o)
+    if old is not None:  # keep every ratio 1e-3 (log space) away from the clip boundaries
+        kinks = np.array([-np.log1p(w.eps), -np.log1p(-w.eps)])
+        with np.errstate(invalid="ignore"):
+            dist = np.min(np.abs((old.astype(np.float64) - lp_o)[..., None] - kinks), axis=-1)
+            old[dist < 1e-3] += np.float32(2e-3)
     assert not H.kink_tokens(lp_o, old, w.eps).any()
     nrm = float(w.N * w.C)
     loss_o, w_o, ell_o = oracle.loss(lp_o, None if old is None else old.astype(np.float64),
@@ -175,3 +181,38 @@ def test_lmhead_grads_full_size_default_workload():
         scored[i, w.P - 1:w.P - 1 + L[i]] = True
     assert not dh_h[~scored].any()
     assert np.isfinite(dh_h).all() and torch.isfinite(dw).all()
+
+
+def test_lmhead_grads_sampled_kl_workload():
+    """The k3-KL workload's shapes (B=1, G=16, P=256, C=512, V = 151,936,
+    about 6,000 scored rows: 24 row blocks, many vocabulary splits of dhidden,
+    95 k-steps per dweight item) with hidden size 896: the forward against the
+    oracle on every token; sampled dhidden rows and dweight rows (targets of
+    scored tokens among them) element by element."""
+    n = H.g()
+    w = H.with_contrast(wl.QWEN_G16_KL)
+    hidden, weight, t_ids, lens, out, h = _setup(w, 896, device_gen=True)
+    _check_fwd(w, out, h)
+    two = torch.tensor([2.0], dtype=torch.float32, device="cuda")
+    dh, dw, ws = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                                        two)
+    assert n.grpo_check_error(ws) == 0
+    rng = np.random.default_rng(11)
+    L = h["len"]
+    rows = []
+    for _ in range(20):
+        i = int(rng.integers(0, w.N))
+        rows.append((i, int(rng.integers(0, L[i]))))
+    rows += [(w.N - 1, int(L[-1]) - 1)]
+    targets = [int(h["ids"][i, w.P + t]) for i, t in rows[:12]]
+    vocab = sorted(set(targets) | set(rng.integers(0, w.V, 20).tolist()) | {w.V - 1})
+    gr = oracle.lmhead_grads(h["Hn"], h["Wn"], w.P, w.C, h["ids"], L, h["lse"], h["w"], 2.0,
+                             rows=rows, vocab=vocab, magnitudes=True)
+    dh_h = dh.cpu().numpy()
+    got = np.stack([dh_h[i, w.P - 1 + t] for i, t in rows])
+    assert_grad(got, gr["dhidden"], gr["dhidden_mag"], "dhidden rows")
+    assert_grad(dw.cpu().numpy()[vocab], gr["dweight"], gr["dweight_mag"], "dweight rows")
+    scored = np.zeros((w.N, w.T), bool)
+    for i in range(w.N):
+        scored[i, w.P - 1:w.P - 1 + L[i]] = True
+    assert not dh_h[~scored].any()
