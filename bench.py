@@ -12,8 +12,10 @@ Prints ONE JSON line (rank 0):
   roofline     the dominant kernel (dlogits_kernel, one launch per step):
                algorithmic bytes / its CUDA-event duration vs measured HBM peak
   e2e          the same metric through the public API with host buffers:
-               pinned host -> device copies of the step's inputs and a
-               device -> host read of the loss inside the timed region
+               the logits in pinned host memory (grpo_loss_fwd_bwd_host moves
+               only the scored rows to the device), host -> device copies of
+               the other inputs and a device -> host read of the loss, all
+               inside the timed region
   cpu_baseline the float64 CPU oracle, timed on a bounded sample
 ``--impl reference`` times the oracle alone (host cores) as the reference arm.
 """
@@ -470,26 +472,34 @@ def run_ours(args, w0: wl.Workload):
     t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in events) / 1e3
     loss_val = float(out["loss"].item())
 
-    # end to end through the public API: host inputs in, loss out
+    # end to end through the public API: host inputs in, loss out.  The logits
+    # stay in pinned host memory and grpo_loss_fwd_bwd_host moves only the
+    # scored rows across the host link (into the device logits buffer, which
+    # serves as its staging buffer); ids, rewards and old/ref log-probs are
+    # copied in whole; the loss comes back.
     h_logits = logits.cpu().pin_memory()
     h_ids = ids.cpu().pin_memory()
     h_R = R.cpu().pin_memory()
     h_old = None if old is None else old.cpu().pin_memory()
     h_ref = None if ref is None else ref.cpu().pin_memory()
     h_loss = torch.empty((1,), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_ids, h_R, h_old, h_ref)
-              if t is not None)
+    h2d = t_valid * w.V * logits.element_size() + sum(
+        t.numel() * t.element_size() for t in (h_ids, h_R, h_old, h_ref) if t is not None)
+    e2e_out = {}
 
     def e2e_step():
-        logits.copy_(h_logits, non_blocking=True)
         ids.copy_(h_ids, non_blocking=True)
         R.copy_(h_R, non_blocking=True)
         if old is not None:
             old.copy_(h_old, non_blocking=True)
         if ref is not None:
             ref.copy_(h_ref, non_blocking=True)
-        step()
-        h_loss.copy_(out["loss"], non_blocking=True)
+        m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
+        a = g.grpo_advantage(R, w.G, adv)
+        e2e_out["o"] = g.grpo_loss_fwd_bwd_host(h_logits, w.P, ids, ln, a, old, ref, w.eps,
+                                                w.beta, 0.0, None, e2e_out.get("o"), ws,
+                                                dlogits, staging=logits)
+        h_loss.copy_(e2e_out["o"]["loss"], non_blocking=True)
         stream.synchronize()
 
     for _ in range(2):
@@ -564,7 +574,9 @@ def run_ours(args, w0: wl.Workload):
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": kbytes},
             "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                    "path": "grpo_mask + grpo_advantage + grpo_loss_fwd_bwd_host (logits in "
+                            "pinned host memory; only the scored rows cross the link)"},
             "copy_ceiling_gbs": copy_gbs,
             "other_path": None if alt is None else dict(
                 alt, logits_roofline_frac=alt["logits_gbs"] / peak),

@@ -283,6 +283,30 @@ grpo_status grpo_loss_fwd_bwd(const void *logits, grpo_dtype dtype, int64_t N, i
                               float *logp, float *lse, float *w, float *loss, void *dlogits,
                               void *workspace, size_t workspace_bytes, grpo_stream_t stream);
 
+/*
+ * grpo_loss_fwd_bwd_host -- grpo_loss_fwd_bwd for logits that sit in
+ * page-locked host memory (cudaHostAlloc, or cudaHostRegister, mapped into the
+ * device's address space).  The loss reads only the scored rows, row P-1+t of
+ * sequence i for t < len_i ("compute_logprobs" and the completion mask), so
+ * only those rows cross the host link: a kernel copies them through the
+ * buffer's device mapping into the same rows of `staging`, device memory of
+ * the logits' shape [N, P+C, V] (its other rows are neither read nor written),
+ * and grpo_loss_fwd_bwd then runs on `staging`.
+ *
+ * Arguments: those of grpo_loss_fwd_bwd with host_logits for logits, plus
+ * staging (device, logits' size, element-aligned, not overlapping dlogits).
+ * The other pointers are device memory as for grpo_loss_fwd_bwd.  Returns
+ * GRPO_ERR_INVALID_ARG when host_logits is not page-locked host memory the
+ * device can address.
+ */
+grpo_status grpo_loss_fwd_bwd_host(const void *host_logits, grpo_dtype dtype, int64_t N,
+                                   int64_t P, int64_t C, int64_t V, const int64_t *input_ids,
+                                   const int32_t *len, const float *adv, const float *old_logp,
+                                   const float *ref_logp, float eps, float beta, float norm,
+                                   const float *grad_loss, float *logp, float *lse, float *w,
+                                   float *loss, void *dlogits, void *staging, void *workspace,
+                                   size_t workspace_bytes, grpo_stream_t stream);
+
 /* grpo_loss_fwd_bwd with the aggregation choice of grpo_loss_fwd_ex. */
 grpo_status grpo_loss_fwd_bwd_ex(const void *logits, grpo_dtype dtype, int64_t N, int64_t P,
                                  int64_t C, int64_t V, const int64_t *input_ids,

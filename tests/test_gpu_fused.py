@@ -118,3 +118,59 @@ def test_fused_full_size_same_bits(w):
     assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
     del logits, da, b
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 1024), ("bf16", 1001), ("f32", 1001)],
+                         ids=["bf16_vec16", "bf16_odd_V", "f32_odd_V"])
+def test_host_logits_match_device_path(dtype, V):
+    """grpo_loss_fwd_bwd_host on pinned host logits gives the bits of
+    grpo_loss_fwd_bwd on the same logits in device memory (16-byte, 4-byte and
+    2-byte copy units), and only the scored rows of the staging buffer are
+    written."""
+    n = H.g()
+    w = H.with_contrast(wl.variant(wl.QWEN_G8, name=f"host_{dtype}_{V}", B=2, G=4, P=6, C=20,
+                                   V=V, eos_id=V - 1, dtype=dtype, seed=91))
+    ids = wl.make_ids(w)
+    R = wl.make_rewards(w)
+    logits = wl.make_logits_cpu(w)
+    t_ids = H.dev(ids)
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(R), w.G)
+    rng = np.random.default_rng(4)
+    old = torch.from_numpy(rng.normal(-7, 1, (w.N, w.C)).astype(np.float32)).cuda()
+    a = n.grpo_loss_fwd_bwd(logits.cuda(), w.P, t_ids, lens, adv, old, None, 0.2, 0.0)
+    staging = torch.full(logits.shape, 7.0, dtype=logits.dtype, device="cuda")
+    b = n.grpo_loss_fwd_bwd_host(logits.pin_memory(), w.P, t_ids, lens, adv, old, None, 0.2, 0.0,
+                                 staging=staging)
+    assert n.grpo_check_error(b["workspace"]) == 0
+    for k in ("logp", "lse", "w", "loss"):
+        assert torch.equal(a[k], b[k]), k
+    assert torch.equal(a["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32),
+                       b["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32))
+    L = lens.cpu().numpy()
+    scored = np.zeros((w.N, w.T), bool)
+    for i in range(w.N):
+        scored[i, w.P - 1:w.P - 1 + L[i]] = True
+    st = staging.float().cpu().numpy()
+    assert np.array_equal(st[scored], logits.float().numpy()[scored])
+    assert np.all(st[~scored] == 7.0)
+
+
+def test_host_logits_refuses_pageable_memory():
+    """Pageable host memory is not addressable by the device: refused before
+    any launch."""
+    import ctypes
+    n = H.g()
+    lib = n.library()
+    buf = np.zeros((2, 8, 64), np.float32)
+    dev = torch.zeros((64,), dtype=torch.uint8, device="cuda")
+    dl = torch.zeros((2, 8, 64), dtype=torch.float32, device="cuda")
+    st = torch.zeros((2, 8, 64), dtype=torch.float32, device="cuda")
+    ws = torch.zeros((1 << 16,), dtype=torch.uint8, device="cuda")
+    p = ctypes.c_void_p
+    rc = lib.grpo_loss_fwd_bwd_host(p(buf.ctypes.data), 0, 2, 4, 4, 64, p(dev.data_ptr()),
+                                    p(dev.data_ptr()), p(dev.data_ptr()), None, None, 0.2, 0.0, 0.0,
+                                    None, p(dev.data_ptr()), p(dev.data_ptr()),
+                                    p(dev.data_ptr()), p(dev.data_ptr()), p(dl.data_ptr()),
+                                    p(st.data_ptr()), p(ws.data_ptr()), ws.numel(), None)
+    assert rc == 1  # GRPO_ERR_INVALID_ARG

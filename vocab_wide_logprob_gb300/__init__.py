@@ -9,7 +9,8 @@ generators stay usable on machines without the built library.
 
 _NAMES = ("grpo_mask", "grpo_advantage", "grpo_advantage_ex", "grpo_workspace_size",
           "grpo_loss_fwd", "grpo_loss_fwd_ex", "grpo_logprobs", "grpo_loss_bwd",
-          "grpo_loss_bwd_ex", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_ex", "grpo_loss_fwd_static",
+          "grpo_loss_bwd_ex", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_ex", "grpo_loss_fwd_bwd_host",
+          "grpo_loss_fwd_static",
           "grpo_lmhead_logprobs", "grpo_lmhead_loss_fwd", "grpo_lmhead_loss_bwd",
           "grpo_check_error", "grpo_copy", "GrpoError")
 

@@ -57,6 +57,8 @@ def _load():
                                   P], INT),
         "grpo_loss_fwd_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P, P,
                                P, P, SZ, P], INT),
+        "grpo_loss_fwd_bwd_host": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
+                                    P, P, P, P, SZ, P], INT),
         "grpo_advantage_ex": ([P, I64, I64, INT, F, P, P, P], INT),
         "grpo_loss_fwd_ex": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P, P, P, P,
                               P, SZ, P], INT),
@@ -329,6 +331,48 @@ def grpo_loss_fwd_bwd(logits, P, input_ids, lens, adv, old_logp=None, ref_logp=N
         _check(_lib.grpo_loss_fwd_bwd(*head, *tail), "grpo_loss_fwd_bwd")
     else:
         _check(_lib.grpo_loss_fwd_bwd_ex(*head, int(agg), *tail), "grpo_loss_fwd_bwd_ex")
+    return out
+
+
+def grpo_loss_fwd_bwd_host(host_logits, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
+                           eps=0.2, beta=0.0, norm=0.0, grad_loss=None, out=None, workspace=None,
+                           dlogits=None, staging=None, stream=None):
+    """:func:`grpo_loss_fwd_bwd` for logits in page-locked host memory
+    (``host_logits`` a pinned CPU tensor): only the scored rows cross the
+    host link, into the same rows of ``staging`` (a device tensor of the
+    logits' shape, allocated when None).  Returns the dict of
+    :func:`grpo_loss_fwd_bwd` plus ``staging``."""
+    if host_logits.is_cuda or not host_logits.is_pinned() or not host_logits.is_contiguous():
+        raise ValueError("host_logits must be a contiguous pinned CPU tensor")
+    N, T, V = host_logits.shape
+    C = T - P
+    for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
+                        ("adv", adv, torch.float32), ("old_logp", old_logp, torch.float32),
+                        ("ref_logp", ref_logp, torch.float32),
+                        ("grad_loss", grad_loss, torch.float32)):
+        _dev(t, name, dt)
+    dev = input_ids.device
+    if out is None:
+        out = {"logp": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "lse": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "w": torch.empty((N, C), dtype=torch.float32, device=dev),
+               "loss": torch.empty((1,), dtype=torch.float32, device=dev)}
+    need = grpo_workspace_size(N, C, V)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if dlogits is None:
+        dlogits = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
+    if staging is None:
+        staging = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
+    _dev(dlogits, "dlogits", host_logits.dtype)
+    _dev(staging, "staging", host_logits.dtype)
+    out.update(workspace=workspace, dlogits=dlogits, staging=staging)
+    _check(_lib.grpo_loss_fwd_bwd_host(
+        _ptr(host_logits), _dtype_code(host_logits), N, P, C, V, _ptr(input_ids), _ptr(lens),
+        _ptr(adv), _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm),
+        _ptr(grad_loss), _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]),
+        _ptr(dlogits), _ptr(staging), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "grpo_loss_fwd_bwd_host")
     return out
 
 

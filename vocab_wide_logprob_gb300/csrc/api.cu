@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "lmhead.cuh"
+#include "host_rows.cuh"
 #include "grpo.h"
 
 namespace grpo {
@@ -375,6 +376,55 @@ grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (launch_zero_rows(b, d, st, logp, lse, w) != cudaSuccess) return GRPO_ERR_CUDA;
   return from_cuda(launch_lse_grad(a, b, d, st));
+}
+
+grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, int64_t N,
+                                   int64_t P, int64_t C, int64_t V, const int64_t* input_ids,
+                                   const int32_t* len, const float* adv, const float* old_logp,
+                                   const float* ref_logp, float eps, float beta, float norm,
+                                   const float* grad_loss, float* logp, float* lse, float* w,
+                                   float* loss, void* dlogits, void* staging, void* workspace,
+                                   size_t workspace_bytes, grpo_stream_t stream) {
+  grpo_status s = check_shapes(dtype, N, P, C, V);
+  if (s != GRPO_OK) return s;
+  if (N == 0 || C == 0)
+    return grpo_loss_fwd_bwd(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp,
+                             eps, beta, norm, grad_loss, logp, lse, w, loss, dlogits, workspace,
+                             workspace_bytes, stream);
+  if (host_logits == nullptr || staging == nullptr || len == nullptr || workspace == nullptr)
+    return GRPO_ERR_INVALID_ARG;
+  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
+  if (!aligned(host_logits, esize) || !aligned(staging, esize) || !aligned(len, 4) ||
+      !aligned(workspace, 256))
+    return GRPO_ERR_MISALIGNED;
+  if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
+  // the logits must be page-locked host memory the device can address
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, host_logits) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GRPO_ERR_INVALID_ARG;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return GRPO_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
+  const char* sg = static_cast<const char*>(staging);
+  const char* dl = static_cast<const char*>(dlogits);
+  if (dlogits != nullptr && dl < sg + bytes && sg < dl + bytes) return GRPO_ERR_INVALID_ARG;
+  FwdArgs a = {};
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.len = len;
+  a.ws = workspace;
+  const cudaStream_t st = (cudaStream_t)stream;
+  DeviceInfo d;
+  if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  if (launch_gather_host_rows(attr.devicePointer, staging, esize, a, d, st) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  return grpo_loss_fwd_bwd(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp,
+                           eps, beta, norm, grad_loss, logp, lse, w, loss, dlogits, workspace,
+                           workspace_bytes, stream);
 }
 
 grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
