@@ -17,10 +17,11 @@
 // lmhead_grad_gemm_kernel<DhOp>   dhidden partials: items (range of
 //     vocabulary k-steps, 256 rows, up to 512 columns of d), fp32 tiles in the
 //     workspace
-// lmhead_dh_reduce_kernel         sums a row's partials in split order
-//     (deterministic) into dhidden [N, P+C, d]; rows that score nothing get 0
 // lmhead_grad_gemm_kernel<DwOp>   dweight: items (256 vocabulary rows, 512
 //     columns of d), K = every scored row, fp32 straight to dweight [V, d]
+// lmhead_dh_reduce_kernel         sums a row's partials in split order
+//     (deterministic) into dhidden [N, P+C, d]; rows that score nothing get 0;
+//     runs beside the dweight kernel
 //
 // The epilogue warps drain TMEM into 32 x 32 shared-memory boxes (128-byte
 // swizzle, two per warp) that TMA stores write out while the next box fills.
@@ -271,13 +272,16 @@ __global__ void __launch_bounds__(64 + 32 * Op::kEpiWarps, 1)
 // dhidden [N, P+C, d]: the scored row (i, P-1+t), t < len_i, is valid token
 // r = offsets[i] + t; its value is the sum of its split partials in order.
 // A CTA per output row (index arithmetic once per row), 16-byte accesses.
+// Launched after the dweight kernel (programmatic dependent launch), it runs
+// beside it: it starts once every dweight CTA has begun, which is after the
+// dhidden kernel it reads from has completed, and it waits for the dweight
+// kernel only before it exits, so the kernels after it still see both done.
 constexpr int kReduceThreads = 128;
 
 __global__ void __launch_bounds__(kReduceThreads)
     lmhead_dh_reduce_kernel(const float* __restrict__ partials, const int4* __restrict__ geometry,
                             const int32_t* __restrict__ off, const int32_t* __restrict__ lens,
                             int64_t N, int64_t P, int64_t C, int64_t d, float* __restrict__ dh) {
-  pdl_wait();
   pdl_trigger();
   const int4 g = geometry[1];
   const int64_t mb = g.x, nb = g.y;
@@ -299,10 +303,11 @@ __global__ void __launch_bounds__(kReduceThreads)
       const int k = 4 * k4, nt = k / kDhN, kk = k - nt * kDhN;
       // partial tile of split s: item (s * mb + rb) * nb + nt
       const float* src = partials + (rb * nb + nt) * kDhTileFloats + rr * kDhN + kk;
-      float4 acc = *reinterpret_cast<const float4*>(src);
+      // L2 loads (not L1): the partials were written by a kernel this one does not wait for
+      float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
 #pragma unroll 4
       for (int s = 1; s < splits; ++s) {
-        const float4 x = *reinterpret_cast<const float4*>(src + s * split_stride);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + s * split_stride));
         acc.x += x.x;
         acc.y += x.y;
         acc.z += x.z;
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(kReduceThreads)
       dst[k4] = acc;
     }
   }
+  pdl_wait();  // the dweight kernel launched before this one has completed
 }
 
 template <class Op>
@@ -364,14 +370,6 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
       cudaSuccess)
     return e;
   if ((e = launch_gemm<DhOp>(a_dh, b_dh, o_dh, p, dev, st)) != cudaSuccess) return e;
-  int64_t blocks = a.N * (a.P + a.C);  // a CTA per row
-  if (blocks > 16 * (int64_t)dev.sms) blocks = 16 * (int64_t)dev.sms;
-  if (blocks < 1) blocks = 1;
-  if ((e = launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0,
-                      st, 1,
-                      (const float*)partials, geometry, off, lens, a.N, a.P, a.C, a.d,
-                      a.dhidden)) != cudaSuccess)
-    return e;
 
   // dweight = dz^T H: A = dz (MN-major, K = scored rows), B = H (MN-major)
   if ((e = encode_dz_slabs(&a_dw, const_cast<uint16_t*>(dz), bl.rows_cap, bl.ldz, 64, false)) !=
@@ -379,7 +377,15 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
     return e;
   if ((e = encode_bf16_2d(&b_dw, dense, a.d, bl.rows_cap, a.d, kGK)) != cudaSuccess) return e;
   if ((e = encode_store_32x32(&o_dw, a.dweight, true, a.d, a.V, a.d)) != cudaSuccess) return e;
-  return launch_gemm<DwOp<kDwN>>(a_dw, b_dw, o_dw, p, dev, st);
+  if ((e = launch_gemm<DwOp<kDwN>>(a_dw, b_dw, o_dw, p, dev, st)) != cudaSuccess) return e;
+
+  // the dhidden partials, summed beside the dweight kernel
+  int64_t blocks = a.N * (a.P + a.C);  // a CTA per row
+  if (blocks > 16 * (int64_t)dev.sms) blocks = 16 * (int64_t)dev.sms;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, st,
+                    1, (const float*)partials, geometry, off, lens, a.N, a.P, a.C, a.d,
+                    a.dhidden);
 }
 
 }  // namespace grpo
