@@ -296,6 +296,50 @@ def time_oracle(w: wl.Workload, seconds: float, rows_per_call: int = 32):
                       "loss terms and dlogits in float64"}
 
 
+def time_oracle_lmhead(w: wl.Workload, d: int, seconds: float, train: bool, rows_per_call: int = 16):
+    """The float64 oracle of the LM-head paths on runs of one completion's
+    scored rows until `seconds` have passed: log-probs from hidden states (the
+    float64 projection, then the row log-softmax), with `train` also the loss
+    terms and both gradients.  The head [V, d] is widened to float64 once,
+    outside the timed region."""
+    import torch
+    import oracle
+    o = oracle.default()
+    hidden = wl.make_hidden(w, d, "cpu")
+    weight = wl.make_lm_head(w, d, "cpu")
+    Hn = hidden.view(torch.int16).numpy().view(np.uint16)
+    W = (weight.view(torch.int16).numpy().view(np.uint16).astype(np.uint32) << 16).view(
+        np.float32).astype(np.float64)
+    ids = wl.make_ids(w)
+    _, lens = o.mask(ids, w.P, w.C, w.eos_id)
+    i0 = int(np.argmax(lens))
+    k = min(rows_per_call, int(lens[i0]))
+    rng = np.random.default_rng(0)
+    tokens, calls, t0 = 0, 0, None
+    while True:
+        t = int(rng.integers(0, int(lens[i0]) - k + 1))
+        hs = Hn[i0:i0 + 1, w.P - 1 + t:w.P + t + k]   # rows scoring tokens t .. t+k-1, plus one
+        ids_s = ids[i0:i0 + 1, w.P - 1 + t:w.P + t + k]
+        ln = np.array([k], np.int32)
+        lp, lse = o.lmhead_logp(hs, W, 1, k, ids_s, ln)
+        if train:
+            _, wt, _ = o.loss(lp, lp - 0.01, None, np.array([0.5]), ln, w.eps, 0.0, float(w.N * w.C))
+            o.lmhead_grads(hs, W, 1, k, ids_s, ln, lse, wt)
+        if t0 is None:  # the first call warms the libraries
+            t0 = time.perf_counter()
+            continue
+        tokens += k
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    what = ("log-probs, loss terms, dhidden and dweight" if train else "log-probs")
+    return {"value": tokens / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{calls} runs of {k} scored rows of {w.name} with hidden size {d} "
+                      f"({tokens} tokens, {el:.1f} s): {what} in float64 (numpy matmuls on "
+                      f"all cores)"}
+
+
 # --------------------------------------------------------------------------
 # the reference arm: the oracle alone
 # --------------------------------------------------------------------------
@@ -694,6 +738,8 @@ def run_lmhead(args, w: wl.Workload):
                      "traffic": recorded_traffic("lmhead_fwd_bwd" if train else
                                                  "lmhead_lse_kernel", w, d)},
         "gpu_launches": (13 if train else 5) * args.steps, "clocks": clocks,
+        "cpu_baseline": None if args.no_cpu_baseline else
+        time_oracle_lmhead(w, d, args.cpu_seconds, train),
     }
     if train:
         line["kernel_ms"] = {"fwd": ms_fwd, "bwd": ms_bwd}
