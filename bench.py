@@ -669,7 +669,10 @@ def run_lmhead(args, w: wl.Workload):
             ref = (lp + torch.from_numpy(n_ref).float().to(dev)).contiguous()
         adv = g.grpo_advantage(R, w.G)
         fwd = g.grpo_lmhead_loss_fwd(hidden, weight, w.P, ids, lens, adv, old, ref, w.eps, w.beta)
-        dh, dw, bws = g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"])
+        bflags = 1 if args.skip_zero_weight else None
+        dh, dw, bws = g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"],
+                                             flags=bflags)
+        t_nonzero = int((fwd["w"] != 0).sum().item())
 
     def step_fwd():
         g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
@@ -683,7 +686,7 @@ def run_lmhead(args, w: wl.Workload):
     def step_bwd():
         if train:
             g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"],
-                                   out=(dh, dw), workspace=bws)
+                                   out=(dh, dw), workspace=bws, flags=bflags)
 
     def step():
         step_fwd()
@@ -715,7 +718,10 @@ def run_lmhead(args, w: wl.Workload):
     ms_fwd = timed(step_fwd) if train else ms
     ms_bwd = timed(step_bwd) if train else 0.0
     unit_flops = 2.0 * t_valid * w.V * d
-    flops = unit_flops * (4 if train else 1)
+    # the backward recomputes the projection and runs both contractions over its rows:
+    # every scored row, or with --skip-zero-weight those whose gradient weight is not 0
+    bwd_rows = (t_nonzero if args.skip_zero_weight else t_valid) if train else 0
+    flops = unit_flops + 3 * 2.0 * bwd_rows * w.V * d
     peaks = measured_peaks()
     peak = peaks.get("bf16_tflops") or 1900.0
     tflops = flops / (ms * 1e-3) / 1e12
@@ -744,7 +750,9 @@ def run_lmhead(args, w: wl.Workload):
     if train:
         line["kernel_ms"] = {"fwd": ms_fwd, "bwd": ms_bwd}
         line["fwd_tflops"] = unit_flops / (ms_fwd * 1e-3) / 1e12
-        line["bwd_tflops"] = 3 * unit_flops / (ms_bwd * 1e-3) / 1e12
+        line["bwd_tflops"] = 3 * 2.0 * bwd_rows * w.V * d / (ms_bwd * 1e-3) / 1e12
+        line["config"]["nonzero_weight_tokens"] = t_nonzero
+        line["config"]["skip_zero_weight"] = bool(args.skip_zero_weight)
     print(json.dumps(line), flush=True)
 
 

@@ -352,6 +352,15 @@ grpo_status grpo_lmhead_loss_fwd(const void *hidden, const void *weight, int64_t
                                  float *logp, float *lse, float *w, float *loss, void *workspace,
                                  size_t workspace_bytes, grpo_stream_t stream);
 
+/* grpo_lmhead_loss_fwd with the aggregation choice of grpo_loss_fwd_ex. */
+grpo_status grpo_lmhead_loss_fwd_ex(const void *hidden, const void *weight, int64_t N, int64_t P,
+                                    int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
+                                    const int32_t *len, const float *adv, const float *old_logp,
+                                    const float *ref_logp, float eps, float beta, float norm,
+                                    grpo_aggregation agg, float *logp, float *lse, float *w,
+                                    float *loss, void *workspace, size_t workspace_bytes,
+                                    grpo_stream_t stream);
+
 /*
  * grpo_lmhead_loss_bwd -- gradients of g * loss with respect to the hidden
  * states and the LM head ("loss.backward()" through "model(...).logits" =
@@ -379,6 +388,21 @@ grpo_status grpo_lmhead_loss_bwd(const void *hidden, const void *weight, int64_t
                                  const int32_t *len, const float *lse, const float *w,
                                  const float *grad_loss, float *dhidden, float *dweight,
                                  void *workspace, size_t workspace_bytes, grpo_stream_t stream);
+
+/*
+ * grpo_lmhead_loss_bwd with flags: GRPO_BWD_SKIP_ZERO_WEIGHT leaves out the
+ * scored rows whose g * w is exactly 0 (no reward contrast in the group and
+ * beta = 0: "Dr. GRPO", the analysis page's no-contrast groups), whose
+ * gradient rows are 0: their logits are not recomputed and they take no part
+ * in the two contractions; their dhidden rows are +0.  dweight is the same sum
+ * over fewer (all-zero) terms, so it agrees to float rounding.
+ */
+grpo_status grpo_lmhead_loss_bwd_ex(const void *hidden, const void *weight, int64_t N, int64_t P,
+                                    int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
+                                    const int32_t *len, const float *lse, const float *w,
+                                    const float *grad_loss, float *dhidden, float *dweight,
+                                    uint32_t flags, void *workspace, size_t workspace_bytes,
+                                    grpo_stream_t stream);
 
 /*
  * grpo_check_error -- synchronises `stream`, then reports what the kernels of

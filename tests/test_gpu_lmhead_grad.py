@@ -216,3 +216,32 @@ def test_lmhead_grads_sampled_kl_workload():
     for i in range(w.N):
         scored[i, w.P - 1:w.P - 1 + L[i]] = True
     assert not dh_h[~scored].any()
+
+
+def test_lmhead_grads_skip_zero_weight():
+    """GRPO_BWD_SKIP_ZERO_WEIGHT: two groups, one without reward contrast
+    (beta = 0, so its tokens' weights are exactly 0): the same gradients as
+    without the flag (dhidden bit for bit on the rows that carry weight, +0 on
+    the skipped ones; dweight to float rounding), both against the oracle;
+    with every weight 0 both gradients are exactly 0."""
+    n = H.g()
+    w = wl.variant(wl.QWEN_G8, name="lmg_skip", B=2, G=4, P=6, C=30, V=2000, eos_id=1999,
+                   seed=95, forced={"rewards": [1, 0, 0, 1, 0, 0, 0, 0]})
+    hidden, weight, t_ids, lens, out, h = _setup(w, 256)
+    _check_fwd(w, out, h)
+    assert np.all(h["w"][4:] == 0) and np.any(h["w"][:4] != 0)
+    a = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"])
+    b = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"], flags=1)
+    assert n.grpo_check_error(b[2]) == 0
+    gr = oracle.lmhead_grads(h["Hn"], h["Wn"], w.P, w.C, h["ids"], h["len"], h["lse"], h["w"],
+                             1.0, magnitudes=True)
+    for dh, dw in (a[:2], b[:2]):
+        assert_grad(dh.cpu().numpy(), gr["dhidden"], gr["dhidden_mag"], "dhidden")
+        assert_grad(dw.cpu().numpy(), gr["dweight"], gr["dweight_mag"], "dweight")
+    assert torch.equal(a[0][:4], b[0][:4])
+    assert not b[0][4:].any()
+    assert torch.equal(b[0][4:].view(torch.int32), torch.zeros_like(b[0][4:]).view(torch.int32))
+    zero_w = torch.zeros_like(out["w"])
+    c = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], zero_w, flags=1)
+    torch.cuda.synchronize()
+    assert not c[0].any() and not c[1].any()

@@ -71,7 +71,11 @@ def _load():
         "grpo_lmhead_logprobs": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P], INT),
         "grpo_lmhead_loss_fwd": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
                                   P, SZ, P], INT),
+        "grpo_lmhead_loss_fwd_ex": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P,
+                                     P, P, P, P, SZ, P], INT),
         "grpo_lmhead_bwd_workspace_size": ([I64, I64, I64, I64, ctypes.POINTER(SZ)], INT),
+        "grpo_lmhead_loss_bwd_ex": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P,
+                                     ctypes.c_uint32, P, SZ, P], INT),
         "grpo_lmhead_loss_bwd": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P],
                                  INT),
     }
@@ -414,7 +418,8 @@ def grpo_lmhead_logprobs(hidden, weight, P, input_ids, lens, out=None, workspace
 
 
 def grpo_lmhead_loss_fwd(hidden, weight, P, input_ids, lens, adv, old_logp=None, ref_logp=None,
-                         eps=0.2, beta=0.0, norm=0.0, out=None, workspace=None, stream=None):
+                         eps=0.2, beta=0.0, norm=0.0, out=None, workspace=None, stream=None,
+                         agg=None):
     """The Dr. GRPO loss forward from hidden states [N, P+C, d] and the LM
     head [V, d] (both bfloat16): the projection fused with the log-softmax on
     the tensor cores, then the surrogate.  Returns a dict like
@@ -440,17 +445,19 @@ def grpo_lmhead_loss_fwd(hidden, weight, P, input_ids, lens, adv, old_logp=None,
     if workspace is None or workspace.numel() < need.value:
         workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
     out["workspace"] = workspace
-    _check(_lib.grpo_lmhead_loss_fwd(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
-                                     _ptr(lens), _ptr(adv), _ptr(old_logp), _ptr(ref_logp),
-                                     float(eps), float(beta), float(norm), _ptr(out["logp"]),
-                                     _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]),
-                                     _ptr(workspace), workspace.numel(), _stream(stream)),
-           "grpo_lmhead_loss_fwd")
+    head = (_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids), _ptr(lens), _ptr(adv),
+            _ptr(old_logp), _ptr(ref_logp), float(eps), float(beta), float(norm))
+    tail = (_ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["w"]), _ptr(out["loss"]),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    if agg is None:
+        _check(_lib.grpo_lmhead_loss_fwd(*head, *tail), "grpo_lmhead_loss_fwd")
+    else:
+        _check(_lib.grpo_lmhead_loss_fwd_ex(*head, int(agg), *tail), "grpo_lmhead_loss_fwd_ex")
     return out
 
 
 def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=None, out=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, flags=None):
     """Gradients of ``grad_loss * loss`` with respect to the hidden states and
     the LM head.  Returns ``(dhidden [N, P+C, d], dweight [V, d], workspace)``,
     float32; ``out`` = (dhidden, dweight) to reuse buffers."""
@@ -472,10 +479,13 @@ def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=N
            "grpo_lmhead_bwd_workspace_size")
     if workspace is None or workspace.numel() < need.value:
         workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
-    _check(_lib.grpo_lmhead_loss_bwd(_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids),
-                                     _ptr(lens), _ptr(lse), _ptr(w), _ptr(grad_loss),
-                                     _ptr(out[0]), _ptr(out[1]), _ptr(workspace),
-                                     workspace.numel(), _stream(stream)), "grpo_lmhead_loss_bwd")
+    head = (_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids), _ptr(lens), _ptr(lse),
+            _ptr(w), _ptr(grad_loss), _ptr(out[0]), _ptr(out[1]))
+    tail = (_ptr(workspace), workspace.numel(), _stream(stream))
+    if flags is None:
+        _check(_lib.grpo_lmhead_loss_bwd(*head, *tail), "grpo_lmhead_loss_bwd")
+    else:
+        _check(_lib.grpo_lmhead_loss_bwd_ex(*head, int(flags), *tail), "grpo_lmhead_loss_bwd_ex")
     return out[0], out[1], workspace
 
 

@@ -474,9 +474,10 @@ grpo_status lmhead_check(const void* hidden, const void* weight, int64_t N, int6
 grpo_status lmhead_fwd_impl(const void* hidden, const void* weight, int64_t N, int64_t P, int64_t C,
                             int64_t V, int64_t d, const int64_t* input_ids, const int32_t* len,
                             const float* adv, const float* old_logp, const float* ref_logp,
-                            float eps, float beta, float norm, float* logp, float* lse, float* w,
-                            float* loss, void* workspace, size_t workspace_bytes,
+                            float eps, float beta, float norm, int agg, float* logp, float* lse,
+                            float* w, float* loss, void* workspace, size_t workspace_bytes,
                             grpo_stream_t stream, int mode) {
+  if (agg != GRPO_AGG_TOKEN_SUM && agg != GRPO_AGG_SEQ_MEAN) return GRPO_ERR_UNSUPPORTED;
   grpo_status s = lmhead_check(hidden, weight, N, P, C, V, d, input_ids, len, workspace);
   if (s != GRPO_OK) return s;
   if (N > 0 && C > 0 && (logp == nullptr || lse == nullptr)) return GRPO_ERR_INVALID_ARG;
@@ -508,7 +509,7 @@ grpo_status lmhead_fwd_impl(const void* hidden, const void* weight, int64_t N, i
   a.eps = eps;
   a.beta = beta;
   a.norm = norm;
-  a.agg = 0;
+  a.agg = agg;
   a.logp = logp;
   a.lse = lse;
   a.w = w;
@@ -532,8 +533,8 @@ grpo_status grpo_lmhead_logprobs(const void* hidden, const void* weight, int64_t
                                  const int32_t* len, float* logp, float* lse, void* workspace,
                                  size_t workspace_bytes, grpo_stream_t stream) {
   return lmhead_fwd_impl(hidden, weight, N, P, C, V, d, input_ids, len, nullptr, nullptr, nullptr,
-                         0.f, 0.f, 0.f, logp, lse, nullptr, nullptr, workspace, workspace_bytes,
-                         stream, 0);
+                         0.f, 0.f, 0.f, GRPO_AGG_TOKEN_SUM, logp, lse, nullptr, nullptr, workspace,
+                         workspace_bytes, stream, 0);
 }
 
 grpo_status grpo_lmhead_loss_fwd(const void* hidden, const void* weight, int64_t N, int64_t P,
@@ -543,8 +544,20 @@ grpo_status grpo_lmhead_loss_fwd(const void* hidden, const void* weight, int64_t
                                  float* logp, float* lse, float* w, float* loss, void* workspace,
                                  size_t workspace_bytes, grpo_stream_t stream) {
   return lmhead_fwd_impl(hidden, weight, N, P, C, V, d, input_ids, len, adv, old_logp, ref_logp,
-                         eps, beta, norm, logp, lse, w, loss, workspace, workspace_bytes, stream,
-                         1);
+                         eps, beta, norm, GRPO_AGG_TOKEN_SUM, logp, lse, w, loss, workspace,
+                         workspace_bytes, stream, 1);
+}
+
+grpo_status grpo_lmhead_loss_fwd_ex(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                    int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                    const int32_t* len, const float* adv, const float* old_logp,
+                                    const float* ref_logp, float eps, float beta, float norm,
+                                    grpo_aggregation agg, float* logp, float* lse, float* w,
+                                    float* loss, void* workspace, size_t workspace_bytes,
+                                    grpo_stream_t stream) {
+  return lmhead_fwd_impl(hidden, weight, N, P, C, V, d, input_ids, len, adv, old_logp, ref_logp,
+                         eps, beta, norm, (int)agg, logp, lse, w, loss, workspace, workspace_bytes,
+                         stream, 1);
 }
 
 grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
@@ -564,6 +577,17 @@ grpo_status grpo_lmhead_loss_bwd(const void* hidden, const void* weight, int64_t
                                  const int32_t* len, const float* lse, const float* w,
                                  const float* grad_loss, float* dhidden, float* dweight,
                                  void* workspace, size_t workspace_bytes, grpo_stream_t stream) {
+  return grpo_lmhead_loss_bwd_ex(hidden, weight, N, P, C, V, d, input_ids, len, lse, w, grad_loss,
+                                 dhidden, dweight, 0u, workspace, workspace_bytes, stream);
+}
+
+grpo_status grpo_lmhead_loss_bwd_ex(const void* hidden, const void* weight, int64_t N, int64_t P,
+                                    int64_t C, int64_t V, int64_t d, const int64_t* input_ids,
+                                    const int32_t* len, const float* lse, const float* w,
+                                    const float* grad_loss, float* dhidden, float* dweight,
+                                    uint32_t flags, void* workspace, size_t workspace_bytes,
+                                    grpo_stream_t stream) {
+  if (flags & ~GRPO_BWD_SKIP_ZERO_WEIGHT) return GRPO_ERR_UNSUPPORTED;
   grpo_status s = lmhead_check(hidden, weight, N, P, C, V, d, input_ids, len, workspace);
   if (s != GRPO_OK) return s;
   if (dweight == nullptr || (N > 0 && dhidden == nullptr)) return GRPO_ERR_INVALID_ARG;
@@ -604,6 +628,7 @@ grpo_status grpo_lmhead_loss_bwd(const void* hidden, const void* weight, int64_t
   a.dhidden = dhidden;
   a.dweight = dweight;
   a.ws = workspace;
+  a.skip_zero_weight = (flags & GRPO_BWD_SKIP_ZERO_WEIGHT) != 0;
   cudaError_t e = launch_lmhead_dz(a, dev, st);
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
   return from_cuda(launch_lmhead_grads(a, dev, st));

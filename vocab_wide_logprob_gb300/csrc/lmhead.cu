@@ -51,6 +51,7 @@ struct LmParams {
   const float* lse;        // [N, C] from the forward
   const float* w;          // [N, C] d loss / d logp from the forward
   const float* grad;       // upstream scalar gradient (nullable: 1)
+  const int32_t* rowmap;   // the token i*C + t of each backward row (geometry[2].x rows)
 };
 
 // Split `ksteps` steps of work for each of `units` independent tiles into
@@ -96,16 +97,13 @@ __device__ int2 choose_split_block(int32_t units, int32_t ksteps, int slots, int
 // ---- gather: dense [rows, d] copy of the scored rows' hidden states ----------
 
 // geometry[0]: the projection pass (256-row blocks, vocabulary splits, tiles
-// per split, 0).  With `grad_gemm`, geometry[1]: the hidden-state gradient
-// contraction (256-row blocks, 512-wide d tiles, vocabulary splits, 64-wide
-// k-steps per split).  `pairs`: CTA pairs of the tensor-core kernels.
+// per split, 0).  `pairs`: CTA pairs of the tensor-core kernels.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* __restrict__ hidden,
                                                                uint16_t* __restrict__ dense,
                                                                const int32_t* __restrict__ off,
                                                                int64_t N, int64_t T, int64_t P,
                                                                int64_t d, int64_t V, int pairs,
-                                                               int4* __restrict__ geometry,
-                                                               int grad_gemm) {
+                                                               int4* __restrict__ geometry) {
   pdl_wait();
   pdl_trigger();
   const int64_t tv = off[N];
@@ -114,12 +112,6 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
     const int32_t ntiles = (int32_t)((V + kVTile - 1) / kVTile);
     const int2 s = choose_split_block(mb, ntiles, pairs, 4 * pairs + 2 * mb);
     if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
-  }
-  if (grad_gemm && blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
-    const int32_t nb = (int32_t)((d + 511) / 512);
-    const int32_t ksteps = (int32_t)((V + kVTile - 1) / kVTile) * (kVTile / kK);
-    const int2 s = choose_split_block(mb * nb, ksteps, pairs, 2 * pairs + mb * nb);
-    if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
   }
   const int64_t vec_per_row = d / 8;  // 16-byte vectors
   const int64_t rows_pad = (int64_t)mb * kRows;
@@ -139,6 +131,102 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
       const int64_t t = r - off[lo];
       const uint4* src =
           reinterpret_cast<const uint4*>(hidden + ((int64_t)lo * T + P - 1 + t) * d);
+      v = ld_stream(src + c);
+    }
+    reinterpret_cast<uint4*>(dense + r * d)[c] = v;
+  }
+}
+
+// ---- backward rows ------------------------------------------------------------------
+
+// The backward's rows: the scored tokens (t < len_i) in token order, or with
+// `skip` only those whose g * w is not exactly 0 (they contribute nothing to
+// either gradient).  One CTA: each thread takes a contiguous run of tokens,
+// counts its rows, and a block-wide exclusive scan of the counts places them:
+// rowmap[row] = i * C + t, tokrow[i * C + t] = row or -1; geometry[2].x = rows.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    active_rows_kernel(const int32_t* __restrict__ lens, const float* __restrict__ w,
+                       const float* __restrict__ grad, int64_t N, int64_t C, int skip,
+                       int32_t* __restrict__ rowmap, int32_t* __restrict__ tokrow,
+                       int4* __restrict__ geometry) {
+  __shared__ int32_t s_warp[kScanThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t NC = N * C;
+  const float g = grad != nullptr ? __ldg(grad) : 1.f;
+  const int64_t per = (NC + kScanThreads - 1) / kScanThreads;
+  const int64_t k0 = min(NC, (int64_t)tid * per), k1 = min(NC, k0 + per);
+  auto active = [&](int64_t k) {
+    const int64_t i = k / C, t = k - i * C;
+    return t < lens[i] && (!skip || g * w[k] != 0.f);
+  };
+  int32_t cnt = 0;
+  for (int64_t k = k0; k < k1; ++k) cnt += active(k) ? 1 : 0;
+  // block-wide exclusive scan of cnt
+  int32_t x = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t v = s_warp[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    s_warp[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  int32_t row = x - cnt + (warp > 0 ? s_warp[warp - 1] : 0);
+  for (int64_t k = k0; k < k1; ++k) {
+    if (active(k)) {
+      rowmap[row] = (int32_t)k;
+      tokrow[k] = row++;
+    } else {
+      tokrow[k] = -1;
+    }
+  }
+  if (tid == kScanThreads - 1) geometry[2] = make_int4(row, 0, 0, 0);
+}
+
+// Dense copy of the backward rows' hidden states (zero rows up to the next
+// multiple of 256), geometry[0] for the projection pass and geometry[1] for
+// the hidden-state gradient contraction (256-row blocks, 512-wide d tiles,
+// vocabulary splits, 64-wide k-steps per split).
+__global__ void __launch_bounds__(kThreads)
+    gather_active_rows_kernel(const uint16_t* __restrict__ hidden, uint16_t* __restrict__ dense,
+                              const int32_t* __restrict__ rowmap, int64_t C, int64_t T, int64_t P,
+                              int64_t d, int64_t V, int pairs, int4* __restrict__ geometry) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t rows = geometry[2].x;
+  const int32_t mb = (int32_t)((rows + kRows - 1) / kRows);
+  if (blockIdx.x == 0) {
+    const int32_t ntiles = (int32_t)((V + kVTile - 1) / kVTile);
+    const int2 s = choose_split_block(mb, ntiles, pairs, 4 * pairs + 2 * mb);
+    if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
+  }
+  if (blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
+    const int32_t nb = (int32_t)((d + 511) / 512);
+    const int32_t ksteps = (int32_t)((V + kVTile - 1) / kVTile) * (kVTile / kK);
+    const int2 s = choose_split_block(mb * nb, ksteps, pairs, 2 * pairs + mb * nb);
+    if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
+  }
+  const int64_t vec_per_row = d / 8;  // 16-byte vectors
+  const int64_t rows_pad = (int64_t)mb * kRows;
+  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < rows_pad * vec_per_row;
+       k += (int64_t)gridDim.x * kThreads) {
+    const int64_t r = k / vec_per_row, c = k - r * vec_per_row;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) {
+      const int64_t tok = rowmap[r], i = tok / C, t = tok - i * C;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(hidden + (i * T + P - 1 + t) * d);
       v = ld_stream(src + c);
     }
     reinterpret_cast<uint4*>(dense + r * d)[c] = v;
@@ -187,7 +275,7 @@ struct LmOp {
   uint32_t chunk;
 
   __device__ void setup() {
-    tv = p.offsets[p.N];
+    tv = kMode == 1 ? (int64_t)p.geometry[2].x : (int64_t)p.offsets[p.N];  // rows of the pass
     const int4 geo = p.geometry[0];
     mb = geo.x;
     splits = geo.y;
@@ -229,12 +317,19 @@ struct LmOp {
     lse_r = 0.f;
     coef = 0.f;
     if (r < tv) {
-      const int i = completion_of(p.offsets, p.N, r);
-      const int64_t t = r - p.offsets[i];
-      y = __ldg(ids + (int64_t)i * (p.P + p.C) + p.P + t);
+      int64_t i, t;
+      if (kMode == 1) {  // the backward's rows: the row map
+        const int64_t tok = p.rowmap[r];
+        i = tok / p.C;
+        t = tok - i * p.C;
+      } else {           // every scored token, in order
+        i = completion_of(p.offsets, p.N, r);
+        t = r - p.offsets[i];
+      }
+      y = __ldg(ids + i * (p.P + p.C) + p.P + t);
       if (kMode == 1) {
-        lse_r = __ldg(p.lse + (int64_t)i * p.C + t);
-        coef = g * __ldg(p.w + (int64_t)i * p.C + t);
+        lse_r = __ldg(p.lse + i * p.C + t);
+        coef = g * __ldg(p.w + i * p.C + t);
       }
     }
     m = -INFINITY;
@@ -549,7 +644,9 @@ LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms) {
   const int64_t nb = (d + 511) / 512;  // d tiles of the hidden-state gradient
   l.items_max = 2 * pairs + mb_max * nb;
   l.geometry = base.total;
-  l.dense = align_up(base.total + 32, 1024);
+  l.rowmap = align_up(base.total + 48, 256);
+  l.tokrow = align_up(l.rowmap + sizeof(int32_t) * (size_t)(N * C), 256);
+  l.dense = align_up(l.tokrow + sizeof(int32_t) * (size_t)(N * C), 1024);
   l.dz = align_up(l.dense + (size_t)l.rows_cap * (size_t)d * 2, 1024);
   l.dh_partials = align_up(l.dz + (size_t)l.rows_cap * (size_t)l.ldz * 2, 1024);
   l.total = align_up(l.dh_partials + (size_t)l.items_max * kRows * 512 * sizeof(float), 256);
@@ -569,7 +666,7 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   int4* geometry = reinterpret_cast<int4*>(ws + ll.geometry);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(hidden), dense, off, a.N,
-                             a.P + a.C, a.P, d, a.V, pairs, geometry, 0);
+                             a.P + a.C, a.P, d, a.V, pairs, geometry);
   if (e != cudaSuccess) return e;
 
   LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, d);
@@ -594,17 +691,25 @@ cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStre
   const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms);
   char* ws = static_cast<char*>(a.ws);
   const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
+  const int32_t* lens = reinterpret_cast<const int32_t*>(ws + wl.lens);
+  int32_t* rowmap = reinterpret_cast<int32_t*>(ws + bl.rowmap);
+  int32_t* tokrow = reinterpret_cast<int32_t*>(ws + bl.tokrow);
   uint16_t* dense = reinterpret_cast<uint16_t*>(ws + bl.dense);
   int4* geometry = reinterpret_cast<int4*>(ws + bl.geometry);
   const int pairs = lm_pairs(dev);
-  cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
-                             st, 1, static_cast<const uint16_t*>(a.hidden), dense, off, a.N,
-                             a.P + a.C, a.P, a.d, a.V, pairs, geometry, 1);
+  cudaError_t e = launch_pdl(active_rows_kernel, dim3(1), dim3(kScanThreads), 0, st, 1, lens, a.w,
+                             a.grad, a.N, a.C, a.skip_zero_weight ? 1 : 0, rowmap, tokrow,
+                             geometry);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(gather_active_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0, st,
+                 1, static_cast<const uint16_t*>(a.hidden), dense, (const int32_t*)rowmap, a.C,
+                 a.P + a.C, a.P, a.d, a.V, pairs, geometry);
   if (e != cudaSuccess) return e;
   LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, a.d);
   p.lse = a.lse;
   p.w = a.w;
   p.grad = a.grad;
+  p.rowmap = rowmap;
   uint16_t* dz = reinterpret_cast<uint16_t*>(ws + bl.dz);
   CUtensorMap map_h, map_w, map_dz;
   if ((e = encode_bf16_2d(&map_h, dense, a.d, bl.rows_cap, a.d, 128)) != cudaSuccess) return e;

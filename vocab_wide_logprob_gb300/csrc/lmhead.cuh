@@ -24,7 +24,9 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
 // geometries, the dense scored hidden rows, the bf16 logits gradient of the
 // scored rows, and the split partials of the hidden-state gradient.
 struct LmBwdLayout {
-  size_t geometry;     // int4[2]: projection pass; hidden-gradient contraction
+  size_t geometry;     // int4[3]: projection pass; hidden-gradient contraction; (rows, ...)
+  size_t rowmap;       // int32 [N*C]: the token i*C + t of each backward row
+  size_t tokrow;       // int32 [N*C]: the backward row of token i*C + t, or -1
   size_t dense;        // bf16 [rows_cap, d]
   size_t dz;           // bf16 [ldz / 64][rows_cap][64] (vocabulary slabs)
   size_t dh_partials;  // fp32 [items_max][256][512]
@@ -45,6 +47,7 @@ struct LmBwdArgs {
   float* dhidden;       // fp32 [N, P+C, d]
   float* dweight;       // fp32 [V, d]
   void* ws;
+  bool skip_zero_weight;  // rows whose g * w is exactly 0 take no part (their dhidden is 0)
 };
 // CTA pairs of the tensor-core kernels on this device.
 int lm_pairs(const DeviceInfo& dev);

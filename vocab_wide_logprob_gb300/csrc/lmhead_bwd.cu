@@ -43,8 +43,8 @@ constexpr int64_t kDhTileFloats = (int64_t)kRows * kDhN;
 
 struct GradParams {
   int64_t N, V, d;
-  const int32_t* offsets;  // [N+1]: offsets[N] = scored rows
-  const int4* geometry;    // [1]: (row blocks, d tiles of 512, splits, k-steps per split)
+  const int4* geometry;    // [1]: (row blocks, d tiles of 512, splits, k-steps per split);
+                           // [2].x: the backward's rows
   int64_t ksteps_v;        // vocabulary k-steps of the hidden-state gradient (ldz / 64)
   WsHeader* hdr;
 };
@@ -193,7 +193,7 @@ struct DwOp {
 
   __device__ void setup() {
     nb = (p.d + kN - 1) / kN;
-    ksteps = (p.offsets[p.N] + kGK - 1) / kGK;  // rows past the last scored one are zero
+    ksteps = (p.geometry[2].x + kGK - 1) / kGK;  // rows past the last one are zero
     n_items = (p.V + kRows - 1) / kRows * nb;
     chunk = 0;
   }
@@ -269,8 +269,9 @@ __global__ void __launch_bounds__(64 + 32 * Op::kEpiWarps, 1)
   pair_pipeline(op, ring, p.hdr);
 }
 
-// dhidden [N, P+C, d]: the scored row (i, P-1+t), t < len_i, is valid token
-// r = offsets[i] + t; its value is the sum of its split partials in order.
+// dhidden [N, P+C, d]: row (i, P-1+t) is backward row r = tokrow[i*C + t]
+// (-1: the token is not scored, or its weight is 0 and was skipped; then the
+// row is 0); its value is the sum of its split partials in order.
 // A CTA per output row (index arithmetic once per row), 16-byte accesses.
 // Launched after the dweight kernel (programmatic dependent launch), it runs
 // beside it: it starts once every dweight CTA has begun, which is after the
@@ -280,8 +281,8 @@ constexpr int kReduceThreads = 128;
 
 __global__ void __launch_bounds__(kReduceThreads)
     lmhead_dh_reduce_kernel(const float* __restrict__ partials, const int4* __restrict__ geometry,
-                            const int32_t* __restrict__ off, const int32_t* __restrict__ lens,
-                            int64_t N, int64_t P, int64_t C, int64_t d, float* __restrict__ dh) {
+                            const int32_t* __restrict__ tokrow, int64_t N, int64_t P, int64_t C,
+                            int64_t d, float* __restrict__ dh) {
   pdl_trigger();
   const int4 g = geometry[1];
   const int64_t mb = g.x, nb = g.y;
@@ -292,12 +293,12 @@ __global__ void __launch_bounds__(kReduceThreads)
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const int64_t i = row / T, t = row - i * T - (P - 1);
     float4* dst = reinterpret_cast<float4*>(dh + row * d);
-    if (t < 0 || t >= lens[i]) {
+    const int64_t r = (t >= 0 && t < C) ? tokrow[i * C + t] : -1;
+    if (r < 0) {
       for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads)
         dst[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
       continue;
     }
-    const int64_t r = off[i] + t;
     const int64_t rb = r / kRows, rr = r - rb * kRows;
     for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads) {
       const int k = 4 * k4, nt = k / kDhN, kk = k - nt * kDhN;
@@ -340,11 +341,9 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 }  // namespace
 
 cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {
-  const WsLayout wl = ws_layout(a.N);
   const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms);
   char* ws = static_cast<char*>(a.ws);
-  const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
-  const int32_t* lens = reinterpret_cast<const int32_t*>(ws + wl.lens);
+  const int32_t* tokrow = reinterpret_cast<const int32_t*>(ws + bl.tokrow);
   const uint16_t* dz = reinterpret_cast<const uint16_t*>(ws + bl.dz);
   const uint16_t* dense = reinterpret_cast<const uint16_t*>(ws + bl.dense);
   const int4* geometry = reinterpret_cast<const int4*>(ws + bl.geometry);
@@ -354,7 +353,6 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
   p.N = a.N;
   p.V = a.V;
   p.d = a.d;
-  p.offsets = off;
   p.geometry = geometry;
   p.ksteps_v = bl.ldz / kGK;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
@@ -384,8 +382,7 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
   if (blocks > 16 * (int64_t)dev.sms) blocks = 16 * (int64_t)dev.sms;
   if (blocks < 1) blocks = 1;
   return launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, st,
-                    1, (const float*)partials, geometry, off, lens, a.N, a.P, a.C, a.d,
-                    a.dhidden);
+                    1, (const float*)partials, geometry, tokrow, a.N, a.P, a.C, a.d, a.dhidden);
 }
 
 }  // namespace grpo
