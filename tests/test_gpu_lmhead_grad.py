@@ -245,3 +245,44 @@ def test_lmhead_grads_skip_zero_weight():
     c = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], zero_w, flags=1)
     torch.cuda.synchronize()
     assert not c[0].any() and not c[1].any()
+
+
+def test_lmhead_loss_seq_mean_and_its_gradients():
+    """grpo_lmhead_loss_fwd_ex with the per-response mean (the original GRPO
+    aggregation): loss and w against the oracle's seq-mean loss, and the
+    backward with those weights against the oracle's gradients."""
+    n = H.g()
+    w = H.with_contrast(wl.variant(wl.QWEN_G16_KL, name="lmg_seqmean", B=1, G=4, P=5, C=24,
+                                   V=1500, eos_id=1499, seed=97))
+    d = 128
+    hidden = wl.make_hidden(w, d, "cpu").cuda()
+    weight = wl.make_lm_head(w, d, "cpu").cuda()
+    ids = wl.make_ids(w)
+    R = wl.make_rewards(w)
+    Hn, Wn = _bits16(hidden), _bits16(weight)
+    m_o, len_o = oracle.mask(ids, w.P, w.C, w.eos_id)
+    A_o = oracle.advantage(R, w.G)
+    lp_o, lse_o = oracle.lmhead_logp(Hn, Wn, w.P, w.C, ids, len_o)
+    old, ref = H.host_inputs(w, lp_o, m_o)
+    kinks = np.array([-np.log1p(w.eps), -np.log1p(-w.eps)])
+    with np.errstate(invalid="ignore"):
+        dist = np.min(np.abs((old.astype(np.float64) - lp_o)[..., None] - kinks), axis=-1)
+        old[dist < 1e-3] += np.float32(2e-3)
+    loss_o, w_o, ell_o = oracle.loss_seq_mean(lp_o, old.astype(np.float64),
+                                              ref.astype(np.float64), A_o, len_o, w.eps, w.beta)
+    t_ids = H.dev(ids)
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(R), w.G)
+    out = n.grpo_lmhead_loss_fwd(hidden, weight, w.P, t_ids, lens, adv, H.dev(old), H.dev(ref),
+                                 w.eps, w.beta, agg=n.GRPO_AGG_SEQ_MEAN)
+    assert n.grpo_check_error(out["workspace"]) == 0
+    H.assert_loss(float(out["loss"].item()), loss_o, ell_o, float(w.N))
+    wt = out["w"].cpu().numpy().astype(np.float64)
+    ok = m_o == 1
+    # the size of w's two terms, per token: (|A| r + beta (1 + exp(ref - logp))) / (N len_i)
+    scale = H.w_scale(lp_o, old, ref, A_o, w.beta, 1.0) / (w.N * np.maximum(len_o, 1)[:, None])
+    assert np.all(np.abs(wt - w_o)[ok] <= 1e-4 * scale[ok] + 1e-12)
+    dh, dw, ws = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"])
+    gr = oracle.lmhead_grads(Hn, Wn, w.P, w.C, ids, len_o, lse_o, w_o, 1.0, magnitudes=True)
+    assert_grad(dh.cpu().numpy(), gr["dhidden"], gr["dhidden_mag"], "dhidden")
+    assert_grad(dw.cpu().numpy(), gr["dweight"], gr["dweight_mag"], "dweight")
