@@ -65,6 +65,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
   __shared__ __align__(8) uint64_t s_empty[kStages];
   __shared__ __align__(8) uint64_t s_acc_full[2];
   __shared__ __align__(8) uint64_t s_acc_empty[2];
+  __shared__ __align__(8) uint64_t s_drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -82,6 +83,7 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
       mbar_init(smem_u32(&s_acc_full[k]), 1);   // the leader's multicast commit
       mbar_init(smem_u32(&s_acc_empty[k]), 2 * kEpi);  // leader: the epilogue warps of 2 CTAs
     }
+    mbar_init(smem_u32(&s_drain), 1);  // the leader's last commit
     mbar_init_fence();
   }
   if (warp == 1) tmem_alloc_pair(&s_tmem, 512);  // all 512 columns: kBufs accumulators
@@ -200,9 +202,12 @@ __device__ __forceinline__ void pair_pipeline(Op& op, uint32_t ring, WsHeader* h
     op.epi_finish();
   }
 
-  // Teardown: every MMA has completed once both CTAs' epilogues consumed their
-  // tiles (or, after a timeout, once the last commit lands); both CTAs free
-  // the pair's TMEM together.
+  // Teardown: a last commit from the leader lands in both CTAs once every MMA
+  // it issued has completed (at once when the epilogues consumed every tile;
+  // after a timeout, it keeps TMEM allocated until the MMAs in flight finish);
+  // then both CTAs free the pair's TMEM together.
+  if (warp == 1 && lane == 0 && rank == 0) umma_commit_pair(smem_u32(&s_drain));
+  if (tid == 0 && !mbar_wait(smem_u32(&s_drain), 0)) atomicOr(&hdr->flags, kFlagTimeout);
   tmem_fence_before();
   pair_sync();
   if (warp == 1) {
