@@ -243,6 +243,15 @@ grpo_status grpo_logprobs(const void *logits, grpo_dtype dtype, int64_t N, int64
  *   0, as autograd through the slice and the mask gives.
  * bfloat16 results are rounded to nearest even from float32.  dlogits must
  * not overlap logits.  Lengths are clamped to [0, C].
+ *
+ * Stream order: when the library's previous call on this stream (and
+ * device) was grpo_loss_fwd or grpo_loss_fwd_ex, the rows that score nothing
+ * are written while that forward's last kernels may still run (they depend
+ * only on len).  The usual contract of a stream-ordered call covers it: len
+ * and dlogits must not be written, and dlogits must not be read, by that
+ * forward call (its outputs, workspace and inputs must not overlap dlogits
+ * or len).  Any other preceding work is complete before this call touches
+ * memory.
  */
 grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
                           int64_t V, const int64_t *input_ids, const int32_t *len,

@@ -1,0 +1,87 @@
+"""Stream order of the backward.  Right after the loss forward on one stream,
+grpo_loss_bwd writes the rows that score nothing before it waits on the
+forward's last kernels (those rows depend only on the lengths), and the
+scored rows after; after any other library call it waits first and walks the
+rows in memory order.  Both orders must write every element with the same
+bits, and the oracle must agree with the first (the parity tests run
+forward -> backward back to back, so they take it too)."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+from vocab_wide_logprob_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+def _both_orders(w, logits, flags=None, grad=None):
+    n = H.g()
+    ids = torch.from_numpy(wl.make_ids(w)).cuda()
+    R = torch.from_numpy(wl.make_rewards(w)).cuda()
+    _, lens = n.grpo_mask(ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(R, w.G)
+    gt = None if grad is None else torch.tensor([grad], dtype=torch.float32, device="cuda")
+    # NaN-filled before the forward, so that no other kernel sits between the
+    # forward and the first backward
+    d_first = torch.full_like(logits, float("nan"))
+    d_wait = torch.full_like(logits, float("nan"))
+    out = n.grpo_loss_fwd(logits, w.P, ids, lens, adv, None, None, w.eps, 0.0)
+    n.grpo_loss_bwd(logits, w.P, ids, lens, out["lse"], out["w"], gt, d_first, flags=flags)
+    n.grpo_advantage(R, w.G, adv)  # a library call in between: the next backward waits first
+    n.grpo_loss_bwd(logits, w.P, ids, lens, out["lse"], out["w"], gt, d_wait, flags=flags)
+    assert n.grpo_check_error(out["workspace"]) == 0
+    torch.cuda.synchronize()
+    return d_first, d_wait, lens.cpu().numpy()
+
+
+def _check(w, logits, **kw):
+    d_first, d_wait, lens = _both_orders(w, logits, **kw)
+    assert not torch.isnan(d_first).any() and not torch.isnan(d_wait).any()
+    assert torch.equal(_bits(d_first), _bits(d_wait))
+    # rows that score nothing are exactly +0 (bit pattern 0)
+    zero = np.ones((w.N, w.T), bool)
+    for i in range(w.N):
+        zero[i, w.P - 1:w.P - 1 + int(lens[i])] = False
+    zb = _bits(d_first)[torch.from_numpy(zero).cuda()]
+    assert not bool((zb != 0).any())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(C=1),
+    dict(P=1),
+    dict(B=1, G=32),
+    dict(forced={"lengths": {i: 1 for i in range(8)}}),
+    dict(forced={"lengths": {i: 0 for i in range(8)}}),
+    dict(B=1, G=2, C=200, V=4099, dtype="bf16"),
+], ids=["tiny", "C1", "P1", "G32", "eos_all", "eos_none", "C200_V4099_bf16"])
+def test_orders_same_bits(kw):
+    w = wl.variant(wl.TINY, name="order", **kw)
+    _check(w, wl.make_logits_cpu(w).cuda())
+
+
+def test_more_completions_than_the_prefix_table():
+    """1,100 completions: above the 1,024 the reordered walk covers, so the
+    backward waits first and walks memory order either way; the oracle agrees."""
+    w = wl.variant(wl.TINY, name="order_n1100", B=275, G=4, P=2, C=3, V=64)
+    _check(w, wl.make_logits_cpu(w).cuda())
+    H.check_small(w)
+
+
+def test_skip_zero_weight_orders_same_bits():
+    w = wl.variant(wl.TINY, name="order_skip", B=4, G=4, C=40, V=2000, dtype="bf16")
+    _check(w, wl.make_logits_cpu(w).cuda(), flags=1, grad=0.5)
+
+
+def test_full_size_orders_same_bits():
+    """The benchmark workload: the rows that score nothing (about two thirds
+    of the 0.93 GB buffer) are written while the forward's kernels run."""
+    w = wl.QWEN_G8
+    logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    wl.fill_logits_cuda(w, logits)
+    _check(w, logits)

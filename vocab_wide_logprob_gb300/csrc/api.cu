@@ -4,6 +4,10 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "common.cuh"
 #include "lmhead.cuh"
 #include "host_rows.cuh"
@@ -52,6 +56,37 @@ cudaError_t current_device(DeviceInfo* d) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// What the library enqueued last on a stream.  The backward may write the
+// rows that score nothing before waiting on the preceding kernel only when
+// that kernel is the loss forward's (whose kernels write neither the lengths
+// nor dlogits), so every entry point that enqueues work calls
+// stream_take_after_fwd() first, and a successful loss forward then calls
+// stream_mark_after_fwd().  The set holds the (device, stream) pairs whose
+// last library call was the loss forward.  Calls from several host threads
+// on one stream are ordered as their launches are only if the caller orders
+// them.
+std::mutex g_order_mutex;
+std::set<std::pair<int, cudaStream_t>> g_after_fwd;
+
+std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) (void)cudaGetLastError();
+  return {dev, st};
+}
+
+// Whether the library's last call on `st` was the loss forward; forgets it.
+bool stream_take_after_fwd(cudaStream_t st) {
+  const auto key = order_key(st);
+  std::lock_guard<std::mutex> lk(g_order_mutex);
+  return g_after_fwd.erase(key) != 0;
+}
+
+void stream_mark_after_fwd(cudaStream_t st) {
+  const auto key = order_key(st);
+  std::lock_guard<std::mutex> lk(g_order_mutex);
+  g_after_fwd.insert(key);
+}
 
 // a*b*c without int64 overflow, or -1
 int64_t mul3(int64_t a, int64_t b, int64_t c) {
@@ -113,6 +148,7 @@ grpo_status grpo_mask(const int64_t* input_ids, int64_t N, int64_t P, int64_t C,
   if (len == nullptr || (C > 0 && input_ids == nullptr)) return GRPO_ERR_INVALID_ARG;
   if (mul3(N, P + C, 8) < 0 || C > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(input_ids, 8) || !aligned(len, 4)) return GRPO_ERR_MISALIGNED;
+  stream_take_after_fwd(stream);
   return from_cuda(launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream));
 }
 
@@ -123,6 +159,7 @@ grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* ad
   if (rewards == nullptr || adv == nullptr) return GRPO_ERR_INVALID_ARG;
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4)) return GRPO_ERR_MISALIGNED;
+  stream_take_after_fwd(stream);
   return from_cuda(launch_advantage(rewards, B, G, 0, 0.f, adv, nullptr, (cudaStream_t)stream));
 }
 
@@ -136,6 +173,7 @@ grpo_status grpo_advantage_ex(const float* rewards, int64_t B, int64_t G, grpo_a
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4) || !aligned(n_contrast, 4))
     return GRPO_ERR_MISALIGNED;
+  stream_take_after_fwd(stream);
   return from_cuda(launch_advantage(rewards, B, G, (int)mode, std_eps, adv, n_contrast,
                                     (cudaStream_t)stream));
 }
@@ -203,13 +241,16 @@ grpo_status loss_fwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64
   DeviceInfo d;
   cudaError_t e = current_device(&d);
   if (e != cudaSuccess) return GRPO_ERR_CUDA;
+  stream_take_after_fwd(st);
   // the prep kernel also resets the error flags and the reduction ticket
   if ((e = launch_prep(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
   if (N == 0 || C == 0)
     return mode == 0 ? from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st)) : GRPO_OK;
   if ((e = launch_lse_gather(a, d, st)) != cudaSuccess) return GRPO_ERR_CUDA;
   if (mode == 1) return from_cuda(launch_mask_fill(a, st));
-  return from_cuda(launch_surrogate(a, st));
+  if ((e = launch_surrogate(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
+  stream_mark_after_fwd(st);
+  return GRPO_OK;
 }
 
 }  // namespace
@@ -282,6 +323,7 @@ grpo_status grpo_loss_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, in
   a.skip_zero_weight = (flags & GRPO_BWD_SKIP_ZERO_WEIGHT) != 0;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  a.after_fwd = stream_take_after_fwd(stream);
   return from_cuda(launch_dlogits(a, d, (cudaStream_t)stream));
 }
 
@@ -370,12 +412,14 @@ grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N
   b.grad = grad_loss;
   b.dlogits = dlogits;
   b.skip_zero_weight = false;
+  b.after_fwd = false;
   const cudaStream_t st = (cudaStream_t)stream;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  stream_take_after_fwd(st);
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
-  if (launch_zero_rows(b, d, st, logp, lse, w) != cudaSuccess) return GRPO_ERR_CUDA;
-  return from_cuda(launch_lse_grad(a, b, d, st));
+  if (launch_lse_grad(a, b, d, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_zero_rows(b, d, st, logp, lse, w));
 }
 
 grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, int64_t N,
@@ -419,6 +463,7 @@ grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, in
   const cudaStream_t st = (cudaStream_t)stream;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  stream_take_after_fwd(st);
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (launch_gather_host_rows(attr.devicePointer, staging, esize, a, d, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
@@ -495,6 +540,7 @@ grpo_status lmhead_fwd_impl(const void* hidden, const void* weight, int64_t N, i
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
   if (workspace_bytes < lm_layout(N, C, d, dev.sms).total) return GRPO_ERR_WORKSPACE;
+  stream_take_after_fwd(stream);
   FwdArgs a = {};
   a.dtype = 1;
   a.N = N;
@@ -598,6 +644,7 @@ grpo_status grpo_lmhead_loss_bwd_ex(const void* hidden, const void* weight, int6
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
   if (workspace_bytes < lm_bwd_layout(N, C, V, d, dev.sms).total) return GRPO_ERR_WORKSPACE;
+  stream_take_after_fwd(stream);
   FwdArgs f = {};
   f.N = N;
   f.P = P;
@@ -638,6 +685,7 @@ grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
   if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
   uint32_t flags = 0;
   const cudaStream_t st = (cudaStream_t)stream;
+  stream_take_after_fwd(st);
   if (cudaMemcpyAsync(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return GRPO_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -656,6 +704,7 @@ grpo_status grpo_copy(void* dst, const void* src, size_t bytes, grpo_stream_t st
   if (d8 < s8 + bytes && s8 < d8 + bytes) return GRPO_ERR_INVALID_ARG;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+  stream_take_after_fwd(stream);
   return from_cuda(launch_copy(dst, src, bytes, d, (cudaStream_t)stream));
 }
 

@@ -174,7 +174,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // writes to be visible, so no ordering is lost, while the launch and the
 // shared-memory prologue overlap the previous kernel's tail.  pdl_trigger()
 // lets the next kernel start launching; it is issued once this kernel's
-// CTAs are all resident, so it cannot take their slots.
+// CTAs are all resident, so it cannot take their slots.  One exception:
+// the backward, launched right after the loss forward on the same stream,
+// writes the rows that score nothing before its wait (dlogits.cu).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -492,6 +494,9 @@ struct BwdArgs {
   const float* grad;
   void* dlogits;
   bool skip_zero_weight;  // rows with g*w == 0: zeros, logits not read
+  // the launch directly follows the loss forward on its stream: rows that
+  // score nothing may be written before waiting on it
+  bool after_fwd;
 };
 cudaError_t launch_dlogits(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st);
 // Store-only pass of the fused path: zero dlogits rows and masked logp/lse/w.

@@ -11,11 +11,23 @@
 // its logits once (16-byte loads) and writes g*w_t*(onehot - exp(z - lse_t));
 // any other row is written with zeros and not read.  The target column uses
 // 1 - p_y = -expm1(z_y - lse) to keep its precision when p_y is close to 1.
-// Work items are (row, 1/K of the row); a persistent grid walks them in
-// memory order.
+// Work items are (row, 1/K of the row), walked by a grid-stride loop.
+//
+// Item order.  By default the items go in memory order and every CTA waits
+// for the preceding kernel first.  A row that scores nothing depends only on
+// the lengths, though, and the loss forward's kernels write neither the
+// lengths nor dlogits; so when the host knows this launch directly follows
+// the loss forward on its stream (`zero_first`), the items are ordered with
+// every such row first: those rows are written without waiting, while the
+// forward's last kernels still run, and a CTA waits only before its first
+// scored row (which needs lse and w).  Each CTA then computes the prefix sums
+// of the lengths itself (batches of up to kZeroFirstMaxN completions).
 #include "common.cuh"
 
 namespace grpo {
+
+constexpr int kZeroFirstMaxN = 1024;
+constexpr int kPrefixPerThread = kZeroFirstMaxN / kThreads;
 
 template <typename T>
 struct DlParams {
@@ -35,19 +47,78 @@ struct DlParams {
   float* lse_out;
   float* w_out;
   int skip_zero_weight;  // a scored row with g*w == 0 is written with zeros, not read
+  int zero_first;        // rows that score nothing first, written before the wait (N <= 1024)
 };
 
+// s_pre[i] = sum of min(max(len[k], 0), C) over k < i, for i = 0..N (N <=
+// kZeroFirstMaxN), computed by the whole CTA.  Reads the lengths through L2:
+// they are not written by any kernel still running.
+__device__ __forceinline__ void length_prefix(const int32_t* __restrict__ len, int64_t N,
+                                              int64_t C, int32_t* s_pre, int32_t* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (int)((N + kThreads - 1) / kThreads);
+  const int k0 = tid * per;
+  int32_t v[kPrefixPerThread];
+  int32_t own = 0;
+#pragma unroll
+  for (int u = 0; u < kPrefixPerThread; ++u) {
+    int32_t L = 0;
+    if (u < per && k0 + u < N) {
+      L = __ldcg(len + k0 + u);
+      L = L < 0 ? 0 : (L > C ? (int32_t)C : L);
+    }
+    v[u] = L;
+    own += L;
+  }
+  int32_t x = own;  // inclusive scan within the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int32_t run = x - own;
+  for (int k = 0; k < warp; ++k) run += s_warp[k];
+  if (tid == 0) s_pre[0] = 0;
+#pragma unroll
+  for (int u = 0; u < kPrefixPerThread; ++u)
+    if (u < per && k0 + u < N) {
+      run += v[u];
+      s_pre[k0 + u + 1] = run;
+    }
+  __syncthreads();
+}
+
 // kZeroOnly: write only the rows that score nothing (and the masked
-// per-token outputs); scored rows are left to lse_grad_kernel.
+// per-token outputs); scored rows are left to lse_grad_kernel, which is
+// launched just before this kernel and writes disjoint rows and positions,
+// so no CTA waits on it before writing (the lengths were written before
+// either started): the zeros stream out while lse_grad_kernel runs.
+// Resident CTAs per SM the register budget is held to: 5 for bf16 (the
+// oversubscribed grid streams faster with more of them), 4 for fp32 (whose
+// wider unroll would spill at 5).
+template <typename T>
+constexpr int dl_min_blocks() {
+  return sizeof(T) == 2 ? 5 : 4;
+}
+
 template <typename T, bool kZeroOnly>
-__global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) {
+__global__ void __launch_bounds__(kThreads, dl_min_blocks<T>()) dlogits_kernel(const DlParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
   constexpr int U = E::kUnroll;
   const int tid = threadIdx.x;
-  pdl_wait();
+  __shared__ int32_t s_pre[kZeroFirstMaxN + 1];
+  __shared__ int32_t s_warp[kThreads / 32];
+  const bool zero_first = !kZeroOnly && p.zero_first;
+  bool waited = false;  // the preceding kernel's outputs (lse, w) are visible once set
+  if (zero_first) {
+    length_prefix(p.len, p.N, p.C, s_pre, s_warp);
+  } else if (!kZeroOnly) {
+    pdl_wait();
+    waited = true;
+  }
   pdl_trigger();
-  const float g = p.grad != nullptr ? __ldg(p.grad) : 1.f;
   const int64_t items = p.N * p.T_len * p.split;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   if (kZeroOnly) {
@@ -64,15 +135,48 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
     }
   }
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-    const int64_t row = item / p.split;
-    const int64_t j = item - row * p.split;
-    const int64_t i = row / p.T_len;
+    const int64_t r = item / p.split;
+    const int64_t j = item - r * p.split;
+    int64_t row, i, L;
+    if (!zero_first) {
+      row = r;
+      i = row / p.T_len;
+      L = __ldg(p.len + i);
+      L = L < 0 ? 0 : (L > p.C ? p.C : L);
+    } else if (r < p.N * p.T_len - s_pre[p.N]) {  // rows that score nothing come first
+      // zero row r: completion i has i*T_len - s_pre[i] zero rows before it
+      // (every completion has at least one, its last row), its own being the
+      // prompt rows 0..P-2 and then the rows past its length
+      int lo = 0, hi = (int)p.N;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)mid * p.T_len - s_pre[mid] <= r)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      i = lo;
+      L = s_pre[lo + 1] - s_pre[lo];
+      const int64_t q = r - (i * p.T_len - s_pre[lo]);
+      row = i * p.T_len + (q < p.P - 1 ? q : q + L);
+    } else {  // then the scored rows
+      const int64_t sr = r - (p.N * p.T_len - s_pre[p.N]);
+      int lo = 0, hi = (int)p.N;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pre[mid] <= sr)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      i = lo;
+      L = s_pre[lo + 1] - s_pre[lo];
+      row = i * p.T_len + p.P - 1 + (sr - s_pre[lo]);
+    }
     const int64_t t = row - i * p.T_len - (p.P - 1);  // completion token this row scores
     const int64_t v0 = j * p.chunk;
     const int64_t v1 = min(p.V, v0 + p.chunk);
     if (v0 >= v1) continue;
-    int64_t L = __ldg(p.len + i);
-    L = L < 0 ? 0 : (L > p.C ? p.C : L);
     T* orow = p.dlogits + row * p.V;
     const T* zrow = p.logits + row * p.V;
     // 16-byte aligned interior [a, b) of the output slice
@@ -86,7 +190,11 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
     bool zero_row = t < 0 || t >= L;  // the row scores nothing
     float gw = 0.f;
     if (!zero_row && !kZeroOnly) {
-      gw = g * __ldg(p.w + i * p.C + t);
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
+      gw = (p.grad != nullptr ? __ldg(p.grad) : 1.f) * __ldg(p.w + i * p.C + t);
       if (p.skip_zero_weight && gw == 0.f) zero_row = true;  // its gradient is 0
     }
     if (zero_row) {  // zeros, logits not read
@@ -151,6 +259,10 @@ __global__ void __launch_bounds__(kThreads) dlogits_kernel(const DlParams<T> p) 
       E::store1(orow + e, o);
     }
   }
+  // The kernel must not complete before the preceding one (the next launch
+  // on the stream relies on it): when no CTA has waited (the store-only mode,
+  // or no scored row in the batch), CTA 0 does.
+  if (!waited && blockIdx.x == 0) pdl_wait();
 }
 
 namespace {
@@ -176,6 +288,7 @@ cudaError_t launch_t(const BwdArgs& a, const DeviceInfo& d, cudaStream_t st, flo
   p.lse_out = lse;
   p.w_out = w_out;
   p.skip_zero_weight = a.skip_zero_weight ? 1 : 0;
+  p.zero_first = !kZeroOnly && a.after_fwd && a.N <= kZeroFirstMaxN ? 1 : 0;
   p.split = row_split(a.V * (int64_t)sizeof(T), "GRPO_BWD_SPLIT", 8);
   p.chunk = ((a.V + p.split - 1) / p.split + EPV - 1) / EPV * EPV;
   // An oversubscribed grid (many more CTAs than fit at once, grid-stride over

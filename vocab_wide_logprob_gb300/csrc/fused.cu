@@ -17,7 +17,8 @@
 // into the same lse and w; pass 2 re-reads the slice (an L2 hit: the slices
 // in flight on the whole GPU total a few tens of MB) and writes the gradient.
 // Rows that score nothing are written with zeros by a separate store-only
-// kernel.  Per element the arithmetic is that of lse_gather_kernel and
+// kernel launched after this one, which runs beside it (its CTAs take the
+// slots this persistent grid leaves free and do not wait on it).  Per element the arithmetic is that of lse_gather_kernel and
 // dlogits_kernel, and the per-token terms are token_terms(), so logp, lse, w
 // and dlogits have the same bits as the unfused path; only the loss's
 // summation order differs (per cluster, then clusters in order).

@@ -40,8 +40,11 @@ __global__ void __launch_bounds__(kThreads) surrogate_kernel(const SurParams p) 
   __shared__ double s_red[kWarps];
   __shared__ bool s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
+  // Trigger first: the backward that follows can then launch while the
+  // log-sum-exp kernel still runs and write its rows that score nothing (it
+  // waits on this kernel before it reads lse or w).
   pdl_trigger();
+  pdl_wait();
   const int64_t NC = p.N * p.C;
   double acc = 0.0;
   for (int64_t k = (int64_t)blockIdx.x * kThreads + tid; k < NC;
