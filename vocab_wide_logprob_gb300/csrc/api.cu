@@ -335,13 +335,36 @@ grpo_status grpo_loss_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64
                           stream);
 }
 
-grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
-                                 int64_t C, int64_t V, const int64_t* input_ids,
-                                 const int32_t* len, const float* adv, const float* old_logp,
-                                 const float* ref_logp, float eps, float beta, float norm,
-                                 grpo_aggregation agg, const float* grad_loss, float* logp,
-                                 float* lse, float* w, float* loss, void* dlogits, void* workspace,
-                                 size_t workspace_bytes, grpo_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Launches prep and the gather of the scored rows from host memory (through
+// the buffer's device mapping `host_src`) into the same rows of `staging`.
+grpo_status launch_host_gather(const void* host_src, void* staging, size_t esize, int64_t N,
+                               int64_t P, int64_t C, int64_t V, const int32_t* len,
+                               void* workspace, const DeviceInfo& d, cudaStream_t st) {
+  FwdArgs a = {};
+  a.N = N;
+  a.P = P;
+  a.C = C;
+  a.V = V;
+  a.len = len;
+  a.ws = workspace;
+  if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  return from_cuda(launch_gather_host_rows(host_src, staging, esize, a, d, st));
+}
+
+// grpo_loss_fwd_bwd_ex; with host_src (the device mapping of page-locked
+// host logits, validated by the caller) the scored rows are first gathered
+// from it into `logits`, the staging buffer.
+grpo_status fwd_bwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
+                         int64_t V, const int64_t* input_ids, const int32_t* len,
+                         const float* adv, const float* old_logp, const float* ref_logp,
+                         float eps, float beta, float norm, grpo_aggregation agg,
+                         const float* grad_loss, float* logp, float* lse, float* w, float* loss,
+                         void* dlogits, void* workspace, size_t workspace_bytes,
+                         grpo_stream_t stream, const void* host_src) {
   if (agg != GRPO_AGG_TOKEN_SUM && agg != GRPO_AGG_SEQ_MEAN) return GRPO_ERR_UNSUPPORTED;
   grpo_status s = check_shapes(dtype, N, P, C, V);
   if (s != GRPO_OK) return s;
@@ -356,26 +379,39 @@ grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N
   }
   const bool same_phase = ((reinterpret_cast<uintptr_t>(logits) ^
                             reinterpret_cast<uintptr_t>(dlogits)) & 15u) == 0;
+  if (N > 0 && C > 0) {
+    // the forward's validation (pointers, eps, beta, norm, workspace), before
+    // anything is enqueued
+    if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) ||
+        isinf(norm))
+      return GRPO_ERR_INVALID_ARG;
+    if (loss == nullptr || workspace == nullptr || len == nullptr || adv == nullptr ||
+        logits == nullptr || input_ids == nullptr || logp == nullptr || lse == nullptr ||
+        w == nullptr)
+      return GRPO_ERR_INVALID_ARG;
+    if (beta != 0.f && ref_logp == nullptr) return GRPO_ERR_INVALID_ARG;
+    if (!aligned(logits, esize) || !aligned(input_ids, 8) || !aligned(len, 4) ||
+        !aligned(adv, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) ||
+        !aligned(logp, 4) || !aligned(lse, 4) || !aligned(w, 4) || !aligned(loss, 4) ||
+        !aligned(workspace, 256))
+      return GRPO_ERR_MISALIGNED;
+    if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
+  }
   if (N == 0 || C == 0 || !same_phase) {  // nothing to fuse, or no common vector grid
+    if (host_src != nullptr && N > 0 && C > 0) {
+      DeviceInfo d;
+      if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
+      stream_take_after_fwd((cudaStream_t)stream);
+      s = launch_host_gather(host_src, const_cast<void*>(logits), esize, N, P, C, V, len,
+                             workspace, d, (cudaStream_t)stream);
+      if (s != GRPO_OK) return s;
+    }
     s = grpo_loss_fwd_ex(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
                          beta, norm, agg, logp, lse, w, loss, workspace, workspace_bytes, stream);
     if (s != GRPO_OK) return s;
     return grpo_loss_bwd(logits, dtype, N, P, C, V, input_ids, len, lse, w, grad_loss, dlogits,
                          stream);
   }
-  // the forward's validation (pointers, eps, beta, norm, workspace)
-  if (!(eps >= 0.f && eps < 1.f) || !(beta >= 0.f) || isinf(beta) || isnan(norm) || isinf(norm))
-    return GRPO_ERR_INVALID_ARG;
-  if (loss == nullptr || workspace == nullptr || len == nullptr || adv == nullptr ||
-      logits == nullptr || input_ids == nullptr || logp == nullptr || lse == nullptr ||
-      w == nullptr)
-    return GRPO_ERR_INVALID_ARG;
-  if (beta != 0.f && ref_logp == nullptr) return GRPO_ERR_INVALID_ARG;
-  if (!aligned(logits, esize) || !aligned(input_ids, 8) || !aligned(len, 4) ||
-      !aligned(adv, 4) || !aligned(old_logp, 4) || !aligned(ref_logp, 4) || !aligned(logp, 4) ||
-      !aligned(lse, 4) || !aligned(w, 4) || !aligned(loss, 4) || !aligned(workspace, 256))
-    return GRPO_ERR_MISALIGNED;
-  if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
 
   FwdArgs a;
   a.logits = logits;
@@ -417,9 +453,36 @@ grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
   stream_take_after_fwd(st);
+  if (host_src != nullptr) {
+    // The zero writer goes between the gather and the gradient kernel: it
+    // needs no logits, so it writes while the gather waits on the host link
+    // (it does not wait on the gather; its CTA 0 waits before exiting, so the
+    // gradient kernel, which waits on it, sees the gathered rows).
+    grpo_status g = launch_host_gather(host_src, const_cast<void*>(logits), esize, N, P, C, V,
+                                       len, workspace, d, st);
+    if (g != GRPO_OK) return g;
+    if (launch_zero_rows(b, d, st, logp, lse, w) != cudaSuccess) return GRPO_ERR_CUDA;
+    return from_cuda(launch_lse_grad(a, b, d, st));
+  }
   if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
   if (launch_lse_grad(a, b, d, st) != cudaSuccess) return GRPO_ERR_CUDA;
   return from_cuda(launch_zero_rows(b, d, st, logp, lse, w));
+}
+
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
+                                 int64_t C, int64_t V, const int64_t* input_ids,
+                                 const int32_t* len, const float* adv, const float* old_logp,
+                                 const float* ref_logp, float eps, float beta, float norm,
+                                 grpo_aggregation agg, const float* grad_loss, float* logp,
+                                 float* lse, float* w, float* loss, void* dlogits, void* workspace,
+                                 size_t workspace_bytes, grpo_stream_t stream) {
+  return fwd_bwd_impl(logits, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                      beta, norm, agg, grad_loss, logp, lse, w, loss, dlogits, workspace,
+                      workspace_bytes, stream, nullptr);
 }
 
 grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, int64_t N,
@@ -453,23 +516,9 @@ grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, in
   const char* sg = static_cast<const char*>(staging);
   const char* dl = static_cast<const char*>(dlogits);
   if (dlogits != nullptr && dl < sg + bytes && sg < dl + bytes) return GRPO_ERR_INVALID_ARG;
-  FwdArgs a = {};
-  a.N = N;
-  a.P = P;
-  a.C = C;
-  a.V = V;
-  a.len = len;
-  a.ws = workspace;
-  const cudaStream_t st = (cudaStream_t)stream;
-  DeviceInfo d;
-  if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
-  stream_take_after_fwd(st);
-  if (launch_prep(a, st) != cudaSuccess) return GRPO_ERR_CUDA;
-  if (launch_gather_host_rows(attr.devicePointer, staging, esize, a, d, st) != cudaSuccess)
-    return GRPO_ERR_CUDA;
-  return grpo_loss_fwd_bwd(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp,
-                           eps, beta, norm, grad_loss, logp, lse, w, loss, dlogits, workspace,
-                           workspace_bytes, stream);
+  return fwd_bwd_impl(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
+                      beta, norm, GRPO_AGG_TOKEN_SUM, grad_loss, logp, lse, w, loss, dlogits,
+                      workspace, workspace_bytes, stream, attr.devicePointer);
 }
 
 grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,

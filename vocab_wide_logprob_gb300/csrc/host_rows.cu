@@ -28,6 +28,11 @@ __device__ __forceinline__ int64_t scored_row(const int32_t* __restrict__ off, i
 
 // U: the unit copied per access (16 bytes when a row is a whole number of
 // 16-byte vectors and both buffers are 16-byte aligned, else one element).
+// Each thread keeps kGatherUnroll loads in flight (the host link's latency is
+// microseconds), so a grid of a few CTAs per SM fills the link and leaves
+// the SMs' other slots to a kernel running beside this one.
+constexpr int kGatherUnroll = 4;
+
 template <typename U>
 __global__ void __launch_bounds__(kThreads) gather_host_rows_kernel(const U* __restrict__ src,
                                                                     U* __restrict__ dst,
@@ -37,15 +42,32 @@ __global__ void __launch_bounds__(kThreads) gather_host_rows_kernel(const U* __r
   pdl_wait();
   pdl_trigger();
   const int64_t total = (int64_t)off[N] * units_per_row;
-  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < total;
-       k += (int64_t)gridDim.x * kThreads) {
-    const int64_t r = k / units_per_row, c = k - r * units_per_row;
-    const int64_t row = scored_row(off, N, T, P, r);
-    const int64_t e = row * units_per_row + c;
-    if constexpr (sizeof(U) == 16)
-      st_stream(dst + e, ld_stream(src + e));
-    else
-      dst[e] = src[e];
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t k0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; k0 < total;
+       k0 += stride * kGatherUnroll) {
+    U v[kGatherUnroll];
+    int64_t e[kGatherUnroll];
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int64_t k = k0 + u * stride;
+      e[u] = -1;
+      if (k < total) {
+        const int64_t r = k / units_per_row, c = k - r * units_per_row;
+        e[u] = scored_row(off, N, T, P, r) * units_per_row + c;
+        if constexpr (sizeof(U) == 16)
+          v[u] = ld_stream(src + e[u]);
+        else
+          v[u] = src[e[u]];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      if (e[u] < 0) continue;
+      if constexpr (sizeof(U) == 16)
+        st_stream(dst + e[u], v[u]);
+      else
+        dst[e[u]] = v[u];
+    }
   }
 }
 
@@ -60,7 +82,8 @@ cudaError_t launch_gather_host_rows(const void* src, void* dst, size_t esize, co
   const size_t row_bytes = (size_t)a.V * esize;
   const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(dst) % 16 == 0;
-  const int64_t grid = 64 * (int64_t)d.sms;  // bound by the host link, not by the SMs
+  // bound by the host link, not by the SMs: a few CTAs per SM
+  const int64_t grid = (int64_t)grid_mult("GRPO_HOST_GRID", 4) * d.sms;
   if (vec)
     return launch_pdl(gather_host_rows_kernel<uint4>, dim3((unsigned)grid), dim3(kThreads), 0, st,
                       1, static_cast<const uint4*>(src), static_cast<uint4*>(dst), off, a.N, T,
