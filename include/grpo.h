@@ -297,10 +297,14 @@ grpo_status grpo_loss_fwd_bwd(const void *logits, grpo_dtype dtype, int64_t N, i
  * page-locked host memory (cudaHostAlloc, or cudaHostRegister, mapped into the
  * device's address space).  The loss reads only the scored rows, row P-1+t of
  * sequence i for t < len_i ("compute_logprobs" and the completion mask), so
- * only those rows cross the host link: a kernel copies them through the
- * buffer's device mapping into the same rows of `staging`, device memory of
- * the logits' shape [N, P+C, V] (its other rows are neither read nor written),
- * and grpo_loss_fwd_bwd then runs on `staging`.
+ * only those rows cross the host link, read through the buffer's device
+ * mapping, and they are written to the same rows of `staging`, device memory
+ * of the logits' shape [N, P+C, V] (its other rows are neither read nor
+ * written).  When host_logits, staging and dlogits share their address modulo
+ * 16 bytes, the gradient kernel reads the host rows itself and computes while
+ * they arrive; otherwise a copy kernel fills `staging` first and
+ * grpo_loss_fwd_bwd runs on it.  Results are bit-identical to
+ * grpo_loss_fwd_bwd on the same logits in device memory either way.
  *
  * Arguments: those of grpo_loss_fwd_bwd with host_logits for logits, plus
  * staging (device, logits' size, element-aligned, not overlapping dlogits).

@@ -120,13 +120,17 @@ def test_fused_full_size_same_bits(w):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("dtype,V", [("bf16", 1024), ("bf16", 1001), ("f32", 1001)],
-                         ids=["bf16_vec16", "bf16_odd_V", "f32_odd_V"])
-def test_host_logits_match_device_path(dtype, V):
+@pytest.mark.parametrize("dtype,V,shift", [("bf16", 1024, 0), ("bf16", 1001, 0), ("f32", 1001, 0),
+                                           ("bf16", 1024, 1), ("f32", 1001, 1)],
+                         ids=["bf16_vec16", "bf16_odd_V", "f32_odd_V", "bf16_host_phase_shift",
+                              "f32_host_phase_shift"])
+def test_host_logits_match_device_path(dtype, V, shift):
     """grpo_loss_fwd_bwd_host on pinned host logits gives the bits of
-    grpo_loss_fwd_bwd on the same logits in device memory (16-byte, 4-byte and
-    2-byte copy units), and only the scored rows of the staging buffer are
-    written."""
+    grpo_loss_fwd_bwd on the same logits in device memory, and only the
+    scored rows of the staging buffer are written.  With the host buffer in
+    the staging buffer's 16-byte phase the gradient kernel reads the host rows
+    itself (ragged heads and tails for odd V); shifted by `shift` elements, the
+    rows are gathered first (16-byte, 4-byte and 2-byte copy units)."""
     n = H.g()
     w = H.with_contrast(wl.variant(wl.QWEN_G8, name=f"host_{dtype}_{V}", B=2, G=4, P=6, C=20,
                                    V=V, eos_id=V - 1, dtype=dtype, seed=91))
@@ -140,7 +144,13 @@ def test_host_logits_match_device_path(dtype, V):
     old = torch.from_numpy(rng.normal(-7, 1, (w.N, w.C)).astype(np.float32)).cuda()
     a = n.grpo_loss_fwd_bwd(logits.cuda(), w.P, t_ids, lens, adv, old, None, 0.2, 0.0)
     staging = torch.full(logits.shape, 7.0, dtype=logits.dtype, device="cuda")
-    b = n.grpo_loss_fwd_bwd_host(logits.pin_memory(), w.P, t_ids, lens, adv, old, None, 0.2, 0.0,
+    host = logits.pin_memory()
+    if shift:
+        buf = torch.empty(logits.numel() + shift, dtype=logits.dtype).pin_memory()
+        host = buf[shift:].view(logits.shape)
+        host.copy_(logits)
+        assert host.is_pinned() and host.data_ptr() % 16 != 0
+    b = n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, old, None, 0.2, 0.0,
                                  staging=staging)
     assert n.grpo_check_error(b["workspace"]) == 0
     for k in ("logp", "lse", "w", "loss"):

@@ -453,9 +453,23 @@ grpo_status fwd_bwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64_
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
   stream_take_after_fwd(st);
+  if (host_src != nullptr && ((reinterpret_cast<uintptr_t>(host_src) ^
+                               reinterpret_cast<uintptr_t>(logits)) & 15u) == 0) {
+    // The gradient kernel reads the scored rows from host memory itself
+    // (writing them to the staging buffer for its second pass), so its
+    // arithmetic runs while the rows cross the host link; the zero writer
+    // runs beside it as in the device-memory case.
+    FwdArgs ah = a;
+    ah.logits = host_src;
+    if (launch_prep(ah, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    if (launch_lse_grad_host(ah, b, const_cast<void*>(logits), d, st) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+    return from_cuda(launch_zero_rows(b, d, st, logp, lse, w));
+  }
   if (host_src != nullptr) {
-    // The zero writer goes between the gather and the gradient kernel: it
-    // needs no logits, so it writes while the gather waits on the host link
+    // Host rows in another 16-byte phase than the staging buffer: gather them
+    // first.  The zero writer goes between the gather and the gradient kernel:
+    // it needs no logits, so it writes while the gather waits on the host link
     // (it does not wait on the gather; its CTA 0 waits before exiting, so the
     // gradient kernel, which waits on it, sees the gathered rows).
     grpo_status g = launch_host_gather(host_src, const_cast<void*>(logits), esize, N, P, C, V,

@@ -29,6 +29,7 @@
 #include <tuple>
 
 #include "common.cuh"
+#include "host_rows.cuh"
 
 namespace grpo {
 namespace {
@@ -43,7 +44,8 @@ constexpr int kSmemOffsets = 4096;
 
 template <typename T>
 struct FusedParams {
-  const T* logits;
+  const T* logits;   // kHost: the device mapping of page-locked host logits
+  T* staging;        // kHost: device buffer of the logits' shape (scored rows written)
   T* dlogits;
   int64_t T_len, P, C, V, N;
   const int64_t* ids;
@@ -95,7 +97,15 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t smem_dst, const void* gsr
       : "memory");
 }
 
-template <typename T, int K>
+// kHost: the logits are in page-locked host memory.  Pass 1 then reads each
+// scored row through the device mapping with plain 16-byte loads (consumers
+// keep a stage's kVecPerThread loads in flight; the many CTAs fill the host
+// link) and writes what it read to the same row of `staging`; pass 2 reads
+// those vectors back, each thread the ones it wrote.  Element order, per-
+// thread batching and arithmetic are those of the ring path, so every result
+// has the same bits as with the logits in device memory; the producer warp
+// only takes part in the cluster barriers.
+template <typename T, int K, bool kHost>
 __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
@@ -168,6 +178,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     const int64_t row_index = i * p.T_len + (p.P - 1 + t);
     const T* row = p.logits + row_index * p.V;
     T* orow = p.dlogits + row_index * p.V;
+    T* srow = kHost ? p.staging + row_index * p.V : nullptr;
     int64_t a, b, nvec;
     if (v0 >= v1) {
       a = b = v0;
@@ -182,6 +193,13 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     const uint32_t bytes = (uint32_t)(nvec * 16);
     const int nchunks = (int)((bytes + kStageBytes - 1) / kStageBytes);
 
+    if (producer && kHost) {  // one arrival per row, as the consumers'
+      if (K > 1) {
+        cluster_arrive_relaxed();
+        cluster_wait();
+      }
+      continue;
+    }
     if (producer) {
       const char* src = reinterpret_cast<const char*>(row + a);
       for (int pass = 0; pass < 2; ++pass) {
@@ -233,6 +251,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     float xe = 0.f;
     if (e >= 0) {
       xe = E::load1(row + e);
+      if (kHost) E::store1(srow + e, xe);
       if (e == y) {
         zy = xe;
         found = true;
@@ -245,9 +264,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     const int cy = ky >= 0 ? (int)(ky / kVecPerStage) : -1;
     const int kl = ky >= 0 ? (int)(ky % kVecPerStage) : 0;
     const int ty = kl % kConsumers, uy = kl / kConsumers;
+    const uint4* hv = reinterpret_cast<const uint4*>(row + a);  // kHost: the host row
+    uint4* sv = kHost ? reinterpret_cast<uint4*>(srow + a) : nullptr;
     for (int c = 0; c < nchunks; ++c) {
       bool ok = !*(volatile int*)&s_abort;
-      if (ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+      if (!kHost && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
         atomicOr(&p.hdr->flags, kFlagTimeout);
         *(volatile int*)&s_abort = 1;
         ok = false;
@@ -256,11 +277,26 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
         const int nv = (int)min((int64_t)kVecPerStage, nvec - (int64_t)c * kVecPerStage);
         const uint32_t sbase = ring + stage * kStageBytes;
         uint4 d[kVecPerThread];
+        if constexpr (kHost) {
+          const int64_t base = (int64_t)c * kVecPerStage;
 #pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
-          const int k = tid + u * kConsumers;
-          d[u] = k < nv ? ld_shared_v4(sbase + 16u * k)
-                        : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            d[u] = k < nv ? ld_stream(hv + base + k)
+                          : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+          }
+#pragma unroll
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            if (k < nv) sv[base + k] = d[u];  // stays in L2 for pass 2
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            d[u] = k < nv ? ld_shared_v4(sbase + 16u * k)
+                          : make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
+          }
         }
         if (c == cy && tid == ty) {
 #pragma unroll
@@ -268,8 +304,10 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
             if (u == uy) zy = E::extract(d[u], ey);
           found = true;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+        if (!kHost) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+        }
         float x[kVecPerThread * EPV];
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) E::unpack(d[u], x + u * EPV);
@@ -389,7 +427,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     uint4* ovp = reinterpret_cast<uint4*>(orow + a);
     for (int c = 0; c < nchunks; ++c) {
       bool ok = !*(volatile int*)&s_abort;
-      if (ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+      if (!kHost && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
         atomicOr(&p.hdr->flags, kFlagTimeout);
         *(volatile int*)&s_abort = 1;
         ok = false;
@@ -398,13 +436,22 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
         const int nv = (int)min((int64_t)kVecPerStage, nvec - (int64_t)c * kVecPerStage);
         const uint32_t sbase = ring + stage * kStageBytes;
         uint4 d[kVecPerThread];
+        if constexpr (kHost) {  // the vectors this thread wrote in pass 1
+          const int64_t base = (int64_t)c * kVecPerStage;
 #pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
-          const int k = tid + u * kConsumers;
-          if (k < nv) d[u] = ld_shared_v4(sbase + 16u * k);
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            if (k < nv) d[u] = __ldcg(sv + base + k);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kVecPerThread; ++u) {
+            const int k = tid + u * kConsumers;
+            if (k < nv) d[u] = ld_shared_v4(sbase + 16u * k);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
           const int k = tid + u * kConsumers;
@@ -460,13 +507,16 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
 std::mutex g_occ_mutex;
 std::map<std::tuple<int, int, int, int>, int> g_occ;
 
+// staging != nullptr: a.logits is the device mapping of host logits (kHost).
 template <typename T, int K>
-cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, cudaStream_t st) {
+cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, cudaStream_t st,
+                     void* staging) {
   constexpr int EPV = Elt<T>::kPerVec;
   const WsLayout l = ws_layout(a.N);
   char* ws = static_cast<char*>(a.ws);
   FusedParams<T> p;
   p.logits = static_cast<const T*>(a.logits);
+  p.staging = static_cast<T*>(staging);
   p.dlogits = static_cast<T*>(bw.dlogits);
   p.T_len = a.P + a.C;
   p.P = a.P;
@@ -493,12 +543,18 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
 
   const size_t smem = (size_t)kStages * kStageBytes +
                       (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
-  auto kern = lse_grad_kernel<T, K>;
-  static bool attr_set[2][4] = {};
-  bool& done = attr_set[sizeof(T) == 4 ? 0 : 1][K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
+  // the grid (and so the loss's summation order) is that of the device-memory
+  // kernel in both modes
+  auto kern = lse_grad_kernel<T, K, false>;
+  auto kern_launch = staging != nullptr ? lse_grad_kernel<T, K, true> : kern;
+  static bool attr_set[2][2][4] = {};
+  bool& done = attr_set[staging != nullptr ? 1 : 0][sizeof(T) == 4 ? 0 : 1]
+                       [K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
   if (!done) {
     const int max_smem = kStages * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern_launch, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     done = true;
   }
@@ -547,20 +603,21 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
     attr[0] = attr[1];
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern_launch, p);
 }
 
 template <typename T>
-cudaError_t launch_t(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d, cudaStream_t st) {
+cudaError_t launch_t(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d, cudaStream_t st,
+                     void* staging) {
   switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_FUSED_CLUSTER", 2)) {
     case 8:
-      return launch_k<T, 8>(a, b, d, st);
+      return launch_k<T, 8>(a, b, d, st, staging);
     case 4:
-      return launch_k<T, 4>(a, b, d, st);
+      return launch_k<T, 4>(a, b, d, st, staging);
     case 2:
-      return launch_k<T, 2>(a, b, d, st);
+      return launch_k<T, 2>(a, b, d, st, staging);
     default:
-      return launch_k<T, 1>(a, b, d, st);
+      return launch_k<T, 1>(a, b, d, st, staging);
   }
 }
 
@@ -569,7 +626,15 @@ cudaError_t launch_t(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d, cu
 cudaError_t launch_lse_grad(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d,
                             cudaStream_t st) {
   if (a.N == 0 || a.C == 0) return cudaSuccess;
-  return a.dtype == 0 ? launch_t<float>(a, b, d, st) : launch_t<uint16_t>(a, b, d, st);
+  return a.dtype == 0 ? launch_t<float>(a, b, d, st, nullptr)
+                      : launch_t<uint16_t>(a, b, d, st, nullptr);
+}
+
+cudaError_t launch_lse_grad_host(const FwdArgs& a, const BwdArgs& b, void* staging,
+                                 const DeviceInfo& d, cudaStream_t st) {
+  if (a.N == 0 || a.C == 0) return cudaSuccess;
+  return a.dtype == 0 ? launch_t<float>(a, b, d, st, staging)
+                      : launch_t<uint16_t>(a, b, d, st, staging);
 }
 
 }  // namespace grpo
