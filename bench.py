@@ -584,6 +584,15 @@ def run_ours(args, w0: wl.Workload):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds)
+        # the same oracle on one core, for the record (a shorter sample)
+        import oracle
+        n_threads = oracle.threads()
+        oracle.set_threads(1)
+        try:
+            one = time_oracle(w, max(1.0, args.cpu_seconds / 4), rows_per_call=8)
+        finally:
+            oracle.set_threads(n_threads)
+        cpu["single_core"] = {"value": one["value"], "cores": 1, "sample": one["sample"]}
 
     if rank == 0:
         peaks = measured_peaks()

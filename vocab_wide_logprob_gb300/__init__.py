@@ -19,4 +19,7 @@ def __getattr__(name):
     if name in _NAMES:
         from . import _native
         return getattr(_native, name)
+    if name in ("GRPOLoss", "grpo_loss"):
+        from . import autograd
+        return getattr(autograd, name)
     raise AttributeError(name)
