@@ -27,6 +27,12 @@ int row_split(int64_t row_bytes, const char* env, int max_split) {
   return k;
 }
 
+int lse_split(int64_t row_bytes, int64_t rows_max, int sms, const char* env) {
+  int k = 1;
+  while (k < 8 && rows_max * k < 4 * (int64_t)sms) k *= 2;
+  return row_split(row_bytes, env, k);
+}
+
 int grid_mult(const char* env, int def) {
   if (const char* s = getenv(env)) {
     const int k = atoi(s);

@@ -417,6 +417,16 @@ struct Elt<uint16_t> {  // bfloat16 bit patterns
 // environment variable that may force 1, 2, 4 or 8.
 int row_split(int64_t row_bytes, const char* env, int max_split);
 
+// CTAs per scored row (a thread block cluster splitting the row over the
+// vocabulary) of the log-sum-exp kernels: 1 when the batch's N*C rows (an
+// upper bound of the scored rows) can occupy the GPU on their own, else the
+// smallest of 2, 4, 8 with rows * K >= 4 * SMs, as row_split allows.  Whole
+// rows per CTA measured faster on GB300 whenever there are enough of them
+// (no cluster barrier per row); the split keeps small batches from idling
+// most SMs.  Both kernels use this rule, so they split a row the same way
+// and their results have the same bits.
+int lse_split(int64_t row_bytes, int64_t rows_max, int sms, const char* env);
+
 // CTAs per SM of an oversubscribed streaming grid: `def`, or the positive
 // integer in environment variable `env`.
 int grid_mult(const char* env, int def);

@@ -9,8 +9,8 @@
 // "The loss" and "loss.backward()" of "Making Dr GRPO go brrr",
 // salahadawi.com, composed for one row at a time).
 //
-// Work layout: the forward's persistent clusters of K CTAs (split-V) and its
-// bulk-copy ring.  For each row a CTA streams its slice twice through the
+// Work layout: the forward's persistent clusters of K CTAs (split-V, K from
+// lse_split as for the forward) and its bulk-copy ring.  For each row a CTA streams its slice twice through the
 // ring: pass 1 from HBM (kept in L2 with an evict-last hint) for (max, sum,
 // target logit); the K partials are exchanged all-to-all through distributed
 // shared memory and a cluster barrier, so every CTA merges them in rank order
@@ -609,7 +609,7 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
 template <typename T>
 cudaError_t launch_t(const FwdArgs& a, const BwdArgs& b, const DeviceInfo& d, cudaStream_t st,
                      void* staging) {
-  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_FUSED_CLUSTER", 2)) {
+  switch (lse_split(a.V * (int64_t)sizeof(T), a.N * a.C, d.sms, "GRPO_FUSED_CLUSTER")) {
     case 8:
       return launch_k<T, 8>(a, b, d, st, staging);
     case 4:

@@ -9,10 +9,12 @@
 // same loads.  Rows past the first EOS are not read at all.
 //
 // Layout of the work: each valid row is split over the K CTAs of a thread
-// block cluster (split-V).  CTA k streams its 1/K of the row with 16-byte
-// loads, reduces its (max, sum) over its 256 threads, and sends the partial
-// to CTA 0 of the cluster through distributed shared memory; CTA 0 merges
-// the K partials in rank order (deterministic) and writes logp and lse.
+// block cluster (split-V; K from lse_split: 1, whole rows per CTA, unless the
+// batch has too few rows to occupy the GPU).  CTA k streams its 1/K of the
+// row with 16-byte loads, reduces its (max, sum) over its 256 threads, and
+// sends the partial to CTA 0 of the cluster through distributed shared
+// memory; CTA 0 merges the K partials in rank order (deterministic) and
+// writes logp and lse.
 // The grid is persistent: as many clusters as fit on the GPU at once, each
 // looping over valid rows r = cluster, cluster + #clusters, ... The row of
 // valid token r is found by binary search in the prefix sums of the lengths
@@ -540,9 +542,7 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
 
 template <typename T>
 cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
-  // pairs of CTAs measured fastest: larger clusters couple more CTAs at every
-  // row's barrier (4: -20%, 8: -50% on the batched workload)
-  switch (row_split(a.V * (int64_t)sizeof(T), "GRPO_LSE_CLUSTER", 2)) {
+  switch (lse_split(a.V * (int64_t)sizeof(T), a.N * a.C, d.sms, "GRPO_LSE_CLUSTER")) {
     case 8:
       return launch_k<T, 8>(a, d, st);
     case 4:
