@@ -538,7 +538,7 @@ def run_ours(args, w0: wl.Workload):
         t.numel() * t.element_size() for t in (h_ids, h_R, h_old, h_ref) if t is not None)
     e2e_out = {}
 
-    def e2e_step():
+    def e2e_enqueue():
         ids.copy_(h_ids, non_blocking=True)
         R.copy_(h_R, non_blocking=True)
         if old is not None:
@@ -551,28 +551,52 @@ def run_ours(args, w0: wl.Workload):
                                                 w.beta, 0.0, None, e2e_out.get("o"), ws,
                                                 dlogits, staging=logits)
         h_loss.copy_(e2e_out["o"]["loss"], non_blocking=True)
+
+    def e2e_step():
+        e2e_enqueue()
         stream.synchronize()
 
-    for _ in range(2):
-        e2e_step()
     n_e2e = max(1, min(args.e2e_steps, args.steps))
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_el = e0.elapsed_time(e1) / 1e3
+
+    def time_e2e(step_fn):
+        for _ in range(2):
+            step_fn()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            step_fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    e2e_eager_el = time_e2e(e2e_step)
+    # The same calls captured once into a CUDA graph and replayed each step
+    # (one launch instead of the copies and kernels one by one; the host
+    # still reads the loss back every step).
+    e2e_graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_enqueue()
+
+        def e2e_graph_step():
+            graph.replay()
+            stream.synchronize()
+
+        e2e_graph = time_e2e(e2e_graph_step)
+    except Exception as ex:  # capture refused: keep the eager number
+        print(f"e2e graph capture failed: {ex!r}", file=sys.stderr)
+    e2e_el = e2e_eager_el if e2e_graph is None else e2e_graph
 
     # aggregate over ranks: units of all ranks / max time
     if world > 1:
-        t = torch.tensor([elapsed, e2e_el], device=dev)
+        t = torch.tensor([elapsed, e2e_el, e2e_eager_el], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, e2e_el = float(t[0]), float(t[1])
+        elapsed, e2e_el, e2e_eager_el = float(t[0]), float(t[1]), float(t[2])
         tv = torch.tensor([t_valid], device=dev, dtype=torch.int64)
         dist.all_reduce(tv)
         t_valid_all = int(tv.item())
@@ -638,7 +662,9 @@ def run_ours(args, w0: wl.Workload):
             "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
                     "path": "grpo_mask + grpo_advantage + grpo_loss_fwd_bwd_host (logits in "
-                            "pinned host memory; only the scored rows cross the link)"},
+                            "pinned host memory; only the scored rows cross the link)",
+                    "cuda_graph": e2e_graph is not None,
+                    "eager_value": t_valid_all * n_e2e / e2e_eager_el},
             "copy_ceiling_gbs": copy_gbs,
             "other_path": None if alt is None else dict(
                 alt, logits_roofline_frac=alt["logits_gbs"] / peak),
