@@ -85,3 +85,29 @@ def test_full_size_orders_same_bits():
     logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
     wl.fill_logits_cuda(w, logits)
     _check(w, logits)
+
+
+def test_no_scored_rows():
+    """Every length 0: no CTA has a scored row, so only CTA 0 waits on the
+    forward (before it exits); every element is written +0 either way."""
+    n = H.g()
+    w = wl.variant(wl.TINY, name="order_len0", dtype="bf16", V=3000)
+    logits = wl.make_logits_cpu(w).cuda()
+    ids = torch.from_numpy(wl.make_ids(w)).cuda()
+    lens = torch.zeros((w.N,), dtype=torch.int32, device="cuda")
+    adv = n.grpo_advantage(torch.from_numpy(wl.make_rewards(w)).cuda(), w.G)
+    d = torch.full_like(logits, float("nan"))
+    out = n.grpo_loss_fwd(logits, w.P, ids, lens, adv)
+    n.grpo_loss_bwd(logits, w.P, ids, lens, out["lse"], out["w"], None, d)
+    assert n.grpo_check_error(out["workspace"]) == 0
+    torch.cuda.synchronize()
+    assert not bool((_bits(d) != 0).any())
+    assert float(out["loss"].item()) == 0.0
+
+
+@pytest.mark.parametrize("B", [256, 257], ids=["N1024_reordered", "N1028_memory_order"])
+def test_prefix_table_boundary(B):
+    """1,024 completions (the largest batch the reordered walk covers) and
+    1,028 (memory order): same bits both ways, every element written."""
+    w = wl.variant(wl.TINY, name=f"order_B{B}", B=B, G=4, P=2, C=3, V=64)
+    _check(w, wl.make_logits_cpu(w).cuda())
