@@ -427,6 +427,20 @@ grpo_status grpo_lmhead_loss_bwd_ex(const void *hidden, const void *weight, int6
 grpo_status grpo_check_error(const void *workspace, grpo_stream_t stream);
 
 /*
+ * grpo_selftest_timeout -- diagnostic of the kernels' bounded waits.  Every
+ * wait of the library's kernels on a shared-memory barrier gives up after
+ * one second, records GRPO_ERR_TIMEOUT in the workspace and lets the kernel
+ * finish instead of hanging.  This call launches one CTA that waits on a
+ * barrier nothing completes: about one second later the kernel has recorded
+ * the timeout in `workspace` (any workspace of grpo_workspace_size bytes,
+ * 256-byte aligned; only its error flags are touched) and exited, so
+ * grpo_check_error(workspace) returns GRPO_ERR_TIMEOUT and the stream and
+ * context stay usable.  Reset the flags (any loss forward on the workspace
+ * does) before reusing the workspace for error checks.
+ */
+grpo_status grpo_selftest_timeout(void *workspace, grpo_stream_t stream);
+
+/*
  * grpo_copy -- dst[0 .. bytes) = src[0 .. bytes) with 16-byte vector loads and
  * streaming stores: the device-to-device copy ceiling the HBM roofline of the
  * other kernels is compared with.  Both pointers 16-byte aligned, bytes a

@@ -52,6 +52,7 @@ def _load():
                            P], INT),
         "grpo_loss_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, P], INT),
         "grpo_check_error": ([P, P], INT),
+        "grpo_selftest_timeout": ([P, P], INT),
         "grpo_copy": ([P, P, SZ, P], INT),
         "grpo_loss_fwd_static": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
                                   P], INT),
@@ -487,6 +488,15 @@ def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=N
     else:
         _check(_lib.grpo_lmhead_loss_bwd_ex(*head, int(flags), *tail), "grpo_lmhead_loss_bwd_ex")
     return out[0], out[1], workspace
+
+
+def grpo_selftest_timeout(workspace, stream=None) -> None:
+    """Launches the bounded-wait self-test on ``workspace`` (a uint8 device
+    tensor of at least 16 bytes, 256-byte aligned): about a second later its
+    error flags hold a timeout, which grpo_check_error reports as
+    GRPO_ERR_TIMEOUT (8)."""
+    _dev(workspace, "workspace")
+    _check(_lib.grpo_selftest_timeout(_ptr(workspace), _stream(stream)), "grpo_selftest_timeout")
 
 
 def grpo_check_error(workspace, stream=None) -> int:

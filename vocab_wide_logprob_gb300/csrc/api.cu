@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "lmhead.cuh"
 #include "host_rows.cuh"
+#include "selftest.cuh"
 #include "grpo.h"
 
 namespace grpo {
@@ -762,6 +763,13 @@ grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
   if (flags & kFlagLengthRange) return GRPO_ERR_LENGTH_RANGE;
   if (flags & kFlagTimeout) return GRPO_ERR_TIMEOUT;
   return GRPO_OK;
+}
+
+grpo_status grpo_selftest_timeout(void* workspace, grpo_stream_t stream) {
+  if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return GRPO_ERR_MISALIGNED;
+  stream_take_after_fwd(stream);
+  return from_cuda(launch_selftest_timeout(workspace, (cudaStream_t)stream));
 }
 
 grpo_status grpo_copy(void* dst, const void* src, size_t bytes, grpo_stream_t stream) {
