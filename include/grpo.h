@@ -109,6 +109,12 @@ grpo_status grpo_mask(const int64_t *input_ids, int64_t N, int64_t P, int64_t C,
  * rewards [B*G] float32, grouped as [B, G]; adv [B*G] float32 out:
  * adv_i = R_i - (sum of the group's rewards) / G, in float32.  For binary
  * rewards and power-of-two G every step is exact.  B >= 0, G >= 1.
+ *
+ * Stream order: when the library's previous call on this stream (and device)
+ * was grpo_mask, the advantages are computed while that call's kernel may
+ * still run (it writes only mask and len); rewards and adv must not overlap
+ * that call's input_ids, mask or len.  The same holds for grpo_advantage_ex
+ * without n_contrast.
  */
 grpo_status grpo_advantage(const float *rewards, int64_t B, int64_t G, float *adv,
                            grpo_stream_t stream);

@@ -4,8 +4,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <map>
 #include <mutex>
-#include <set>
 #include <utility>
 
 #include "common.cuh"
@@ -64,17 +64,19 @@ cudaError_t current_device(DeviceInfo* d) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// What the library enqueued last on a stream.  The backward may write the
-// rows that score nothing before waiting on the preceding kernel only when
-// that kernel is the loss forward's (whose kernels write neither the lengths
-// nor dlogits), so every entry point that enqueues work calls
-// stream_take_after_fwd() first, and a successful loss forward then calls
-// stream_mark_after_fwd().  The set holds the (device, stream) pairs whose
-// last library call was the loss forward.  Calls from several host threads
-// on one stream are ordered as their launches are only if the caller orders
-// them.
+// What the library enqueued last on a stream.  Two launches may touch memory
+// before waiting on the kernel before them, when the host knows that kernel:
+// the backward, right after the loss forward (whose kernels write neither the
+// lengths nor dlogits), writes the rows that score nothing; the advantage,
+// right after the mask (which writes only the mask and lengths), computes its
+// groups.  So every entry point that enqueues work calls stream_take_last()
+// first, and a successful loss forward or mask call records itself.  The map
+// holds the (device, stream) pairs whose last library call was one of those
+// two.  Calls from several host threads on one stream are ordered as their
+// launches are only if the caller orders them.
+enum LastCall { kLastOther = 0, kLastLossFwd = 1, kLastMask = 2 };
 std::mutex g_order_mutex;
-std::set<std::pair<int, cudaStream_t>> g_after_fwd;
+std::map<std::pair<int, cudaStream_t>, int> g_last_call;
 
 std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
   int dev = -1;
@@ -82,18 +84,24 @@ std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
   return {dev, st};
 }
 
-// Whether the library's last call on `st` was the loss forward; forgets it.
-bool stream_take_after_fwd(cudaStream_t st) {
+// The library's last call on `st` (a LastCall); forgets it.
+int stream_take_last(cudaStream_t st) {
   const auto key = order_key(st);
   std::lock_guard<std::mutex> lk(g_order_mutex);
-  return g_after_fwd.erase(key) != 0;
+  const auto it = g_last_call.find(key);
+  if (it == g_last_call.end()) return kLastOther;
+  const int last = it->second;
+  g_last_call.erase(it);
+  return last;
 }
+bool stream_take_after_fwd(cudaStream_t st) { return stream_take_last(st) == kLastLossFwd; }
 
-void stream_mark_after_fwd(cudaStream_t st) {
+void stream_mark_last(cudaStream_t st, int last) {
   const auto key = order_key(st);
   std::lock_guard<std::mutex> lk(g_order_mutex);
-  g_after_fwd.insert(key);
+  g_last_call[key] = last;
 }
+void stream_mark_after_fwd(cudaStream_t st) { stream_mark_last(st, kLastLossFwd); }
 
 // a*b*c without int64 overflow, or -1
 int64_t mul3(int64_t a, int64_t b, int64_t c) {
@@ -155,8 +163,10 @@ grpo_status grpo_mask(const int64_t* input_ids, int64_t N, int64_t P, int64_t C,
   if (len == nullptr || (C > 0 && input_ids == nullptr)) return GRPO_ERR_INVALID_ARG;
   if (mul3(N, P + C, 8) < 0 || C > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(input_ids, 8) || !aligned(len, 4)) return GRPO_ERR_MISALIGNED;
-  stream_take_after_fwd(stream);
-  return from_cuda(launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream));
+  stream_take_last(stream);
+  const cudaError_t e = launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream);
+  if (e == cudaSuccess) stream_mark_last(stream, kLastMask);
+  return from_cuda(e);
 }
 
 grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* adv,
@@ -166,8 +176,9 @@ grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* ad
   if (rewards == nullptr || adv == nullptr) return GRPO_ERR_INVALID_ARG;
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4)) return GRPO_ERR_MISALIGNED;
-  stream_take_after_fwd(stream);
-  return from_cuda(launch_advantage(rewards, B, G, 0, 0.f, adv, nullptr, (cudaStream_t)stream));
+  const bool after_mask = stream_take_last(stream) == kLastMask;
+  return from_cuda(
+      launch_advantage(rewards, B, G, 0, 0.f, adv, nullptr, (cudaStream_t)stream, after_mask));
 }
 
 grpo_status grpo_advantage_ex(const float* rewards, int64_t B, int64_t G, grpo_adv_mode mode,
@@ -180,9 +191,9 @@ grpo_status grpo_advantage_ex(const float* rewards, int64_t B, int64_t G, grpo_a
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4) || !aligned(n_contrast, 4))
     return GRPO_ERR_MISALIGNED;
-  stream_take_after_fwd(stream);
+  const bool after_mask = stream_take_last(stream) == kLastMask;
   return from_cuda(launch_advantage(rewards, B, G, (int)mode, std_eps, adv, n_contrast,
-                                    (cudaStream_t)stream));
+                                    (cudaStream_t)stream, after_mask));
 }
 
 grpo_status grpo_workspace_size(int64_t N, int64_t C, int64_t V, size_t* bytes) {

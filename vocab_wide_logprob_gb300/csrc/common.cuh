@@ -464,7 +464,8 @@ struct DeviceInfo {
 cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int64_t eos,
                         uint8_t* mask, int32_t* len, cudaStream_t st);
 cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, int mode, float std_eps,
-                             float* adv, int32_t* n_contrast, cudaStream_t st);
+                             float* adv, int32_t* n_contrast, cudaStream_t st,
+                             bool after_mask);
 
 struct FwdArgs {
   const void* logits;

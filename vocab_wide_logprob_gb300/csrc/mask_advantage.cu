@@ -60,13 +60,9 @@ cudaError_t launch_mask(const int64_t* ids, int64_t N, int64_t P, int64_t C, int
 //   mode 1 (original GRPO): A = (R - mu) / (sigma + std_eps), sigma over the G
 //                           rewards (dividing by G), IEEE sqrt and division
 // n_contrast (optional) counts the groups whose rewards are not all equal.
-__global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __restrict__ R,
-                                                             int64_t B, int64_t G, int mode,
-                                                             float std_eps,
-                                                             float* __restrict__ adv,
-                                                             int32_t* __restrict__ n_contrast) {
-  pdl_wait();
-  pdl_trigger();
+__device__ __forceinline__ void advantage_group(const float* __restrict__ R, int64_t B, int64_t G,
+                                                int mode, float std_eps, float* __restrict__ adv,
+                                                int32_t* __restrict__ n_contrast) {
   const int64_t b = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -92,16 +88,33 @@ __global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __rest
   }
 }
 
+// after_mask: the preceding kernel is grpo_mask's, which reads the ids and
+// writes the mask and lengths only (everything before it has completed), so
+// the rewards and advantages are touched without waiting on it; thread 0 of
+// CTA 0 waits before it exits, so this kernel still completes after it.
+__global__ void __launch_bounds__(kThreads) advantage_kernel(const float* __restrict__ R,
+                                                             int64_t B, int64_t G, int mode,
+                                                             float std_eps,
+                                                             float* __restrict__ adv,
+                                                             int32_t* __restrict__ n_contrast,
+                                                             int after_mask) {
+  if (!after_mask) pdl_wait();
+  pdl_trigger();
+  advantage_group(R, B, G, mode, std_eps, adv, n_contrast);
+  if (after_mask && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
+}
+
 cudaError_t launch_advantage(const float* R, int64_t B, int64_t G, int mode, float std_eps,
-                             float* adv, int32_t* n_contrast, cudaStream_t st) {
+                             float* adv, int32_t* n_contrast, cudaStream_t st, bool after_mask) {
   if (B == 0) return n_contrast ? cudaMemsetAsync(n_contrast, 0, sizeof(int32_t), st) : cudaSuccess;
   if (n_contrast != nullptr) {
     cudaError_t e = cudaMemsetAsync(n_contrast, 0, sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
+    after_mask = false;  // the memset now comes between the two kernels
   }
   const unsigned blocks = (unsigned)((B + kWarps - 1) / kWarps);
   return launch_pdl(advantage_kernel, dim3(blocks), dim3(kThreads), 0, st, 1, R, B, G, mode,
-                    std_eps, adv, n_contrast);
+                    std_eps, adv, n_contrast, after_mask ? 1 : 0);
 }
 
 }  // namespace grpo
