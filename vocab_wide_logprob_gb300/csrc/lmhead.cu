@@ -9,16 +9,17 @@
 //   gather_rows_kernel   copies the hidden state of every scored row into a
 //                        dense [rows, d] buffer (row r = valid token r) and
 //                        zeroes the rows up to the next multiple of 256
+//                        (and zeroes logp and lse past each length)
 //   lmhead_lse_kernel    work items (block of 256 rows, range of vocabulary
 //                        tiles of 256) on the pair pipeline (pair_pipeline.cuh):
 //                        each CTA loads 128 rows of H and 128 vocabulary rows
 //                        of W per 64-wide k-step; the epilogue folds each
 //                        finished 256-column tile of its 128 rows into a
 //                        running (max, sum of exp) and the target logit.  Each
-//                        item writes one partial per row.
-//   lmhead_merge_kernel  merges a row's partials in order (deterministic) into
-//                        lse and logp = z_y - lse, and zeroes positions past
-//                        each length.
+//                        item writes one partial per row and counts it; the
+//                        thread that writes a row's last partial merges the
+//                        row's partials in split order (deterministic) into lse
+//                        and logp = z_y - lse.
 //
 // The backward ("loss.backward()" through the projection) recomputes the
 // logits with the same pipeline: lmhead_dz_kernel's epilogue turns each tile
@@ -46,6 +47,9 @@ struct LmParams {
   const int32_t* offsets;  // prefix sums of the clamped lengths ([N+1])
   int4* geometry;          // [0] (row blocks, splits, tiles per split): written by the gather
   float4* partials;        // forward: [items][256] (max, sum, target logit, has target)
+  uint32_t* counters;      // forward: partials written per row (zeroed by the gather)
+  float* logp_out;         // forward: [N, C]
+  float* lse_out;          // forward: [N, C]
   WsHeader* hdr;
   // logits-gradient pass only
   const float* lse;        // [N, C] from the forward
@@ -103,7 +107,10 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
                                                                const int32_t* __restrict__ off,
                                                                int64_t N, int64_t T, int64_t P,
                                                                int64_t d, int64_t V, int pairs,
-                                                               int4* __restrict__ geometry) {
+                                                               int4* __restrict__ geometry,
+                                                               uint32_t* __restrict__ counters,
+                                                               float* __restrict__ logp,
+                                                               float* __restrict__ lse) {
   pdl_wait();
   pdl_trigger();
   const int64_t tv = off[N];
@@ -135,6 +142,21 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(const uint16_t* _
     }
     reinterpret_cast<uint4*>(dense + r * d)[c] = v;
   }
+  // the log-sum-exp kernel counts each row's partials from 0; positions past
+  // each length are 0 in logp and lse
+  const int64_t C = T - P;
+  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < N * C;
+       k += (int64_t)gridDim.x * kThreads) {
+    if (k < rows_pad) counters[k] = 0u;
+    const int64_t i = k / C;
+    if (k - i * C >= off[i + 1] - off[i]) {
+      logp[k] = 0.f;
+      lse[k] = 0.f;
+    }
+  }
+  for (int64_t k = N * C + (int64_t)blockIdx.x * kThreads + threadIdx.x; k < rows_pad;
+       k += (int64_t)gridDim.x * kThreads)
+    counters[k] = 0u;
 }
 
 // ---- backward rows ------------------------------------------------------------------
@@ -271,6 +293,7 @@ struct LmOp {
   int64_t r, y;
   float lse_r, coef, g, m, s_extra, zy;
   uint64_t acc01, acc23;
+  int64_t tok;  // forward: the token i*C + t of this thread's row (-1: a padding row)
   bool has;
   uint32_t chunk;
 
@@ -314,6 +337,7 @@ struct LmOp {
     const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
     r = (it / splits) * kRows + rank * 128 + quarter * 32 + lane;
     y = -1;
+    tok = -1;
     lse_r = 0.f;
     coef = 0.f;
     if (r < tv) {
@@ -327,6 +351,7 @@ struct LmOp {
         t = r - p.offsets[i];
       }
       y = __ldg(ids + i * (p.P + p.C) + p.P + t);
+      tok = i * p.C + t;
       if (kMode == 1) {
         lse_r = __ldg(p.lse + i * p.C + t);
         coef = g * __ldg(p.w + i * p.C + t);
@@ -446,9 +471,41 @@ struct LmOp {
       f2_unpack(acc01, a0, a1);
       f2_unpack(acc23, a2, a3);
       const float s = ((a0 + a1) + (a2 + a3)) + s_extra;
-      if (r < tv)
-        p.partials[it * kRows + rank * 128 + quarter * 32 + lane] =
-            make_float4(m, s, zy, has ? 1.f : 0.f);
+      if (r < tv) {
+        const int64_t rr = rank * 128 + quarter * 32 + lane;  // the row within its block
+        p.partials[it * kRows + rr] = make_float4(m, s, zy, has ? 1.f : 0.f);
+        // The thread that writes a row's last partial merges the row: every
+        // writer makes its partial visible before counting it, the last one
+        // sees every count and so every partial.
+        __threadfence();
+        if (atomicAdd(p.counters + r, 1u) == (uint32_t)(splits - 1)) {
+          __threadfence();
+          merge_row(it / splits, rr);
+        }
+      }
+    }
+  }
+  // Partials of row (block rb, row rr) in split order -> lse, logp.
+  __device__ void merge_row(int64_t rb, int64_t rr) const {
+    float4 pk = __ldcg(p.partials + (rb * splits) * kRows + rr);
+    float cm = pk.x, cs = pk.y, z = pk.z;
+    bool found = pk.w != 0.f;
+    for (int64_t sp = 1; sp < splits; ++sp) {
+      pk = __ldcg(p.partials + (rb * splits + sp) * kRows + rr);
+      lse_merge(cm, cs, pk.x, pk.y);
+      if (pk.w != 0.f) {
+        z = pk.z;
+        found = true;
+      }
+    }
+    const float l = cm + logf(cs);
+    if (found) {
+      p.logp_out[tok] = z - l;
+      p.lse_out[tok] = l;
+    } else {  // the sampled id is outside [0, V)
+      p.logp_out[tok] = __int_as_float(0x7fc00000);
+      p.lse_out[tok] = __int_as_float(0x7fc00000);
+      atomicOr(&p.hdr->flags, kFlagTokenRange);
     }
   }
   __device__ void epi_finish() {
@@ -481,50 +538,6 @@ __global__ void __launch_bounds__(64 + 32 * LmOp<1>::kEpiWarps, 1)
                      const __grid_constant__ CUtensorMap map_dz, const int64_t* __restrict__ ids,
                      const LmParams p) {
   lm_kernel_body<1>(&map_h, &map_w, &map_dz, ids, p);
-}
-
-// ---- merge: partials of a row in split order -> lse, logp ----------------------
-
-__global__ void __launch_bounds__(kThreads) lmhead_merge_kernel(const LmParams p,
-                                                                const int64_t* __restrict__ ids,
-                                                                float* __restrict__ logp,
-                                                                float* __restrict__ lse,
-                                                                const int32_t* __restrict__ lens) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t splits = p.geometry->y;
-  const int64_t NC = p.N * p.C;
-  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < NC;
-       k += (int64_t)gridDim.x * kThreads) {
-    const int64_t i = k / p.C, t = k - i * p.C;
-    if (t >= lens[i]) {
-      logp[k] = 0.f;
-      lse[k] = 0.f;
-      continue;
-    }
-    const int64_t r = p.offsets[i] + t;
-    const int64_t rb = r / kRows, rr = r - rb * kRows;
-    float4 pk = p.partials[(rb * splits) * kRows + rr];
-    float cm = pk.x, cs = pk.y, z = pk.z;
-    bool has = pk.w != 0.f;
-    for (int64_t sp = 1; sp < splits; ++sp) {
-      pk = p.partials[(rb * splits + sp) * kRows + rr];
-      lse_merge(cm, cs, pk.x, pk.y);
-      if (pk.w != 0.f) {
-        z = pk.z;
-        has = true;
-      }
-    }
-    const float l = cm + logf(cs);
-    if (has) {
-      logp[k] = z - l;
-      lse[k] = l;
-    } else {  // the sampled id is outside [0, V)
-      logp[k] = __int_as_float(0x7fc00000);
-      lse[k] = __int_as_float(0x7fc00000);
-      atomicOr(&p.hdr->flags, kFlagTokenRange);
-    }
-  }
 }
 
 // ---- host side --------------------------------------------------------------------
@@ -630,7 +643,8 @@ LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms) {
   l.dense = align_up(base.total + 32, 1024);
   l.partials = align_up(l.dense + (size_t)(mb_max * kRows) * (size_t)d * 2, 256);
   const int64_t items_max = 4 * pairs + 2 * mb_max;  // mb * splits bound
-  l.total = align_up(l.partials + (size_t)items_max * kRows * sizeof(float4), 256);
+  l.counters = align_up(l.partials + (size_t)items_max * kRows * sizeof(float4), 256);
+  l.total = align_up(l.counters + (size_t)(mb_max * kRows) * sizeof(uint32_t), 256);
   return l;
 }
 
@@ -664,26 +678,24 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   const int pairs = lm_pairs(dev);
 
   int4* geometry = reinterpret_cast<int4*>(ws + ll.geometry);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + ll.counters);
   cudaError_t e = launch_pdl(gather_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
                              st, 1, static_cast<const uint16_t*>(hidden), dense, off, a.N,
-                             a.P + a.C, a.P, d, a.V, pairs, geometry);
+                             a.P + a.C, a.P, d, a.V, pairs, geometry, counters, a.logp, a.lse);
   if (e != cudaSuccess) return e;
 
   LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, d);
   p.partials = reinterpret_cast<float4*>(ws + ll.partials);
+  p.counters = counters;
+  p.logp_out = a.logp;
+  p.lse_out = a.lse;
   CUtensorMap map_h, map_w;
   if ((e = encode_bf16_2d(&map_h, dense, d, rows, d, 128)) != cudaSuccess) return e;
   if ((e = encode_bf16_2d(&map_w, weight, d, a.V, d, 128)) != cudaSuccess) return e;
   static bool attr_done = false;
   if ((e = set_smem((const void*)lmhead_lse_kernel, kLmSmem, &attr_done)) != cudaSuccess) return e;
-  if ((e = launch_pdl(lmhead_lse_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
-                      (size_t)kLmSmem, st, 2, map_h, map_w, a.ids, p)) != cudaSuccess)
-    return e;
-  int64_t blocks = (a.N * a.C + kThreads - 1) / kThreads;
-  if (blocks > 1024) blocks = 1024;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(lmhead_merge_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1, p,
-                    a.ids, a.logp, a.lse, reinterpret_cast<const int32_t*>(ws + wl.lens));
+  return launch_pdl(lmhead_lse_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
+                    (size_t)kLmSmem, st, 2, map_h, map_w, a.ids, p);
 }
 
 cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {

@@ -13,10 +13,12 @@ struct LmLayout {
   size_t geometry;  // int4: row blocks, vocabulary splits, tiles per split
   size_t dense;     // bf16 [N*C rounded up to 256, d]
   size_t partials;  // float4 [items][256]
+  size_t counters;  // uint32 [N*C rounded up to 256]: partials written per row
   size_t total;
 };
 LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms);
-// After launch_prep: gather, tensor-core log-sum-exp, merge.
+// After launch_prep: gather, then the tensor-core log-sum-exp (whose last
+// partial of a row merges the row).
 cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs& a, int64_t d,
                           const DeviceInfo& dev, cudaStream_t st);
 
