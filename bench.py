@@ -43,6 +43,7 @@ METRIC = "completion tokens/s and logits GB/s (% of HBM roofline), Dr.GRPO loss 
 UNIT = "completion tokens/s"
 KERNELS_PER_STEP = 6  # mask, advantage, prep, lse_gather, surrogate, dlogits (fused: 5)
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300's nominal HBM3e bandwidth, for context only
 
 
 def parse_args():
@@ -140,6 +141,74 @@ def recorded_traffic(kernel: str, w: wl.Workload, hidden: int | None = None):
             or rec.get("hidden") != hidden):
         return None
     return rec["dram_bytes_per_launch"]
+
+
+def cpu_model() -> str | None:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
+
+
+def run_env(dev) -> dict:
+    """What produced the numbers: GPU, driver, toolkit, torch, and a hash of
+    the library's sources (the GPU machine gets the tree without its git history)."""
+    import torch
+    env = {"gpu": torch.cuda.get_device_name(dev), "torch": torch.__version__,
+           "cuda_runtime": torch.version.cuda, "driver": None, "nvcc": None}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        env["driver"] = out.splitlines()[0] if out else None
+    except (OSError, subprocess.SubprocessError, IndexError):
+        pass
+    try:
+        out = subprocess.run(["nvcc", "--version"], capture_output=True, text=True,
+                             timeout=20).stdout
+        env["nvcc"] = next((l.split("release", 1)[1].strip() for l in out.splitlines()
+                            if "release" in l), None)
+    except (OSError, subprocess.SubprocessError):
+        pass
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "vocab_wide_logprob_gb300", "csrc", "*"))
+                       + glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
+            h.update(f.read())
+    env["sources_sha256"] = h.hexdigest()[:16]
+    return env
+
+
+def input_record(w: wl.Workload, ids_np, R_np, logits) -> dict:
+    """Seed and fingerprints of the step's inputs, and the workload's
+    statistics (truncated completions, groups with reward contrast)."""
+    import torch
+    bits = logits.view(torch.int16 if logits.element_size() == 2 else torch.int32)
+    # order-sensitive device checksum of the logits: sum of value * (index mod a prime)
+    chk = 0
+    rows = bits.reshape(-1, bits.shape[-1])
+    weights = (torch.arange(bits.shape[-1], device=bits.device, dtype=torch.int64) % 1000003) + 1
+    for r0 in range(0, rows.shape[0], 1024):
+        part = rows[r0:r0 + 1024].to(torch.int64)
+        chk = (chk + int(((part * weights).sum(dim=1) % 2147483647
+                          * ((torch.arange(r0, r0 + part.shape[0], device=bits.device) % 65521)
+                             + 1)).sum().item())) % 2147483647
+    comp = ids_np[:, w.P:]
+    truncated = float(np.mean(~np.any(comp == w.eos_id, axis=1))) if w.C > 0 else 0.0
+    Rg = R_np.reshape(w.B, w.G)
+    return {"seed": w.seed, "ids_sha256": hashlib.sha256(ids_np.tobytes()).hexdigest()[:16],
+            "rewards_sha256": hashlib.sha256(R_np.tobytes()).hexdigest()[:16],
+            "logits_checksum": chk, "truncated_fraction": truncated,
+            "groups_without_contrast": int(np.sum(Rg.max(axis=1) == Rg.min(axis=1)))}
 
 
 def copy_ceiling(g, dev, nbytes: int = 4 << 30, reps: int = 10) -> float:
@@ -627,6 +696,7 @@ def run_ours(args, w0: wl.Workload):
         finally:
             oracle.set_threads(n_threads)
         cpu["single_core"] = {"value": one["value"], "cores": 1, "sample": one["sample"]}
+        cpu["cpu_model"] = cpu_model()
 
     if rank == 0:
         peaks = measured_peaks()
@@ -682,6 +752,9 @@ def run_ours(args, w0: wl.Workload):
             "cpu_baseline": cpu,
             "clocks": clocks,
             "loss": loss_val,
+            "logits_nominal_frac": step_bytes / ms / 1e9 / NOMINAL_HBM_GBS,
+            "inputs": input_record(w, ids_np, R_np, logits),
+            "env": run_env(dev),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -791,16 +864,20 @@ def run_lmhead(args, w: wl.Workload):
                    "l2": "weights larger than L2 (%.2f GB); no flush" % (w.V * d * 2 / 1e9)},
         "roofline": {"kernel": ("lmhead fwd + bwd (projection, recomputed projection, "
                                 "dhidden and dweight contractions)") if train else
-                               "lmhead_lse_kernel (+ gather, merge)",
+                               "lmhead_lse_kernel (+ gather)",
                      "bound": "tensor", "achieved": tflops, "peak": peak,
                      "peak_source": "measured" if peaks.get("bf16_tflops") else "fallback",
                      "unit": "TFLOP/s", "frac": tflops / peak, "flops_per_step": flops,
                      "traffic": recorded_traffic("lmhead_fwd_bwd" if train else
                                                  "lmhead_lse_kernel", w, d)},
-        "gpu_launches": (13 if train else 5) * args.steps, "clocks": clocks,
+        # per step: mask, prep, gather, log-sum-exp (+ advantage, surrogate, and
+        # the backward's prep, row scan, gather, logits-gradient, dhidden,
+        # dweight and reduce kernels)
+        "gpu_launches": (13 if train else 4) * args.steps, "clocks": clocks,
         "cpu_baseline": None if args.no_cpu_baseline else
         time_oracle_lmhead(w, d, args.cpu_seconds, train),
     }
+    line["env"] = run_env(torch.device("cuda", 0))
     if train:
         line["kernel_ms"] = {"fwd": ms_fwd, "bwd": ms_bwd}
         line["fwd_tflops"] = unit_flops / (ms_fwd * 1e-3) / 1e12
