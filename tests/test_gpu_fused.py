@@ -184,3 +184,28 @@ def test_host_logits_refuses_pageable_memory():
                                     p(dev.data_ptr()), p(dev.data_ptr()), p(dl.data_ptr()),
                                     p(st.data_ptr()), p(ws.data_ptr()), ws.numel(), None)
     assert rc == 1  # GRPO_ERR_INVALID_ARG
+
+
+def test_host_logits_full_size_same_bits():
+    """The benchmark workload (V = 151,936, whole rows per CTA) with the logits
+    in pinned host memory: the gradient kernel reads the scored rows from host
+    memory itself, and every output has the bits of the device-memory path."""
+    n = H.g()
+    w = H.with_contrast(wl.QWEN_G8)
+    logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    wl.fill_logits_cuda(w, logits)
+    t_ids = torch.from_numpy(wl.make_ids(w)).cuda()
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(torch.from_numpy(wl.make_rewards(w)).cuda(), w.G)
+    a = n.grpo_loss_fwd_bwd(logits, w.P, t_ids, lens, adv, None, None, 0.2, 0.0)
+    host = logits.cpu().pin_memory()
+    staging = torch.empty_like(logits)
+    b = n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, None, None, 0.2, 0.0,
+                                 staging=staging)
+    torch.cuda.synchronize()
+    assert n.grpo_check_error(b["workspace"]) == 0
+    for k in ("logp", "lse", "w", "loss"):
+        assert torch.equal(_bits(a[k]), _bits(b[k])), k
+    assert torch.equal(_bits(a["dlogits"]), _bits(b["dlogits"]))
+    del logits, staging, host, a, b
+    torch.cuda.empty_cache()
