@@ -9,19 +9,22 @@
 // "The loss" and "loss.backward()" of "Making Dr GRPO go brrr",
 // salahadawi.com, composed for one row at a time).
 //
-// Work layout: the forward's persistent clusters of K CTAs (split-V, K from
-// lse_split as for the forward) and its bulk-copy ring.  For each row a CTA streams its slice twice through the
-// ring: pass 1 from HBM (kept in L2 with an evict-last hint) for (max, sum,
-// target logit); the K partials are exchanged all-to-all through distributed
-// shared memory and a cluster barrier, so every CTA merges them in rank order
-// into the same lse and w; pass 2 re-reads the slice (an L2 hit: the slices
-// in flight on the whole GPU total a few tens of MB) and writes the gradient.
-// Rows that score nothing are written with zeros by a separate store-only
-// kernel launched after this one, which runs beside it (its CTAs take the
-// slots this persistent grid leaves free and do not wait on it).  Per element the arithmetic is that of lse_gather_kernel and
-// dlogits_kernel, and the per-token terms are token_terms(), so logp, lse, w
-// and dlogits have the same bits as the unfused path; only the loss's
-// summation order differs (per cluster, then clusters in order).
+// Work layout: the forward's persistent grid, rows split over clusters of K
+// CTAs as lse_split decides for the forward (K = 1, whole rows per CTA, unless
+// the batch is small), and its bulk-copy ring.  For each row a CTA streams its
+// row (slice) twice through the ring: pass 1 from HBM (kept in L2 with an
+// evict-last hint) for (max, sum, target logit); with K > 1 the partials are
+// exchanged all-to-all through distributed shared memory and a cluster
+// barrier, so every CTA merges them in rank order into the same lse and w;
+// pass 2 re-reads the row from L2 where it is still there (whole rows keep
+// ~90 MB live over the grid, so part of it comes from HBM again) and writes
+// the gradient.  Rows that score nothing are written with zeros by a separate
+// store-only kernel launched after this one, which runs beside it (its CTAs
+// take the slots this persistent grid leaves free and do not wait on it).
+// Per element the arithmetic is that of lse_gather_kernel and dlogits_kernel,
+// and the per-token terms are token_terms(), so logp, lse, w and dlogits have
+// the same bits as the unfused path; only the loss's summation order differs
+// (per cluster, then clusters in order).
 #include <stdlib.h>
 
 #include <map>
