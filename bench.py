@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -76,7 +77,8 @@ def parse_args():
 
 
 # --------------------------------------------------------------------------
-# byte counts (stated in the design doc)
+# algorithmic byte counts: two reads of the scored rows + one write of
+# dlogits (the method's count), and the fused path's one read + one write
 # --------------------------------------------------------------------------
 
 def algorithmic_bytes(w: wl.Workload, t_valid: int, t_read_bwd: int | None = None) -> dict:
@@ -245,7 +247,7 @@ class ClockSampler:
 
     def __init__(self, gpu_id: str | None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"grpo_bench_clocks_{os.getpid()}.csv")
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                "-lms", "100"]
         if gpu_id:
