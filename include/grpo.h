@@ -111,10 +111,11 @@ grpo_status grpo_mask(const int64_t *input_ids, int64_t N, int64_t P, int64_t C,
  * rewards and power-of-two G every step is exact.  B >= 0, G >= 1.
  *
  * Stream order: when the library's previous call on this stream (and device)
- * was grpo_mask, the advantages are computed while that call's kernel may
- * still run (it writes only mask and len); rewards and adv must not overlap
- * that call's input_ids, mask or len.  The same holds for grpo_advantage_ex
- * without n_contrast.
+ * was grpo_mask and rewards and adv are disjoint from that call's mask and
+ * len (adv also from its input_ids; the library checks the address ranges),
+ * the advantages are computed while that call's kernel may still run;
+ * otherwise the call waits for it as usual.  The same holds for
+ * grpo_advantage_ex without n_contrast.
  */
 grpo_status grpo_advantage(const float *rewards, int64_t B, int64_t G, float *adv,
                            grpo_stream_t stream);
@@ -251,13 +252,12 @@ grpo_status grpo_logprobs(const void *logits, grpo_dtype dtype, int64_t N, int64
  * not overlap logits.  Lengths are clamped to [0, C].
  *
  * Stream order: when the library's previous call on this stream (and
- * device) was grpo_loss_fwd or grpo_loss_fwd_ex, the rows that score nothing
- * are written while that forward's last kernels may still run (they depend
- * only on len).  The usual contract of a stream-ordered call covers it: len
- * and dlogits must not be written, and dlogits must not be read, by that
- * forward call (its outputs, workspace and inputs must not overlap dlogits
- * or len).  Any other preceding work is complete before this call touches
- * memory.
+ * device) was grpo_loss_fwd or grpo_loss_fwd_ex, and dlogits overlaps none of
+ * that call's buffers and len none of the buffers it writes (the library
+ * keeps their address ranges and checks), the rows that score nothing are
+ * written while that forward's last kernels may still run (they depend only
+ * on len); otherwise, and after any other preceding work, the call waits for
+ * it as usual.  Either way the results are those of stream order.
  */
 grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
                           int64_t V, const int64_t *input_ids, const int32_t *len,

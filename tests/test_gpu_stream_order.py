@@ -111,3 +111,36 @@ def test_prefix_table_boundary(B):
     1,028 (memory order): same bits both ways, every element written."""
     w = wl.variant(wl.TINY, name=f"order_B{B}", B=B, G=4, P=2, C=3, V=64)
     _check(w, wl.make_logits_cpu(w).cuda())
+
+
+def test_overlapping_buffers_wait_first():
+    """dlogits carved from the same allocation as the forward's workspace (its
+    first prompt rows, rows that score nothing, cover the workspace): in
+    stream order the backward overwrites the workspace only after the forward
+    is done with it.  The library sees the overlap and waits first, so the
+    loss and dlogits equal those of separate buffers bit for bit."""
+    n = H.g()
+    w = H.with_contrast(wl.variant(wl.TINY, name="order_overlap", dtype="bf16", V=3000))
+    logits = wl.make_logits_cpu(w).cuda()
+    ids = torch.from_numpy(wl.make_ids(w)).cuda()
+    R = torch.from_numpy(wl.make_rewards(w)).cuda()
+    _, lens = n.grpo_mask(ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(R, w.G)
+    ref = n.grpo_loss_fwd(logits, w.P, ids, lens, adv, None, None, w.eps, 0.0)
+    d_ref = n.grpo_loss_bwd(logits, w.P, ids, lens, ref["lse"], ref["w"], None)
+    torch.cuda.synchronize()
+
+    need = n.grpo_workspace_size(w.N, w.C, w.V)
+    dl_bytes = logits.numel() * logits.element_size()
+    # the workspace lies within sequence 0's prompt rows, which score nothing
+    assert need <= (w.P - 1) * w.V * logits.element_size()
+    buf = torch.full((dl_bytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    dl = buf.view(torch.bfloat16).view(logits.shape)
+    ws = buf[:need]
+    out = n.grpo_loss_fwd(logits, w.P, ids, lens, adv, None, None, w.eps, 0.0, workspace=ws)
+    n.grpo_loss_bwd(logits, w.P, ids, lens, out["lse"], out["w"], None, dl)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(ref["loss"]), _bits(out["loss"]))
+    for k in ("logp", "lse", "w"):
+        assert torch.equal(_bits(ref[k]), _bits(out[k])), k
+    assert torch.equal(_bits(d_ref), _bits(dl))

@@ -64,19 +64,47 @@ cudaError_t current_device(DeviceInfo* d) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// What the library enqueued last on a stream.  Two launches may touch memory
-// before waiting on the kernel before them, when the host knows that kernel:
-// the backward, right after the loss forward (whose kernels write neither the
-// lengths nor dlogits), writes the rows that score nothing; the advantage,
-// right after the mask (which writes only the mask and lengths), computes its
-// groups.  So every entry point that enqueues work calls stream_take_last()
-// first, and a successful loss forward or mask call records itself.  The map
-// holds the (device, stream) pairs whose last library call was one of those
-// two.  Calls from several host threads on one stream are ordered as their
-// launches are only if the caller orders them.
+// What the library enqueued last on a stream, and which memory it touches.
+// Two launches may touch memory before waiting on the kernel before them,
+// when the host knows that kernel: the backward, right after the loss
+// forward, writes the rows that score nothing (it reads only the lengths and
+// writes only dlogits before its wait); the advantage, right after the mask,
+// computes its groups (it reads the rewards and writes the advantages).  Each
+// may do so only when its own buffers are disjoint from those of the call
+// before it (what that call writes must not be read or written, what it
+// reads must not be written); otherwise it waits first as every launch does.
+// So every entry point that enqueues work calls stream_take_last() first, and
+// a successful loss forward or mask call records itself and its buffers.
+// Calls from several host threads on one stream are ordered as their launches
+// are only if the caller orders them.
 enum LastCall { kLastOther = 0, kLastLossFwd = 1, kLastMask = 2 };
+
+struct Span {  // [lo, hi) in the process's (unified) address space
+  uintptr_t lo = 0, hi = 0;
+};
+Span span(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return p == nullptr ? Span{} : Span{a, a + bytes};
+}
+struct CallRecord {
+  int kind = kLastOther;
+  Span writes[5];
+  Span reads[6];
+};
+bool overlaps(const Span* set, int n, Span x) {
+  if (x.lo == x.hi) return false;
+  for (int k = 0; k < n; ++k)
+    if (set[k].lo < x.hi && x.lo < set[k].hi) return true;
+  return false;
+}
+// Whether a launch that writes `w` and reads `r` before its wait may follow
+// the recorded call without waiting on it.
+bool disjoint_from(const CallRecord& c, Span w, Span r) {
+  return !overlaps(c.writes, 5, w) && !overlaps(c.reads, 6, w) && !overlaps(c.writes, 5, r);
+}
+
 std::mutex g_order_mutex;
-std::map<std::pair<int, cudaStream_t>, int> g_last_call;
+std::map<std::pair<int, cudaStream_t>, CallRecord> g_last_call;
 
 std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
   int dev = -1;
@@ -84,24 +112,23 @@ std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
   return {dev, st};
 }
 
-// The library's last call on `st` (a LastCall); forgets it.
-int stream_take_last(cudaStream_t st) {
+// The library's last call on `st` (kind kLastOther if not recorded); forgets it.
+CallRecord stream_take_last(cudaStream_t st) {
   const auto key = order_key(st);
   std::lock_guard<std::mutex> lk(g_order_mutex);
   const auto it = g_last_call.find(key);
-  if (it == g_last_call.end()) return kLastOther;
-  const int last = it->second;
+  if (it == g_last_call.end()) return CallRecord{};
+  const CallRecord last = it->second;
   g_last_call.erase(it);
   return last;
 }
-bool stream_take_after_fwd(cudaStream_t st) { return stream_take_last(st) == kLastLossFwd; }
+void stream_take_after_fwd(cudaStream_t st) { (void)stream_take_last(st); }
 
-void stream_mark_last(cudaStream_t st, int last) {
+void stream_mark_last(cudaStream_t st, const CallRecord& rec) {
   const auto key = order_key(st);
   std::lock_guard<std::mutex> lk(g_order_mutex);
-  g_last_call[key] = last;
+  g_last_call[key] = rec;
 }
-void stream_mark_after_fwd(cudaStream_t st) { stream_mark_last(st, kLastLossFwd); }
 
 // a*b*c without int64 overflow, or -1
 int64_t mul3(int64_t a, int64_t b, int64_t c) {
@@ -165,7 +192,14 @@ grpo_status grpo_mask(const int64_t* input_ids, int64_t N, int64_t P, int64_t C,
   if (!aligned(input_ids, 8) || !aligned(len, 4)) return GRPO_ERR_MISALIGNED;
   stream_take_last(stream);
   const cudaError_t e = launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream);
-  if (e == cudaSuccess) stream_mark_last(stream, kLastMask);
+  if (e == cudaSuccess) {
+    CallRecord rec;
+    rec.kind = kLastMask;
+    rec.writes[0] = span(mask, (size_t)(N * C));
+    rec.writes[1] = span(len, sizeof(int32_t) * (size_t)N);
+    rec.reads[0] = span(input_ids, sizeof(int64_t) * (size_t)(N * (P + C)));
+    stream_mark_last(stream, rec);
+  }
   return from_cuda(e);
 }
 
@@ -176,7 +210,10 @@ grpo_status grpo_advantage(const float* rewards, int64_t B, int64_t G, float* ad
   if (rewards == nullptr || adv == nullptr) return GRPO_ERR_INVALID_ARG;
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4)) return GRPO_ERR_MISALIGNED;
-  const bool after_mask = stream_take_last(stream) == kLastMask;
+  const CallRecord last = stream_take_last(stream);
+  const bool after_mask =
+      last.kind == kLastMask && disjoint_from(last, span(adv, sizeof(float) * (size_t)(B * G)),
+                                              span(rewards, sizeof(float) * (size_t)(B * G)));
   return from_cuda(
       launch_advantage(rewards, B, G, 0, 0.f, adv, nullptr, (cudaStream_t)stream, after_mask));
 }
@@ -191,7 +228,10 @@ grpo_status grpo_advantage_ex(const float* rewards, int64_t B, int64_t G, grpo_a
   if (mul3(B, G, 4) < 0 || B > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(rewards, 4) || !aligned(adv, 4) || !aligned(n_contrast, 4))
     return GRPO_ERR_MISALIGNED;
-  const bool after_mask = stream_take_last(stream) == kLastMask;
+  const CallRecord last = stream_take_last(stream);
+  const bool after_mask =
+      last.kind == kLastMask && disjoint_from(last, span(adv, sizeof(float) * (size_t)(B * G)),
+                                              span(rewards, sizeof(float) * (size_t)(B * G)));
   return from_cuda(launch_advantage(rewards, B, G, (int)mode, std_eps, adv, n_contrast,
                                     (cudaStream_t)stream, after_mask));
 }
@@ -267,7 +307,21 @@ grpo_status loss_fwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64
   if ((e = launch_lse_gather(a, d, st)) != cudaSuccess) return GRPO_ERR_CUDA;
   if (mode == 1) return from_cuda(launch_mask_fill(a, st));
   if ((e = launch_surrogate(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
-  stream_mark_after_fwd(st);
+  CallRecord rec;
+  rec.kind = kLastLossFwd;
+  const size_t nc4 = sizeof(float) * (size_t)(N * C);
+  rec.writes[0] = span(logp, nc4);
+  rec.writes[1] = span(lse, nc4);
+  rec.writes[2] = span(w, nc4);
+  rec.writes[3] = span(loss, sizeof(float));
+  rec.writes[4] = span(workspace, workspace_bytes);
+  rec.reads[0] = span(logits, (size_t)mul3(N, P + C, V) * (dtype == GRPO_F32 ? 4 : 2));
+  rec.reads[1] = span(input_ids, sizeof(int64_t) * (size_t)(N * (P + C)));
+  rec.reads[2] = span(len, sizeof(int32_t) * (size_t)N);
+  rec.reads[3] = span(adv, sizeof(float) * (size_t)N);
+  rec.reads[4] = span(old_logp, nc4);
+  rec.reads[5] = span(a.ref_logp, nc4);
+  stream_mark_last(st, rec);
   return GRPO_OK;
 }
 
@@ -341,7 +395,12 @@ grpo_status grpo_loss_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N, in
   a.skip_zero_weight = (flags & GRPO_BWD_SKIP_ZERO_WEIGHT) != 0;
   DeviceInfo d;
   if (current_device(&d) != cudaSuccess) return GRPO_ERR_CUDA;
-  a.after_fwd = stream_take_after_fwd(stream);
+  {
+    // before its wait the backward writes dlogits (zero rows) and reads len
+    const CallRecord last = stream_take_last(stream);
+    a.after_fwd = last.kind == kLastLossFwd &&
+                  disjoint_from(last, span(dlogits, bytes), span(len, sizeof(int32_t) * (size_t)N));
+  }
   return from_cuda(launch_dlogits(a, d, (cudaStream_t)stream));
 }
 
