@@ -257,7 +257,8 @@ grpo_status grpo_logprobs(const void *logits, grpo_dtype dtype, int64_t N, int64
  * keeps their address ranges and checks), the rows that score nothing are
  * written while that forward's last kernels may still run (they depend only
  * on len); otherwise, and after any other preceding work, the call waits for
- * it as usual.  Either way the results are those of stream order.
+ * it as usual.  Either way the results are those of stream order (see
+ * grpo_set_early_start for kernels of other code in between).
  */
 grpo_status grpo_loss_bwd(const void *logits, grpo_dtype dtype, int64_t N, int64_t P, int64_t C,
                           int64_t V, const int64_t *input_ids, const int32_t *len,
@@ -445,6 +446,18 @@ grpo_status grpo_check_error(const void *workspace, grpo_stream_t stream);
  * does) before reusing the workspace for error checks.
  */
 grpo_status grpo_selftest_timeout(void *workspace, grpo_stream_t stream);
+
+/*
+ * grpo_set_early_start -- the two early starts (grpo_loss_bwd right after
+ * grpo_loss_fwd, grpo_advantage right after grpo_mask; see those calls) are
+ * on by default (enable != 0) and can be turned off process-wide (0).  The
+ * library checks its own two calls' buffers, but it cannot see other code's
+ * launches: a kernel enqueued between the two calls that itself lets its
+ * successor start early (programmatic dependent launch) and reads dlogits or
+ * writes len (or the advantage call's buffers) needs them off.  Kernels
+ * launched the ordinary way are complete before either call touches memory.
+ */
+void grpo_set_early_start(int enable);
 
 /*
  * grpo_copy -- dst[0 .. bytes) = src[0 .. bytes) with 16-byte vector loads and

@@ -144,3 +144,31 @@ def test_overlapping_buffers_wait_first():
     for k in ("logp", "lse", "w"):
         assert torch.equal(_bits(ref[k]), _bits(out[k])), k
     assert torch.equal(_bits(d_ref), _bits(dl))
+
+
+def test_early_starts_can_be_turned_off():
+    """grpo_set_early_start(False): the backward and the advantage wait first
+    like every launch; the results keep their bits."""
+    n = H.g()
+    w = H.with_contrast(wl.variant(wl.TINY, name="order_off", dtype="bf16", V=3000))
+    logits = wl.make_logits_cpu(w).cuda()
+
+    def run():
+        ids = torch.from_numpy(wl.make_ids(w)).cuda()
+        _, lens = n.grpo_mask(ids, w.P, w.C, w.eos_id)
+        adv = n.grpo_advantage(torch.from_numpy(wl.make_rewards(w)).cuda(), w.G)
+        out = n.grpo_loss_fwd(logits, w.P, ids, lens, adv)
+        dl = n.grpo_loss_bwd(logits, w.P, ids, lens, out["lse"], out["w"])
+        torch.cuda.synchronize()
+        return adv, out, dl
+
+    adv1, out1, dl1 = run()
+    n.grpo_set_early_start(False)
+    try:
+        adv2, out2, dl2 = run()
+    finally:
+        n.grpo_set_early_start(True)
+    assert torch.equal(adv1, adv2)
+    for k in ("logp", "lse", "w", "loss"):
+        assert torch.equal(_bits(out1[k]), _bits(out2[k])), k
+    assert torch.equal(_bits(dl1), _bits(dl2))

@@ -12,7 +12,7 @@ _NAMES = ("grpo_mask", "grpo_advantage", "grpo_advantage_ex", "grpo_workspace_si
           "grpo_loss_bwd_ex", "grpo_loss_fwd_bwd", "grpo_loss_fwd_bwd_ex", "grpo_loss_fwd_bwd_host",
           "grpo_loss_fwd_static",
           "grpo_lmhead_logprobs", "grpo_lmhead_loss_fwd", "grpo_lmhead_loss_bwd",
-          "grpo_check_error", "grpo_selftest_timeout", "grpo_copy", "GrpoError")
+          "grpo_check_error", "grpo_selftest_timeout", "grpo_set_early_start", "grpo_copy", "GrpoError")
 
 
 def __getattr__(name):

@@ -53,6 +53,7 @@ def _load():
         "grpo_loss_bwd": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, P, P], INT),
         "grpo_check_error": ([P, P], INT),
         "grpo_selftest_timeout": ([P, P], INT),
+        "grpo_set_early_start": ([ctypes.c_int], None),
         "grpo_copy": ([P, P, SZ, P], INT),
         "grpo_loss_fwd_static": ([P, INT, I64, I64, I64, I64, P, P, P, P, P, F, F, F, P, P, P, P,
                                   P], INT),
@@ -488,6 +489,12 @@ def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=N
     else:
         _check(_lib.grpo_lmhead_loss_bwd_ex(*head, int(flags), *tail), "grpo_lmhead_loss_bwd_ex")
     return out[0], out[1], workspace
+
+
+def grpo_set_early_start(enable: bool) -> None:
+    """Turns the early starts of grpo_loss_bwd (after grpo_loss_fwd) and
+    grpo_advantage (after grpo_mask) on or off for the process."""
+    _lib.grpo_set_early_start(1 if enable else 0)
 
 
 def grpo_selftest_timeout(workspace, stream=None) -> None:

@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -112,7 +113,11 @@ std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
   return {dev, st};
 }
 
-// The library's last call on `st` (kind kLastOther if not recorded); forgets it.
+// grpo_set_early_start(0) turns the two early starts off process-wide.
+std::atomic<int> g_early_start{1};
+
+// The library's last call on `st` (kind kLastOther if not recorded, or if
+// early starts are off); forgets it.
 CallRecord stream_take_last(cudaStream_t st) {
   const auto key = order_key(st);
   std::lock_guard<std::mutex> lk(g_order_mutex);
@@ -120,7 +125,7 @@ CallRecord stream_take_last(cudaStream_t st) {
   if (it == g_last_call.end()) return CallRecord{};
   const CallRecord last = it->second;
   g_last_call.erase(it);
-  return last;
+  return g_early_start.load() ? last : CallRecord{};
 }
 void stream_take_after_fwd(cudaStream_t st) { (void)stream_take_last(st); }
 
@@ -834,6 +839,8 @@ grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {
   if (flags & kFlagTimeout) return GRPO_ERR_TIMEOUT;
   return GRPO_OK;
 }
+
+void grpo_set_early_start(int enable) { g_early_start.store(enable != 0 ? 1 : 0); }
 
 grpo_status grpo_selftest_timeout(void* workspace, grpo_stream_t stream) {
   if (workspace == nullptr) return GRPO_ERR_INVALID_ARG;
