@@ -17,8 +17,9 @@
 // exchanged all-to-all through distributed shared memory and a cluster
 // barrier, so every CTA merges them in rank order into the same lse and w;
 // pass 2 re-reads the row from L2 where it is still there (whole rows keep
-// ~90 MB live over the grid, so part of it comes from HBM again) and writes
-// the gradient.  Rows that score nothing are written with zeros by a separate
+// ~90 MB live over the grid, so part of it comes from HBM again), last chunk
+// first (the most recently loaded lines are the likeliest to be in L2), and
+// writes the gradient.  Rows that score nothing are written with zeros by a separate
 // store-only kernel launched after this one, which runs beside it (its CTAs
 // take the slots this persistent grid leaves free and do not wait on it).
 // Per element the arithmetic is that of lse_gather_kernel and dlogits_kernel,
@@ -214,10 +215,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
               *(volatile int*)&s_abort = 1;
               break;
             }
-            const uint32_t nb = min((uint32_t)kStageBytes, bytes - (uint32_t)c * kStageBytes);
+            const int cc = pass == 0 ? c : nchunks - 1 - c;
+            const uint32_t nb = min((uint32_t)kStageBytes, bytes - (uint32_t)cc * kStageBytes);
             const uint32_t full = smem_u32(&s_full[stage]);
             mbar_arrive_expect_tx(full, nb);
-            bulk_g2s_hint(ring + stage * kStageBytes, src + (size_t)c * kStageBytes, nb, full,
+            bulk_g2s_hint(ring + stage * kStageBytes, src + (size_t)cc * kStageBytes, nb, full,
                           pass == 0 ? pol_keep : pol_drop);
             ++issued;
             if (++stage == kStages) {
@@ -428,7 +430,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
 
     // ---------------- consumers: pass 2 (the gradient) ------------------
     uint4* ovp = reinterpret_cast<uint4*>(orow + a);
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c2 = 0; c2 < nchunks; ++c2) {
+      const int c = nchunks - 1 - c2;  // the chunks most recently read in pass 1 first
       bool ok = !*(volatile int*)&s_abort;
       if (!kHost && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
         atomicOr(&p.hdr->flags, kFlagTimeout);
