@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, dl_min_blocks<T>()) dlogits_kernel(c
       L = s_pre[lo + 1] - s_pre[lo];
       const int64_t q = r - (i * p.T_len - s_pre[lo]);
       row = i * p.T_len + (q < p.P - 1 ? q : q + L);
-    } else {  // then the scored rows
-      const int64_t sr = r - (p.N * p.T_len - s_pre[p.N]);
+    } else {  // then the scored rows, last first: the forward read those most
+              // recently, so they are the likeliest to be still in L2
+      const int64_t sr = (int64_t)s_pre[p.N] - 1 - (r - (p.N * p.T_len - s_pre[p.N]));
       int lo = 0, hi = (int)p.N;
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
