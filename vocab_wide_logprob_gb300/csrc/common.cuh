@@ -491,8 +491,6 @@ inline double default_norm(const FwdArgs& a) {
 cudaError_t launch_prep(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st);
 cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st);
-// logp = lse = 0 past each length (the log-prob-only pass).
-cudaError_t launch_mask_fill(const FwdArgs& a, cudaStream_t st);
 
 struct BwdArgs {
   const void* logits;

@@ -106,6 +106,9 @@ struct LseParams {
   float* lse;
   WsHeader* hdr;
   int64_t chunk;  // elements of a row per CTA of the cluster (multiple of kPerVec)
+  // the log-probs-only call: this kernel also writes 0 to logp and lse past
+  // each length (the loss forward's surrogate kernel does that otherwise)
+  const int32_t* zero_past_len;  // clamped lengths, or nullptr
 };
 
 // Ring of shared-memory stages filled by bulk copies (TMA).
@@ -214,7 +217,7 @@ __device__ __forceinline__ void finalize_row(const P& p, const float4* part, int
 // three slots: slot r%3 is rewritten for row r+3 only after every thread has
 // passed the wait of row r+1, which CTA 0 reaches after merging row r.
 template <typename T, int K>
-__global__ void __launch_bounds__(kLseThreads) lse_gather_kernel(const LseParams<T> p) {
+__global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LseParams<T> p) {
   using E = Elt<T>;
   constexpr int EPV = E::kPerVec;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -444,6 +447,18 @@ __global__ void __launch_bounds__(kLseThreads) lse_gather_kernel(const LseParams
     cluster_wait();
     if (rank == 0 && tid == 0) finalize_row<K>(p, s_part[(it - 1) % 3], prev_i, prev_t);
   }
+  // after the rows, where little state is live (keeps the row loop's
+  // register count)
+  if (p.zero_past_len != nullptr) {  // positions past each length: 0
+    const int64_t nct = (int64_t)gridDim.x * kLseThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kLseThreads + tid; k < p.N * p.C; k += nct) {
+      const int64_t i = k / p.C;
+      if (k - i * p.C >= p.zero_past_len[i]) {
+        p.logp[k] = 0.f;
+        p.lse[k] = 0.f;
+      }
+    }
+  }
   // copies this CTA issued that no consumer waited for (only after a timeout)
   if (producer && lane == 0 && *(volatile int*)&s_abort) {
     for (uint32_t k = 0; k < kStages && k < issued; ++k) {
@@ -480,6 +495,8 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.lse = a.lse;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.chunk = ((a.V + K - 1) / K + EPV - 1) / EPV * EPV;
+  // no gradient weights requested: the log-probs-only call
+  p.zero_past_len = a.w == nullptr ? reinterpret_cast<const int32_t*>(ws + l.lens) : nullptr;
 
   const size_t smem = (size_t)kStages * kStageBytes +
                       (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
@@ -559,34 +576,6 @@ cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
 cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   if (a.N == 0 || a.C == 0) return cudaSuccess;
   return a.dtype == 0 ? launch_t<float>(a, d, st) : launch_t<uint16_t>(a, d, st);
-}
-
-// logp = lse = 0 at positions past each completion's (clamped) length.
-__global__ void __launch_bounds__(kThreads) mask_fill_kernel(const int32_t* __restrict__ lens,
-                                                             int64_t N, int64_t C,
-                                                             float* __restrict__ logp,
-                                                             float* __restrict__ lse) {
-  pdl_wait();
-  pdl_trigger();
-  for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < N * C;
-       k += (int64_t)gridDim.x * kThreads) {
-    const int64_t i = k / C;
-    if (k - i * C >= lens[i]) {
-      logp[k] = 0.f;
-      lse[k] = 0.f;
-    }
-  }
-}
-
-cudaError_t launch_mask_fill(const FwdArgs& a, cudaStream_t st) {
-  const int64_t NC = a.N * a.C;
-  if (NC == 0) return cudaSuccess;
-  const WsLayout l = ws_layout(a.N);
-  const char* ws = static_cast<const char*>(a.ws);
-  int64_t blocks = (NC + kThreads - 1) / kThreads;
-  if (blocks > 1024) blocks = 1024;
-  return launch_pdl(mask_fill_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, 1,
-                    reinterpret_cast<const int32_t*>(ws + l.lens), a.N, a.C, a.logp, a.lse);
 }
 
 }  // namespace grpo
