@@ -16,10 +16,11 @@
 // evict-last hint) for (max, sum, target logit); with K > 1 the partials are
 // exchanged all-to-all through distributed shared memory and a cluster
 // barrier, so every CTA merges them in rank order into the same lse and w;
-// pass 2 re-reads the row from L2 where it is still there (whole rows keep
-// ~90 MB live over the grid, so part of it comes from HBM again), last chunk
-// first (the most recently loaded lines are the likeliest to be in L2), and
-// writes the gradient.  Rows that score nothing are written with zeros by a separate
+// pass 2 writes the gradient, reading the row's first chunks from the
+// shared-memory slots pass 1 loaded them into, and the rest from L2 where it
+// is still there (whole rows keep ~90 MB live over the grid, so part of it
+// comes from HBM again), last chunk first (the most recently loaded lines are
+// the likeliest to be in L2).  Rows that score nothing are written with zeros by a separate
 // store-only kernel launched after this one, which runs beside it (its CTAs
 // take the slots this persistent grid leaves free and do not wait on it).
 // Per element the arithmetic is that of lse_gather_kernel and dlogits_kernel,
@@ -45,6 +46,12 @@ constexpr int kFusedThreads = kConsumers + 32;
 constexpr int kVecPerStage = kStageBytes / 16;
 constexpr int kVecPerThread = kVecPerStage / kConsumers;
 constexpr int kSmemOffsets = 4096;
+// Chunks at the head of each row (slice) that pass 1 loads into slots of
+// their own and pass 2 reads from there, not from L2: with whole rows per CTA
+// the head of a row is the part likeliest to have left L2 by pass 2.  As many
+// slots as leave two CTAs per SM (keep_slots): four with a small offsets
+// table (N < 128), three up to the largest one.
+constexpr int kKeepMax = 4;
 
 template <typename T>
 struct FusedParams {
@@ -68,6 +75,7 @@ struct FusedParams {
   WsHeader* hdr;
   double* partials;        // one per cluster
   int64_t chunk;
+  int nkeep;               // head chunks held in shared memory (0 .. kKeepMax; 0 with kHost)
 };
 
 __device__ __forceinline__ int locate_row(const int32_t* off, int64_t N, int64_t r) {
@@ -116,6 +124,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t s_full[kStages];
   __shared__ __align__(8) uint64_t s_empty[kStages];
+  __shared__ __align__(8) uint64_t s_kfull[kKeepMax];   // head slot loaded
+  __shared__ __align__(8) uint64_t s_kempty[kKeepMax];  // head slot read by pass 2
   __shared__ float4 s_part[2][K];  // every CTA: the K partials of a row
   __shared__ float2 s_red[kWarps];
   __shared__ float s_zy;
@@ -138,11 +148,16 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
       mbar_init(smem_u32(&s_full[k]), 1);
       mbar_init(smem_u32(&s_empty[k]), kWarps);
     }
+    for (int k = 0; k < kKeepMax; ++k) {
+      mbar_init(smem_u32(&s_kfull[k]), 1);
+      mbar_init(smem_u32(&s_kempty[k]), kWarps);
+    }
     mbar_init_fence();
   }
   pdl_wait();
   pdl_trigger();
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
+  const uint32_t keep = ring + kStages * kStageBytes;  // head slots
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + (kStages + p.nkeep) * kStageBytes);
   const int32_t* off = p.offsets;
   if (p.N + 1 <= kSmemOffsets) {
     for (int64_t k = tid; k <= p.N; k += kFusedThreads) s_off[k] = p.offsets[k];
@@ -160,6 +175,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0;
+  // bit k: parity of head slot k's current use (flipped once per row that uses it)
+  uint32_t kph = 0, kused = 0;
   double loss_acc = 0.0;  // rank 0, thread 0: sum of this cluster's ell
   const uint64_t pol_keep = l2_policy_evict_last();
   const uint64_t pol_drop = l2_policy_evict_first();
@@ -196,6 +213,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     }
     const uint32_t bytes = (uint32_t)(nvec * 16);
     const int nchunks = (int)((bytes + kStageBytes - 1) / kStageBytes);
+    const int nk = min(p.nkeep, nchunks);  // head chunks: slots, not the ring
+    const uint32_t kmask = (1u << nk) - 1u;
 
     if (producer && kHost) {  // one arrival per row, as the consumers'
       if (K > 1) {
@@ -210,12 +229,28 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
         if (lane == 0) {
           for (int c = 0; c < nchunks; ++c) {
             if (*(volatile int*)&s_abort) break;
+            if (c < nk) {  // a head chunk: its own slot in pass 1, nothing in pass 2
+              if (pass == 1) continue;
+              if (!mbar_wait(smem_u32(&s_kempty[c]), ((kph >> c) & 1u) ^ 1u)) {
+                atomicOr(&p.hdr->flags, kFlagTimeout);
+                *(volatile int*)&s_abort = 1;
+                break;
+              }
+              const uint32_t nb = min((uint32_t)kStageBytes, bytes - (uint32_t)c * kStageBytes);
+              const uint32_t full = smem_u32(&s_kfull[c]);
+              mbar_arrive_expect_tx(full, nb);
+              bulk_g2s_hint(keep + c * kStageBytes, src + (size_t)c * kStageBytes, nb, full,
+                            pol_drop);
+              kph ^= 1u << c;
+              kused |= 1u << c;
+              continue;
+            }
             if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u)) {
               atomicOr(&p.hdr->flags, kFlagTimeout);
               *(volatile int*)&s_abort = 1;
               break;
             }
-            const int cc = pass == 0 ? c : nchunks - 1 - c;
+            const int cc = pass == 0 ? c : nchunks - 1 - (c - nk);
             const uint32_t nb = min((uint32_t)kStageBytes, bytes - (uint32_t)cc * kStageBytes);
             const uint32_t full = smem_u32(&s_full[stage]);
             mbar_arrive_expect_tx(full, nb);
@@ -272,15 +307,18 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
     const uint4* hv = reinterpret_cast<const uint4*>(row + a);  // kHost: the host row
     uint4* sv = kHost ? reinterpret_cast<uint4*>(srow + a) : nullptr;
     for (int c = 0; c < nchunks; ++c) {
+      const bool head = c < nk;
       bool ok = !*(volatile int*)&s_abort;
-      if (!kHost && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+      if (!kHost && ok &&
+          !mbar_wait(head ? smem_u32(&s_kfull[c]) : smem_u32(&s_full[stage]),
+                     head ? (kph >> c) & 1u : phase)) {
         atomicOr(&p.hdr->flags, kFlagTimeout);
         *(volatile int*)&s_abort = 1;
         ok = false;
       }
       if (ok) {
         const int nv = (int)min((int64_t)kVecPerStage, nvec - (int64_t)c * kVecPerStage);
-        const uint32_t sbase = ring + stage * kStageBytes;
+        const uint32_t sbase = head ? keep + c * kStageBytes : ring + stage * kStageBytes;
         uint4 d[kVecPerThread];
         if constexpr (kHost) {
           const int64_t base = (int64_t)c * kVecPerStage;
@@ -309,7 +347,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
             if (u == uy) zy = E::extract(d[u], ey);
           found = true;
         }
-        if (!kHost) {
+        if (!kHost && !head) {  // head slots stay until pass 2
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
         }
@@ -335,7 +373,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
           }
         }
       }
-      if (++stage == kStages) {
+      if (!head && ++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -430,17 +468,20 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
 
     // ---------------- consumers: pass 2 (the gradient) ------------------
     uint4* ovp = reinterpret_cast<uint4*>(orow + a);
+    // the head chunks from their slots first (frees them for the next row's
+    // copies), then the others from L2, most recently read in pass 1 first
     for (int c2 = 0; c2 < nchunks; ++c2) {
-      const int c = nchunks - 1 - c2;  // the chunks most recently read in pass 1 first
+      const bool head = c2 < nk;
+      const int c = head ? c2 : nchunks - 1 - (c2 - nk);
       bool ok = !*(volatile int*)&s_abort;
-      if (!kHost && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+      if (!kHost && !head && ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
         atomicOr(&p.hdr->flags, kFlagTimeout);
         *(volatile int*)&s_abort = 1;
         ok = false;
       }
       if (ok) {
         const int nv = (int)min((int64_t)kVecPerStage, nvec - (int64_t)c * kVecPerStage);
-        const uint32_t sbase = ring + stage * kStageBytes;
+        const uint32_t sbase = head ? keep + c * kStageBytes : ring + stage * kStageBytes;
         uint4 d[kVecPerThread];
         if constexpr (kHost) {  // the vectors this thread wrote in pass 1
           const int64_t base = (int64_t)c * kVecPerStage;
@@ -456,7 +497,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
             if (k < nv) d[u] = ld_shared_v4(sbase + 16u * k);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+          if (lane == 0) mbar_arrive(head ? smem_u32(&s_kempty[c]) : smem_u32(&s_empty[stage]));
         }
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
@@ -475,11 +516,12 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
           st_stream(ovp + (int64_t)c * kVecPerStage + k, E::pack(ov));
         }
       }
-      if (++stage == kStages) {
+      if (!head && ++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
+    kph ^= kmask;
     if (e >= 0) {
       const float ov = e == y ? ngw * expm1f(xe - lse_t) : ngw * ex2(fmaf(xe, kLog2e, -lseL));
       E::store1(orow + e, ov);
@@ -492,6 +534,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
       const uint32_t n = issued - 1 - k;
       mbar_wait(smem_u32(&s_full[n % kStages]), (n / kStages) & 1u);
     }
+    for (int k = 0; k < kKeepMax; ++k)  // the last copy into each head slot used
+      if ((kused >> k) & 1u) mbar_wait(smem_u32(&s_kfull[k]), ((kph >> k) & 1u) ^ 1u);
   }
   // the loss: each cluster's sum, then the last cluster adds them in order
   if (rank == 0 && tid == 0) {
@@ -512,6 +556,45 @@ __global__ void __launch_bounds__(kFusedThreads, 2) lse_grad_kernel(const FusedP
 
 std::mutex g_occ_mutex;
 std::map<std::tuple<int, int, int, int>, int> g_occ;
+
+// Head slots per CTA: as many as fit beside the ring and the offsets table
+// (offs bytes) with two CTAs per SM (half the SM's shared memory, less the
+// per-block reservation and the kernel's static arrays), at most kKeepMax,
+// and at most GRPO_FUSED_KEEP when that is set.
+template <typename T, int K>
+cudaError_t keep_slots(int device, size_t offs, int* n) {
+  static std::map<int, long> avail;  // per device: dynamic bytes per CTA at two CTAs per SM
+  static const int cap = [] {
+    const char* v = getenv("GRPO_FUSED_KEEP");
+    if (v == nullptr || *v == 0) return kKeepMax;
+    const int k = atoi(v);
+    return k < 0 ? 0 : (k > kKeepMax ? kKeepMax : k);
+  }();
+  long bytes = -1;
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mutex);
+    auto it = avail.find(device);
+    if (it != avail.end()) bytes = it->second;
+  }
+  if (bytes < 0) {
+    int per_sm = 0, reserved = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                           device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, device);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, lse_grad_kernel<T, K, false>);
+    if (e != cudaSuccess) return e;
+    bytes = (long)per_sm / 2 - reserved - (long)fa.sharedSizeBytes;
+    std::lock_guard<std::mutex> lk(g_occ_mutex);
+    avail[device] = bytes;
+  }
+  long k = (bytes - (long)kStages * kStageBytes - (long)offs) / kStageBytes;
+  if (k < 0) k = 0;
+  if (k > cap) k = cap;
+  *n = (int)k;
+  return cudaSuccess;
+}
 
 // staging != nullptr: a.logits is the device mapping of host logits (kHost).
 template <typename T, int K>
@@ -546,9 +629,13 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.partials = reinterpret_cast<double*>(ws + l.partials);
   p.chunk = ((a.V + K - 1) / K + EPV - 1) / EPV * EPV;
+  const size_t offs = a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0;
+  int nkeep = 0;
+  if (cudaError_t e = keep_slots<T, K>(d.device, offs, &nkeep); e != cudaSuccess) return e;
+  p.nkeep = staging != nullptr ? 0 : nkeep;
 
-  const size_t smem = (size_t)kStages * kStageBytes +
-                      (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
+  const size_t smem_dev = (size_t)(kStages + nkeep) * kStageBytes + offs;
+  const size_t smem = (size_t)(kStages + p.nkeep) * kStageBytes + offs;
   // the grid (and so the loss's summation order) is that of the device-memory
   // kernel in both modes
   auto kern = lse_grad_kernel<T, K, false>;
@@ -557,7 +644,8 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   bool& done = attr_set[staging != nullptr ? 1 : 0][sizeof(T) == 4 ? 0 : 1]
                        [K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
   if (!done) {
-    const int max_smem = kStages * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
+    const int max_smem =
+        (kStages + kKeepMax) * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern_launch, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
@@ -573,12 +661,12 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kFusedThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = smem_dev;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = K > 1 ? 1 : 0;
   int clusters = 0;
-  const auto key = std::make_tuple(d.device, (int)sizeof(T), K, (int)smem);
+  const auto key = std::make_tuple(d.device, (int)sizeof(T), K, (int)smem_dev);
   {
     std::lock_guard<std::mutex> lk(g_occ_mutex);
     auto itc = g_occ.find(key);
@@ -591,7 +679,7 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
       e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
     } else {
       int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFusedThreads, smem_dev);
       clusters = per_sm * d.sms;
     }
     if (e != cudaSuccess) return e;
@@ -603,6 +691,7 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   const int64_t max_rows = a.N * a.C;
   const int64_t nq = clusters < max_rows ? clusters : max_rows;
   cfg.gridDim = dim3((unsigned)(nq * K));
+  cfg.dynamicSmemBytes = smem;
   if (K > 1) {
     cfg.numAttrs = 2;
   } else {
