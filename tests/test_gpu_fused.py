@@ -65,6 +65,31 @@ def test_fused_same_bits_as_two_calls(w):
     assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
 
 
+@pytest.mark.parametrize("B,C,V", [(50, 4, 50001), (1025, 1, 50000)],
+                         ids=["N200_three_head_slots", "N4100_offsets_in_memory"])
+def test_fused_head_slots_same_bits(B, C, V):
+    """The fused kernel holds each row's first chunks in shared-memory slots,
+    as many as fit beside its ring and offsets table with two CTAs per SM:
+    three at 200 completions, four again at 4,100 (the offsets table then
+    stays in global memory).  Whole rows per CTA (N*C above four rows per
+    SM), seven 16 KiB chunks a row, so the ring carries the rest; the
+    outputs have the bits of the two calls."""
+    w = H.with_contrast(wl.variant(wl.TINY, name=f"slots_N{4 * B}", B=B, G=4, P=1, C=C, V=V,
+                                   dtype="bf16", logit_std=3.0, seed=500 + B))
+    logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    wl.fill_logits_cuda(w, logits)
+    ids, R = wl.make_ids(w), wl.make_rewards(w)
+    a = H.run_gpu(w, logits, ids, R, None, None, grad=1.5, beta=0.0)
+    b = H.run_gpu(w, logits, ids, R, None, None, grad=1.5, beta=0.0, fused=True)
+    assert a["status"] == 0 and b["status"] == 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w.N * w.C >= 4 * sms and int(a["lens"].sum()) >= 2 * sms
+    for k in ("logp", "lse", "w", "dlogits"):
+        assert torch.equal(_bits(a[k]), _bits(b[k])), k
+    la, lb = float(a["loss"].item()), float(b["loss"].item())
+    assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
+
+
 def test_fused_scaled_gradient():
     w = wl.variant(wl.TINY, old_sigma=0.1, ref_sigma=0.1, beta=0.04)
     H.check_small(w, grad=float(w.N * w.C), fused=True)

@@ -309,7 +309,7 @@ grpo_status loss_fwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64
   if ((e = launch_prep(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
   if (N == 0 || C == 0)
     return mode == 0 ? from_cuda(cudaMemsetAsync(loss, 0, sizeof(float), st)) : GRPO_OK;
-  if ((e = launch_lse_gather(a, d, st)) != cudaSuccess) return GRPO_ERR_CUDA;
+  if ((e = launch_lse_gather(a, d, st, true)) != cudaSuccess) return GRPO_ERR_CUDA;
   if (mode == 1) return GRPO_OK;  // the log-sum-exp kernel zeroed the masked positions
   if ((e = launch_surrogate(a, st)) != cudaSuccess) return GRPO_ERR_CUDA;
   CallRecord rec;

@@ -174,12 +174,44 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // writes to be visible, so no ordering is lost, while the launch and the
 // shared-memory prologue overlap the previous kernel's tail.  pdl_trigger()
 // lets the next kernel start launching; it is issued once this kernel's
-// CTAs are all resident, so it cannot take their slots.  One exception:
+// CTAs are all resident, so it cannot take their slots.  Two exceptions:
 // the backward, launched right after the loss forward on the same stream,
-// writes the rows that score nothing before its wait (dlogits.cu).
+// writes the rows that score nothing before its wait (dlogits.cu); and the
+// loss forward's log-sum-exp kernel, launched right after prep (which waits
+// before it triggers, so every kernel before prep has completed when it
+// starts), reads the raw lengths and the logits before its wait, and waits
+// only before it touches what prep writes (the workspace header).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// off[0..N]: exclusive prefix sums of the lengths clamped to [0, C] (what
+// prep writes to the workspace), computed by every thread of one block into
+// shared memory (N below 2^31); s_warp holds one int per warp.
+static __device__ __noinline__ void block_clamped_offsets(const int32_t* __restrict__ len, int64_t N,
+                                                         int64_t C, int32_t* off, int32_t* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = (int)N, c = (int)min(C, (int64_t)INT32_MAX);
+  const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int k0 = min(tid * per, n), k1 = min(k0 + per, n);
+  int32_t own = 0;
+  for (int k = k0; k < k1; ++k) own += min(max(__ldg(len + k), 0), c);
+  int32_t x = own;  // inclusive scan within the warp
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int32_t run = x - own;
+  for (int k = 0; k < warp; ++k) run += s_warp[k];
+  if (tid == 0) off[0] = 0;
+  for (int k = k0; k < k1; ++k) {
+    run += min(max(__ldg(len + k), 0), c);
+    off[k + 1] = run;
+  }
+  __syncthreads();
 }
 
 // ---- packed float pairs (Blackwell f32x2 FMA/ADD/MUL: two lanes per
@@ -489,7 +521,10 @@ inline double default_norm(const FwdArgs& a) {
   return a.norm > 0.f ? (double)a.norm : (a.agg == 0 ? (double)a.N * (double)a.C : (double)a.N);
 }
 cudaError_t launch_prep(const FwdArgs& a, cudaStream_t st);
-cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st);
+// after_prep: launched directly after launch_prep on the same stream (the
+// kernel then reads the lengths and logits before its wait)
+cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st,
+                              bool after_prep);
 cudaError_t launch_surrogate(const FwdArgs& a, cudaStream_t st);
 
 struct BwdArgs {

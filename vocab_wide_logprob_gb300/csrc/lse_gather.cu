@@ -108,7 +108,11 @@ struct LseParams {
   int64_t chunk;  // elements of a row per CTA of the cluster (multiple of kPerVec)
   // the log-probs-only call: this kernel also writes 0 to logp and lse past
   // each length (the loss forward's surrogate kernel does that otherwise)
-  const int32_t* zero_past_len;  // clamped lengths, or nullptr
+  bool zero_past;
+  // launched right after prep with the offsets table in shared memory: the
+  // table is computed here from the raw lengths before waiting on prep
+  bool early;
+  const int32_t* len;  // raw lengths
 };
 
 // Ring of shared-memory stages filled by bulk copies (TMA).
@@ -203,6 +207,7 @@ __device__ __forceinline__ void finalize_row(const P& p, const float4* part, int
   } else {  // y outside [0, V): no CTA saw it
     p.logp[o] = __int_as_float(0x7fc00000);
     p.lse[o] = __int_as_float(0x7fc00000);
+    pdl_wait();  // prep has reset the header
     atomicOr(&p.hdr->flags, kFlagTokenRange);
   }
 }
@@ -228,6 +233,7 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
   __shared__ float s_zy[3];
   __shared__ int64_t s_found[3];       // row whose target logit this CTA picked up
   __shared__ int s_abort;              // a bounded wait gave up
+  __shared__ int32_t s_warp[kLseThreads / 32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool producer = warp == kWarps;
@@ -245,13 +251,22 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
     }
     mbar_init_fence();
   }
-  pdl_wait();  // the previous kernel's writes (offsets, ids) are visible from here
-  pdl_trigger();
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes);
   const int32_t* off = p.offsets;
-  if (p.N + 1 <= kSmemOffsets) {
-    for (int64_t k = tid; k <= p.N; k += kLseThreads) s_off[k] = p.offsets[k];
+  if (p.early) {
+    // every kernel before prep has completed (prep waits before it lets this
+    // kernel launch): lengths, ids and logits can be read now; the header
+    // prep resets is touched only after pdl_wait()
+    pdl_trigger();
+    block_clamped_offsets(p.len, p.N, p.C, s_off, s_warp);
     off = s_off;
+  } else {
+    pdl_wait();  // the previous kernel's writes (offsets, ids) are visible from here
+    pdl_trigger();
+    if (p.N + 1 <= kSmemOffsets) {
+      for (int64_t k = tid; k <= p.N; k += kLseThreads) s_off[k] = p.offsets[k];
+      off = s_off;
+    }
   }
   // every CTA of the cluster is running and initialised before any
   // distributed-shared-memory store or bulk copy
@@ -294,6 +309,7 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
         for (int c = 0; c < sl.nchunks; ++c) {
           if (*(volatile int*)&s_abort) break;
           if (!mbar_wait(smem_u32(&s_empty[stage]), phase ^ 1u)) {
+            pdl_wait();
             atomicOr(&p.hdr->flags, kFlagTimeout);
             *(volatile int*)&s_abort = 1;
             break;
@@ -339,6 +355,7 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
       for (int c = 0; c < sl.nchunks; ++c) {
         bool ok = !*(volatile int*)&s_abort;
         if (ok && !mbar_wait(smem_u32(&s_full[stage]), phase)) {
+          pdl_wait();
           atomicOr(&p.hdr->flags, kFlagTimeout);
           *(volatile int*)&s_abort = 1;
           ok = false;
@@ -449,11 +466,11 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
   }
   // after the rows, where little state is live (keeps the row loop's
   // register count)
-  if (p.zero_past_len != nullptr) {  // positions past each length: 0
+  if (p.zero_past) {  // positions past each length: 0
     const int64_t nct = (int64_t)gridDim.x * kLseThreads;
     for (int64_t k = (int64_t)blockIdx.x * kLseThreads + tid; k < p.N * p.C; k += nct) {
       const int64_t i = k / p.C;
-      if (k - i * p.C >= p.zero_past_len[i]) {
+      if (k - i * p.C >= off[i + 1] - off[i]) {
         p.logp[k] = 0.f;
         p.lse[k] = 0.f;
       }
@@ -466,6 +483,9 @@ __global__ void __launch_bounds__(kLseThreads, 3) lse_gather_kernel(const LsePar
       mbar_wait(smem_u32(&s_full[n % kStages]), (n / kStages) & 1u);
     }
   }
+  // the grid completes only after prep has (the kernels after this one read
+  // prep's table through this kernel's completion)
+  if (tid == 0) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -478,7 +498,7 @@ std::mutex g_occ_mutex;
 std::map<std::tuple<int, int, int, int>, int> g_occ;  // (device, dtype, K, smem) -> clusters
 
 template <typename T, int K>
-cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
+cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st, bool after_prep) {
   constexpr int EPV = Elt<T>::kPerVec;
   const WsLayout l = ws_layout(a.N);
   char* ws = static_cast<char*>(a.ws);
@@ -496,7 +516,9 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
   p.hdr = reinterpret_cast<WsHeader*>(ws);
   p.chunk = ((a.V + K - 1) / K + EPV - 1) / EPV * EPV;
   // no gradient weights requested: the log-probs-only call
-  p.zero_past_len = a.w == nullptr ? reinterpret_cast<const int32_t*>(ws + l.lens) : nullptr;
+  p.zero_past = a.w == nullptr;
+  p.early = after_prep && a.N + 1 <= kSmemOffsets;
+  p.len = a.len;
 
   const size_t smem = (size_t)kStages * kStageBytes +
                       (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
@@ -558,24 +580,26 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
 }
 
 template <typename T>
-cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
+cudaError_t launch_t(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st, bool after_prep) {
   switch (lse_split(a.V * (int64_t)sizeof(T), a.N * a.C, d.sms, "GRPO_LSE_CLUSTER")) {
     case 8:
-      return launch_k<T, 8>(a, d, st);
+      return launch_k<T, 8>(a, d, st, after_prep);
     case 4:
-      return launch_k<T, 4>(a, d, st);
+      return launch_k<T, 4>(a, d, st, after_prep);
     case 2:
-      return launch_k<T, 2>(a, d, st);
+      return launch_k<T, 2>(a, d, st, after_prep);
     default:
-      return launch_k<T, 1>(a, d, st);
+      return launch_k<T, 1>(a, d, st, after_prep);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st) {
+cudaError_t launch_lse_gather(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st,
+                              bool after_prep) {
   if (a.N == 0 || a.C == 0) return cudaSuccess;
-  return a.dtype == 0 ? launch_t<float>(a, d, st) : launch_t<uint16_t>(a, d, st);
+  return a.dtype == 0 ? launch_t<float>(a, d, st, after_prep)
+                      : launch_t<uint16_t>(a, d, st, after_prep);
 }
 
 }  // namespace grpo
