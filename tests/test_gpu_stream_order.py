@@ -73,6 +73,16 @@ def test_more_completions_than_the_prefix_table():
     H.check_small(w)
 
 
+def test_offsets_table_in_memory():
+    """4,100 completions: the forward's log-sum-exp kernel reads the prefix
+    table prep writes instead of building it in shared memory (it then waits
+    on prep first); forward and backward still match the oracle and both
+    backward orders agree."""
+    w = wl.variant(wl.TINY, name="order_n4100", B=1025, G=4, P=2, C=3, V=64)
+    _check(w, wl.make_logits_cpu(w).cuda())
+    H.check_small(w)
+
+
 def test_skip_zero_weight_orders_same_bits():
     w = wl.variant(wl.TINY, name="order_skip", B=4, G=4, C=40, V=2000, dtype="bf16")
     _check(w, wl.make_logits_cpu(w).cuda(), flags=1, grad=0.5)

@@ -106,8 +106,14 @@ def test_seq_mean_fused_same_bits():
     assert torch.equal(_bits(da), _bits(db))
 
 
-@pytest.mark.parametrize("w", [wl.TINY, CASES[1]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [wl.TINY, CASES[1],
+                               wl.variant(wl.TINY, name="lp_N1100", B=275, G=4, P=2, C=3, V=64),
+                               wl.variant(wl.TINY, name="lp_N4100", B=1025, G=4, P=2, C=3, V=64)],
+                         ids=lambda w: w.name)
 def test_logprobs_only(w):
+    """The log-probs-only call gives the loss forward's logp and lse bits and
+    0 past each length; 1,100 completions build the length prefix table in
+    each CTA, 4,100 read the one prep writes."""
     g = H.g()
     logits = wl.make_logits_cpu(w).cuda()
     ids = torch.from_numpy(wl.make_ids(w)).cuda()
@@ -117,6 +123,10 @@ def test_logprobs_only(w):
     lp, lse, ws = g.grpo_logprobs(logits, w.P, ids, lens)
     assert g.grpo_check_error(ws) == 0
     assert torch.equal(_bits(lp), _bits(full["logp"])) and torch.equal(_bits(lse), _bits(full["lse"]))
+    _, len_o = oracle.mask(wl.make_ids(w), w.P, w.C, w.eos_id)
+    past = np.arange(w.C)[None, :] >= len_o[:, None]
+    assert past.any() and not past.all()
+    assert np.all(_bits(lp).cpu().numpy()[past] == 0) and np.all(_bits(lse).cpu().numpy()[past] == 0)
 
 
 def test_skip_zero_weight():
