@@ -65,18 +65,20 @@ def test_fused_same_bits_as_two_calls(w):
     assert abs(la - lb) <= 1e-6 * max(abs(la), 1e-12), (la, lb)
 
 
-@pytest.mark.parametrize("B,C,V", [(50, 4, 50001), (1025, 1, 50000)],
-                         ids=["N200_three_head_slots", "N4100_offsets_in_memory"])
-def test_fused_head_slots_same_bits(B, C, V):
+@pytest.mark.parametrize("B,C,V,dtype", [(50, 4, 50001, "bf16"), (1025, 1, 50000, "bf16"),
+                                         (50, 4, 20001, "f32")],
+                         ids=["N200_three_head_slots", "N4100_offsets_in_memory", "N200_f32"])
+def test_fused_head_slots_same_bits(B, C, V, dtype):
     """The fused kernel holds each row's first chunks in shared-memory slots,
     as many as fit beside its ring and offsets table with two CTAs per SM:
     three at 200 completions, four again at 4,100 (the offsets table then
     stays in global memory).  Whole rows per CTA (N*C above four rows per
-    SM), seven 16 KiB chunks a row, so the ring carries the rest; the
-    outputs have the bits of the two calls."""
-    w = H.with_contrast(wl.variant(wl.TINY, name=f"slots_N{4 * B}", B=B, G=4, P=1, C=C, V=V,
-                                   dtype="bf16", logit_std=3.0, seed=500 + B))
-    logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    SM), five to seven 16 KiB chunks a row, so the ring carries the rest;
+    the outputs have the bits of the two calls."""
+    w = H.with_contrast(wl.variant(wl.TINY, name=f"slots_N{4 * B}_{dtype}", B=B, G=4, P=1, C=C,
+                                   V=V, dtype=dtype, logit_std=3.0, seed=500 + B))
+    logits = torch.empty((w.N, w.T, w.V), device="cuda",
+                         dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
     wl.fill_logits_cuda(w, logits)
     ids, R = wl.make_ids(w), wl.make_rewards(w)
     a = H.run_gpu(w, logits, ids, R, None, None, grad=1.5, beta=0.0)
