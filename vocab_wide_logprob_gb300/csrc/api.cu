@@ -540,7 +540,7 @@ grpo_status fwd_bwd_impl(const void* logits, grpo_dtype dtype, int64_t N, int64_
     // The gradient kernel reads the scored rows from host memory itself
     // (writing them to the staging buffer for its second pass), so its
     // arithmetic runs while the rows cross the host link; the zero writer
-    // runs beside it as in the device-memory case.
+    // runs beside it (this variant holds no head slots in shared memory).
     FwdArgs ah = a;
     ah.logits = host_src;
     if (launch_prep(ah, st) != cudaSuccess) return GRPO_ERR_CUDA;

@@ -20,9 +20,11 @@
 // shared-memory slots pass 1 loaded them into, and the rest from L2 where it
 // is still there (whole rows keep ~90 MB live over the grid, so part of it
 // comes from HBM again), last chunk first (the most recently loaded lines are
-// the likeliest to be in L2).  Rows that score nothing are written with zeros by a separate
-// store-only kernel launched after this one, which runs beside it (its CTAs
-// take the slots this persistent grid leaves free and do not wait on it).
+// the likeliest to be in L2).  Rows that score nothing are written with
+// zeros by a separate store-only kernel launched after this one, which does
+// not wait on it: its CTAs take the SM slots this persistent grid's CTAs free
+// as they finish (with the head slots two CTAs fill an SM's shared memory;
+// the host-memory variant holds none, and there they also run beside it).
 // Per element the arithmetic is that of lse_gather_kernel and dlogits_kernel,
 // and the per-token terms are token_terms(), so logp, lse, w and dlogits have
 // the same bits as the unfused path; only the loss's summation order differs
