@@ -32,6 +32,9 @@
  *    outside [0, C]) cannot be seen on the host without a synchronisation;
  *    the kernels record them in the workspace and grpo_check_error reports
  *    them.  The kernels never trap.
+ *  - Within one call, the output arrays and the workspace must not overlap
+ *    one another or that call's inputs (inputs may share memory).  Buffers
+ *    of different calls may overlap; stream order then applies.
  *  - Inputs at positions the mask excludes (old_logp and ref_logp past the
  *    first EOS) are never read; outputs there are 0.
  *  - Index arithmetic is 64-bit; N*C must be below 2^31.
