@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--workload", default=wl.QWEN_G8.name, choices=sorted(wl.BY_NAME))
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--reference-seconds", type=float, default=90.0,
+                   help="--impl reference: host seconds the whole run (warm-up + timed) aims at")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-copy-ceiling", action="store_true")
@@ -421,13 +423,14 @@ def run_reference(args, w: wl.Workload):
         return
     import oracle
     s = OracleSample(w)
-    # calibrate rows per step so the whole run takes about 90 s: one whole
-    # sequence (its prompt rows and its scored rows) gives the mean row cost
+    # calibrate rows per step so the whole run takes about --reference-seconds
+    # (90 s by default): one whole sequence (its prompt rows and its scored
+    # rows) gives the mean row cost
     t0 = time.perf_counter()
     s.step(w.T)
     per_row = (time.perf_counter() - t0) / w.T
     total_steps = args.steps + args.warmup
-    rows = max(1, int(90.0 / max(total_steps, 1) / max(per_row, 1e-6)))
+    rows = max(1, int(args.reference_seconds / max(total_steps, 1) / max(per_row, 1e-6)))
     for _ in range(args.warmup):
         s.step(rows)
     tokens = 0
