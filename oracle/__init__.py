@@ -14,6 +14,8 @@ with ctypes and marshals numpy arrays.  Each method cites the part of the page
 
 * :meth:`Oracle.mask`       -- "The completion mask" (``build_completion_mask``)
 * :meth:`Oracle.advantage`  -- "Dr. GRPO": A_i = R_i - group mean, no sigma
+* :meth:`Oracle.contrast_count` -- the analysis page "The Quiet Library",
+  "The sparse-reward bottleneck": groups whose rewards are not all equal
 * :meth:`Oracle.logp`, :meth:`Oracle.logp_rows` -- "compute_logprobs": shift
   by one, ``log_softmax`` over the vocabulary, gather at the sampled id
 * :meth:`Oracle.loss`       -- "The loss" (``grpo_loss``) plus the pseudo-code's
@@ -109,6 +111,7 @@ class Oracle:
             "oracle_mask": [P, I64, I64, I64, I64, P, P],
             "oracle_advantage": [P, I64, I64, P],
             "oracle_advantage_std": [P, I64, I64, D, P],
+            "oracle_contrast_count": [P, I64, I64, P],
             "oracle_loss_agg": [P, P, P, P, P, I64, I64, D, D, D, INT, P, P, P],
             "oracle_logp_rows": [P, INT, I64, I64, P, P, P],
             "oracle_logp": [P, INT, I64, I64, I64, I64, P, P, P, P],
@@ -167,6 +170,19 @@ class Oracle:
         _check(self.lib.oracle_advantage_std(_ptr(R), R.size // G, G, float(std_eps), _ptr(A)),
                "advantage_std")
         return A
+
+    # -- "The sparse-reward bottleneck" ----------------------------------------
+    def contrast_count(self, rewards: np.ndarray, G: int) -> int:
+        """Number of groups of G consecutive completions whose rewards are not
+        all equal (the groups that carry a learning signal; a uniform group's
+        advantages are all zero)."""
+        R = np.ascontiguousarray(rewards, dtype=np.float64).reshape(-1)
+        if G < 1 or R.size % G:
+            raise ValueError("len(rewards) must be a multiple of G >= 1")
+        out = ctypes.c_int64(0)
+        _check(self.lib.oracle_contrast_count(_ptr(R), R.size // G, G, ctypes.addressof(out)),
+               "contrast_count")
+        return int(out.value)
 
     # -- "compute_logprobs" --------------------------------------------------
     def logp_rows(self, rows: np.ndarray, dtype: str, y: np.ndarray):
@@ -355,6 +371,10 @@ def advantage(*a, **k):
 
 def advantage_std(*a, **k):
     return default().advantage_std(*a, **k)
+
+
+def contrast_count(*a, **k):
+    return default().contrast_count(*a, **k)
 
 
 def loss_seq_mean(*a, **k):

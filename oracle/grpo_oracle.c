@@ -237,6 +237,32 @@ int oracle_advantage_std(const double *R, int64_t B, int64_t G, double std_eps, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* reward contrast  ("The Quiet Library", "The sparse-reward bottleneck":   */
+/* a group whose completions all get the same reward carries no contrast,   */
+/* so its advantages are all zero; the useful groups are the others)        */
+/* ------------------------------------------------------------------------ */
+
+/* R: [B*G] grouped as [B, G].  *count = the number of groups b whose G
+ * rewards are not all equal to one another. */
+int oracle_contrast_count(const double *R, int64_t B, int64_t G, int64_t *count)
+{
+    if (B < 0 || G < 1 || !count || (B > 0 && !R))
+        return -1;
+    int64_t useful = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        const double *grp = R + b * G;
+        int all_equal = 1;
+        for (int64_t k = 1; k < G && all_equal; ++k)
+            if (grp[k] != grp[0])
+                all_equal = 0;
+        if (!all_equal)
+            useful += 1;
+    }
+    *count = useful;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* log-probabilities  ("compute_logprobs": shift, log_softmax, gather)       */
 /* ------------------------------------------------------------------------ */
 

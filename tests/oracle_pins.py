@@ -123,6 +123,48 @@ def pin_advantage_monte_carlo(o, groups=1_000_000):
 
 
 # --------------------------------------------------------------------------
+# reward contrast ("The Quiet Library", "The sparse-reward bottleneck"): a
+# group whose rewards are all equal has no contrast; the others are useful
+# --------------------------------------------------------------------------
+
+def pin_contrast_count_examples(o):
+    """Hand-counted groups: the differing reward may sit first, in the middle
+    or last in its group; G = 1 never has contrast; real-valued rewards."""
+    cases = [
+        ([1, 0, 0, 0], 4, 1),
+        ([0, 0, 0, 1], 4, 1),               # only the last reward differs
+        ([0, 0, 1, 0], 4, 1),
+        ([1, 1, 1, 1, 0, 0, 0, 0], 4, 0),   # two uniform groups (all pass, all fail)
+        ([0, 0, 0, 1, 1, 1, 1, 1, 0, 1, 0, 0], 4, 2),
+        ([1, 1, 0, 0, 0, 0, 0, 0], 4, 1),   # group 1 equals group 0's last rewards
+        ([1, 0, 1, 0, 1, 1], 2, 2),
+        ([1.0, 0.0, 1.0], 1, 0),            # a single completion is never contrasted
+        ([0.5, 0.5, 0.5, 0.5, 0.5, 0.25], 3, 1),
+        ([], 4, 0),
+    ]
+    for R, G, want in cases:
+        got = o.contrast_count(np.array(R, np.float64), G)
+        assert got == want, (R, G, got, want)
+
+
+def pin_contrast_count_monte_carlo(o, groups=200_000):
+    """Binary rewards from the generator's Bernoulli draw: the fraction of
+    groups the oracle counts as contrasted is 1 - [(1-p)^G + p^G], the
+    complement of the pages' no-contrast probability (0.6634 printed at
+    p = 0.05, G = 8; 0.4401 all-fail at G = 16), within 4 standard errors."""
+    printed = {(p, G): v for q, p, G, v, _ in no_contrast_golden() if q == "no_contrast"}
+    for p, G in ((0.05, 8), (0.05, 16), (0.3, 4)):
+        exact = (1 - p) ** G + p ** G
+        if (p, G) in printed:
+            assert abs(exact - printed[(p, G)]) < 1e-4
+        w = wl.Workload("mc_c", B=groups, G=G, P=1, C=1, V=2, dtype="f32", logit_std=1.0,
+                        eos_id=0, reward_p=p, seed=991 + G)
+        frac = o.contrast_count(wl.make_rewards(w), G) / groups
+        se = math.sqrt(exact * (1 - exact) / groups)
+        assert abs(frac - (1 - exact)) < 4 * se, (p, G, frac, 1 - exact, se)
+
+
+# --------------------------------------------------------------------------
 # "compute_logprobs": shift by one, log_softmax, gather
 # --------------------------------------------------------------------------
 
@@ -639,6 +681,7 @@ ALL_CHEAP = [
     pin_lmhead_reduces_to_logits, pin_lmhead_grads_fd, pin_lmhead_grads_identity_and_subsets,
     pin_advantage_std_examples, pin_seq_mean_aggregation, pin_dlogits_fd_seq_mean,
     pin_mask_golden, pin_mask_batch_matches_rows, pin_advantage_examples,
+    pin_contrast_count_examples, pin_contrast_count_monte_carlo,
     pin_logp_constant_row, pin_logp_two_level, pin_logp_library, pin_logp_token_range,
     pin_logp_shift, pin_surrogate_golden, pin_kl_golden, pin_step0_identity,
     pin_ratio_closed_form, pin_kl_closed_form, pin_masked_never_read,

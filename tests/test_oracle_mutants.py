@@ -22,6 +22,13 @@ MUTANTS = {
     # advantage
     "advantage_divides_by_G_minus_1": ("mu = sum / (double)G;\n        for (int64_t g = 0; g < G; ++g)\n            A[b * G + g] = R[b * G + g] - mu;",
                                        "mu = sum / (double)(G - 1);\n        for (int64_t g = 0; g < G; ++g)\n            A[b * G + g] = R[b * G + g] - mu;"),
+    # reward contrast ("The sparse-reward bottleneck")
+    "contrast_counts_uniform_groups": ("if (!all_equal)\n            useful += 1;",
+                                       "if (all_equal)\n            useful += 1;"),
+    "contrast_skips_last_reward": ("k < G && all_equal", "k < G - 1 && all_equal"),
+    "contrast_compares_to_batch_start": ("grp[k] != grp[0]", "grp[k] != R[0]"),
+    "contrast_compares_neighbours_only_once": ("for (int64_t k = 1; k < G && all_equal; ++k)",
+                                              "for (int64_t k = 1; k < 2 && k < G && all_equal; ++k)"),
     # original GRPO advantage
     "std_sample_not_population": ("sqrt(ss / (double)G)", "sqrt(ss / (double)(G - 1))"),
     "std_missing_sqrt": ("double sigma = sqrt(ss / (double)G);", "double sigma = ss / (double)G;"),
