@@ -199,7 +199,10 @@ grpo_status grpo_loss_fwd(const void *logits, grpo_dtype dtype, int64_t N, int64
  * enqueues nothing.  Nothing is allocated and no allocating routine is called.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.
+ * before any stream capture.  The address is kept per CUDA context (keyed on
+ * the context's id), so after cudaDeviceReset, or in another context made
+ * current on the same device, the next call looks it up again; that call too
+ * should come before any capture.
  * All calls share the one array and it keeps the last call's contents; each
  * call resets what must start at zero before using it.  Calls whose work can
  * overlap on the GPU (different streams, or different host threads) race on

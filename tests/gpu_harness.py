@@ -62,9 +62,10 @@ def dev(x, device="cuda"):
 
 
 def run_gpu(w: wl.Workload, logits, ids, R, old, ref, grad=None, dlogits=None, eps=None,
-            beta=None, norm=0.0, fused=False):
+            beta=None, norm=0.0, fused=False, bwd_flags=0):
     """mask -> advantage -> fwd -> bwd (or the fused fwd+bwd) through the C
-    ABI; returns tensors."""
+    ABI; returns tensors.  bwd_flags: grpo_loss_bwd_ex flags of the two-pass
+    backward (GRPO_BWD_SKIP_ZERO_WEIGHT = 1)."""
     n = g()
     t_ids = dev(ids)
     mask, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
@@ -78,7 +79,11 @@ def run_gpu(w: wl.Workload, logits, ids, R, old, ref, grad=None, dlogits=None, e
         dl = out["dlogits"]
     else:
         out = n.grpo_loss_fwd(logits, w.P, t_ids, lens, adv, dev(old), dev(ref), e, b, norm)
-        dl = n.grpo_loss_bwd(logits, w.P, t_ids, lens, out["lse"], out["w"], gt, dlogits)
+        if bwd_flags:
+            dl = n.grpo_loss_bwd_ex(logits, w.P, t_ids, lens, out["lse"], out["w"], gt, dlogits,
+                                    flags=bwd_flags)
+        else:
+            dl = n.grpo_loss_bwd(logits, w.P, t_ids, lens, out["lse"], out["w"], gt, dlogits)
     status = n.grpo_check_error(out["workspace"])
     torch.cuda.synchronize()
     out.update(mask=mask, lens=lens, adv=adv, dlogits=dl, status=status)
@@ -126,7 +131,7 @@ def to_host_logits(t: torch.Tensor):
 
 
 def check_small(w: wl.Workload, logits_cpu=None, grad=None, norm=0.0, logits_gpu=None,
-                fused=False, dlogits=None):
+                fused=False, dlogits=None, bwd_flags=0):
     """Whole-batch element-wise comparison (sizes the oracle finishes fast)."""
     ids = wl.make_ids(w)
     R = wl.make_rewards(w)
@@ -146,7 +151,7 @@ def check_small(w: wl.Workload, logits_cpu=None, grad=None, norm=0.0, logits_gpu
 
     logits = logits_cpu.cuda() if logits_gpu is None else logits_gpu
     out = run_gpu(w, logits, ids, R, old, ref, grad=grad, norm=norm, fused=fused,
-                  dlogits=dlogits)
+                  dlogits=dlogits, bwd_flags=bwd_flags)
     assert out["status"] == 0
     assert np.array_equal(out["mask"].cpu().numpy(), m_o)
     assert np.array_equal(out["lens"].cpu().numpy(), len_o)
@@ -188,9 +193,25 @@ def oracle_logp_device_rows(w: wl.Workload, logits: torch.Tensor, ids, len_o):
     return lp_o, lse_o
 
 
-def check_full_size(w: wl.Workload, n_valid_rows=12, n_zero_rows=6, seed=0):
+def oracle_dlogits_rows(z, dt, y, lse, wt, g=1.0):
+    """The oracle's gradient of k independent scored rows z [k, V] with
+    targets y [k], log-sum-exps lse [k] and weights wt [k]: the rows laid out
+    as a batch of one sequence (prompt length 1, so row t scores token t) and
+    passed to :func:`oracle.dlogits`, which runs them on all host cores."""
+    k, V = z.shape
+    zb = np.concatenate([z, np.zeros((1, V), z.dtype)])[None]
+    ids_b = np.concatenate([[0], np.asarray(y, np.int64)])[None]
+    d = oracle.dlogits(zb, dt, 1, k, ids_b, np.array([k], np.int32),
+                       np.asarray(lse, np.float64)[None], np.asarray(wt, np.float64)[None], g)
+    return d[0, :k]
+
+
+def check_full_size(w: wl.Workload, rows="all", grad=None, seed=0):
     """A full-size workload in the benchmark's launch configuration: the whole
-    loss, every log-prob, and sampled dlogits rows computed one by one."""
+    loss, every log-prob, the gradient of scored rows computed by the oracle
+    one completion at a time (``rows="all"``: every scored row; ``"ends"``:
+    the first, middle and last scored row of every completion), and every
+    row that scores nothing checked to be +0 bit for bit."""
     ids = wl.make_ids(w)
     R = wl.make_rewards(w)
     logits = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16 if w.dtype == "bf16"
@@ -204,41 +225,49 @@ def check_full_size(w: wl.Workload, n_valid_rows=12, n_zero_rows=6, seed=0):
     loss_o, w_o, ell_o = oracle.loss(lp_o, None if old is None else old.astype(np.float64),
                                      None if ref is None else ref.astype(np.float64), A_o,
                                      len_o, w.eps, w.beta, nrm)
-    out = run_gpu(w, logits, ids, R, old, ref)
+    out = run_gpu(w, logits, ids, R, old, ref, grad=grad)
+    gval = 1.0 if grad is None else grad
     assert out["status"] == 0
     assert np.array_equal(out["mask"].cpu().numpy(), m_o)
     assert np.array_equal(out["lens"].cpu().numpy(), len_o)
     assert np.array_equal(out["adv"].cpu().numpy(), A_o.astype(np.float32))
     lp = out["logp"].cpu().numpy().astype(np.float64)
     assert np.max(np.abs(lp - lp_o)) <= LOGP_ATOL[w.dtype], np.max(np.abs(lp - lp_o))
+    lse_gpu = out["lse"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse_gpu - lse_o)) <= LOGP_ATOL[w.dtype]
     assert_loss(float(out["loss"].item()), loss_o, ell_o, nrm)
     kink = kink_tokens(lp_o, old, w.eps)
 
-    rng = np.random.default_rng(seed)
-    valid = np.argwhere(m_o == 1)
-    valid = valid[~kink[valid[:, 0], valid[:, 1]]]
-    picks = valid[rng.choice(len(valid), size=min(n_valid_rows, len(valid)), replace=False)]
     dl = out["dlogits"]
-    lse_gpu = out["lse"].cpu().numpy()
-    for i, t in picks:
-        row = w.P - 1 + t
-        zr, dt = to_host_logits(logits[i, row])
-        y = int(ids[i, w.P + t])
-        d_o = oracle.dlogits_row(zr, dt, y, lse_o[i, t], w_o[i, t])
-        d_g, _ = to_host_logits(dl[i, row])
-        d_g = _as_f64(d_g, dt)
-        assert_dlogits(d_g, d_o, f"{w.name} row ({i},{t})")
-        assert abs(lse_gpu[i, t] - lse_o[i, t]) <= LOGP_ATOL[w.dtype]
-    # rows that score nothing: prompt rows, the last row, rows past the EOS
-    zero_rows = [(i, int(r)) for i in range(w.N) for r in
-                 (0, w.P - 2, w.T - 1, w.P - 1 + int(len_o[i]))
-                 if 0 <= r < w.T and not (0 <= r - (w.P - 1) < len_o[i])]
-    for k in rng.choice(len(zero_rows), size=min(n_zero_rows, len(zero_rows)), replace=False):
-        i, r = zero_rows[k]
-        d_g, dt = to_host_logits(dl[i, r])
-        assert not np.any(_as_f64(d_g, dt)), (w.name, i, r)
-    return out, dict(loss=loss_o, picks=picks, kink=int(kink.sum()), logits=logits, ids=ids,
-                     w_o=w_o, lse_o=lse_o, len_o=len_o)
+    compared = 0
+    for i in range(w.N):
+        L = int(len_o[i])
+        if L == 0:
+            continue
+        ts = np.arange(L) if rows == "all" else np.unique([0, L // 2, L - 1])
+        ts = ts[~kink[i, ts]]
+        if len(ts) == 0:
+            continue
+        sel = torch.from_numpy(w.P - 1 + ts).to(logits.device)
+        z, dt = to_host_logits(logits[i].index_select(0, sel))
+        y = ids[i, w.P + ts]
+        d_o = oracle_dlogits_rows(z, dt, y, lse_o[i, ts], w_o[i, ts], gval)
+        d_g, _ = to_host_logits(dl[i].index_select(0, sel))
+        assert_dlogits(_as_f64(d_g, dt), d_o, f"{w.name} completion {i}")
+        compared += len(ts)
+    # rows that score nothing: prompt rows 0..P-2, rows past each length,
+    # the last row; +0 exactly (bit pattern 0)
+    bits = dl.view(torch.int16 if dl.dtype == torch.bfloat16 else torch.int32)
+    zero_rows = 0
+    for i in range(w.N):
+        first = w.P - 1 + int(len_o[i])
+        assert not bool(bits[i, :w.P - 1].any()), (w.name, i, "prompt rows")
+        assert not bool(bits[i, first:].any()), (w.name, i, "rows past the length")
+        zero_rows += (w.P - 1) + (w.T - first)
+    torch.cuda.synchronize()
+    return out, dict(loss=loss_o, compared=compared, zero_rows=zero_rows,
+                     kink=int(kink.sum()), logits=logits, ids=ids, w_o=w_o, lse_o=lse_o,
+                     len_o=len_o)
 
 
 def _as_f64(a, dt):

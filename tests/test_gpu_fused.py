@@ -213,6 +213,61 @@ def test_host_logits_refuses_pageable_memory():
     assert rc == 1  # GRPO_ERR_INVALID_ARG
 
 
+def test_host_logits_registered_too_short():
+    """A host buffer page-locked over only part of the logits' size is refused
+    before anything is enqueued (the kernels read any scored row, up to the
+    last byte); the same buffer page-locked in full is accepted and gives the
+    bits of the device-memory path."""
+    import ctypes
+    n = H.g()
+    lib = n.library()
+    w = H.with_contrast(wl.variant(wl.QWEN_G8, name="short_host", B=2, G=4, P=6, C=26, V=1024,
+                                   eos_id=1023, seed=92))
+    logits = wl.make_logits_cpu(w)
+    nbytes = logits.numel() * 2
+    assert nbytes % 8192 == 0
+    raw = np.zeros(nbytes + 4096, np.uint8)
+    off = (-raw.ctypes.data) % 4096
+    buf = raw[off:off + nbytes]
+    buf[:] = logits.view(torch.int16).numpy().view(np.uint8).reshape(-1)
+    t_ids = H.dev(wl.make_ids(w))
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(wl.make_rewards(w)), w.G)
+    ref = n.grpo_loss_fwd_bwd(logits.cuda(), w.P, t_ids, lens, adv, None, None, 0.2, 0.0)
+    out = {k: torch.empty_like(ref[k]) for k in ("logp", "lse", "w", "loss")}
+    dl = torch.empty((w.N, w.T, w.V), dtype=torch.bfloat16, device="cuda")
+    st = torch.empty_like(dl)
+    ws = torch.zeros((n.grpo_workspace_size(w.N, w.C, w.V),), dtype=torch.uint8, device="cuda")
+    p = ctypes.c_void_p
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return lib.grpo_loss_fwd_bwd_host(
+            p(buf.ctypes.data), 1, w.N, w.P, w.C, w.V, p(t_ids.data_ptr()), p(lens.data_ptr()),
+            p(adv.data_ptr()), None, None, 0.2, 0.0, 0.0, None, p(out["logp"].data_ptr()),
+            p(out["lse"].data_ptr()), p(out["w"].data_ptr()), p(out["loss"].data_ptr()),
+            p(dl.data_ptr()), p(st.data_ptr()), p(ws.data_ptr()), ws.numel(), p(stream))
+
+    cudart = torch.cuda.cudart()
+    flags = 3  # cudaHostRegisterPortable | cudaHostRegisterMapped
+    for registered in (nbytes // 2, nbytes - 4096):
+        assert int(cudart.cudaHostRegister(buf.ctypes.data, registered, flags)) == 0
+        try:
+            assert call() == 1  # GRPO_ERR_INVALID_ARG, nothing enqueued
+        finally:
+            assert int(cudart.cudaHostUnregister(buf.ctypes.data)) == 0
+    assert int(cudart.cudaHostRegister(buf.ctypes.data, nbytes, flags)) == 0
+    try:
+        assert call() == 0
+        torch.cuda.synchronize()
+    finally:
+        assert int(cudart.cudaHostUnregister(buf.ctypes.data)) == 0
+    assert n.grpo_check_error(ws) == 0
+    for k in ("logp", "lse", "w", "loss"):
+        assert torch.equal(_bits(ref[k]), _bits(out[k])), k
+    assert torch.equal(_bits(ref["dlogits"]), _bits(dl))
+
+
 def test_host_logits_full_size_same_bits():
     """The benchmark workload (V = 151,936, whole rows per CTA) with the logits
     in pinned host memory: the gradient kernel reads the scored rows from host

@@ -203,10 +203,21 @@ def test_bitwise_deterministic_and_no_overrun():
 
 # -------------------------------------------------- full-size workloads
 
+def _rows_for(w):
+    # every scored row where the oracle finishes it in seconds (the two
+    # Qwen2.5-shaped single-group workloads); the first, middle and last
+    # scored row of every completion on the two large ones
+    return "all" if w.N * w.C <= 16 * 512 else "ends"
+
+
 @pytest.mark.parametrize("w", wl.CONFIGS[1:], ids=lambda w: w.name)
 def test_full_size(w):
-    out, o = H.check_full_size(w)
-    torch.cuda.synchronize()
+    if _rows_for(w) == "ends":
+        # these workloads' own seeds have reward contrast, so their gradient
+        # is live without a seed search
+        assert oracle.contrast_count(wl.make_rewards(w), w.G) > 0
+    out, o = H.check_full_size(w, rows=_rows_for(w))
+    assert o["compared"] > 0 and o["zero_rows"] > 0
     del out, o
     torch.cuda.empty_cache()
 
@@ -214,7 +225,11 @@ def test_full_size(w):
 @pytest.mark.parametrize("w", wl.CONFIGS[1:3], ids=lambda w: w.name)
 def test_full_size_with_contrast(w):
     """The primary seeds of these workloads have no reward contrast (zero
-    advantages); the next seed with contrast exercises the gradient."""
-    out, o = H.check_full_size(H.with_contrast(w), seed=1)
+    advantages); the next seed with contrast exercises the gradient, with the
+    upstream gradient set to the normaliser so per-token weights are O(A)
+    and the relative tolerance binds."""
+    wc = H.with_contrast(w)
+    out, o = H.check_full_size(wc, rows="all", grad=float(wc.N * wc.C))
+    assert o["compared"] == int(o["len_o"].sum()) - o["kink"]
     del out, o
     torch.cuda.empty_cache()

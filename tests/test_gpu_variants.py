@@ -28,8 +28,7 @@ def test_advantage_std_and_contrast_count(G):
         adv, cnt = g.grpo_advantage_ex(torch.from_numpy(R).cuda(), G, 1, 1e-4, count_contrast=True)
         a = adv.cpu().numpy().astype(np.float64)
         assert np.all(np.abs(a - A_o) <= 2e-6 * np.maximum(1.0, np.abs(A_o))), np.max(np.abs(a - A_o))
-        Rg = R.reshape(B, G)
-        assert int(cnt.item()) == int(np.sum(Rg.max(1) != Rg.min(1)))
+        assert int(cnt.item()) == oracle.contrast_count(R, G)
         # mode 0 is grpo_advantage, bit for bit
         a0, c0 = g.grpo_advantage_ex(torch.from_numpy(R).cuda(), G, 0, 0.0, count_contrast=True)
         assert torch.equal(a0, g.grpo_advantage(torch.from_numpy(R).cuda(), G))
@@ -127,6 +126,34 @@ def test_logprobs_only(w):
     past = np.arange(w.C)[None, :] >= len_o[:, None]
     assert past.any() and not past.all()
     assert np.all(_bits(lp).cpu().numpy()[past] == 0) and np.all(_bits(lse).cpu().numpy()[past] == 0)
+
+
+SKIP_CASES = [
+    # no reward contrast, beta = 0: every gradient weight is exactly 0
+    wl.variant(wl.QWEN_G8, name="skip_nc", B=1, G=4, P=8, C=24, seed=5,
+               forced={"rewards": [0.0] * 4}, old_sigma=0.1),
+    # two groups, one with contrast: zero-weight rows beside live ones
+    wl.variant(wl.QWEN_G8, name="skip_c", B=2, G=4, P=8, C=24, reward_p=0.5, old_sigma=0.1,
+               seed=6, forced={"rewards": [1.0, 0.0, 0.0, 1.0, 1.0, 1.0, 1.0, 1.0]}),
+    # beta > 0: the KL term keeps every weight nonzero, nothing is skipped
+    wl.variant(wl.QWEN_G8, name="skip_kl", B=2, G=4, P=8, C=24, reward_p=0.5, old_sigma=0.1,
+               ref_sigma=0.1, beta=0.04, seed=7, forced={"rewards": [1.0] * 8}),
+    # float32 logits, ragged vocabulary
+    wl.variant(wl.TINY, name="skip_f32", V=1003, old_sigma=0.1, reward_p=0.5, seed=8),
+]
+
+
+@pytest.mark.parametrize("w", SKIP_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("grad", [None, 7.0], ids=["g1", "g7"])
+def test_skip_zero_weight_against_oracle(w, grad):
+    """The backward with GRPO_BWD_SKIP_ZERO_WEIGHT against the float64 oracle,
+    element by element over the whole batch (the rows it skips are compared
+    like every other row)."""
+    out, o = H.check_small(w, grad=grad, bwd_flags=1)
+    nonzero = int((out["w"] != 0).sum().item())
+    assert (nonzero == 0) == (w.name == "skip_nc"), (w.name, nonzero)
+    if w.name == "skip_c":
+        assert 0 < nonzero < int(out["lens"].sum().item())
 
 
 def test_skip_zero_weight():

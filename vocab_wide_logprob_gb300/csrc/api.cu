@@ -581,6 +581,31 @@ grpo_status grpo_loss_fwd_bwd_ex(const void* logits, grpo_dtype dtype, int64_t N
                       workspace_bytes, stream, nullptr);
 }
 
+// [p, p + bytes) must be page-locked host memory the device can address:
+// its first and its last byte both registered host memory, mapped by the
+// device `bytes - 1` apart (a buffer pinned or registered shorter than the
+// array fails the second test).  *dev_ptr receives the device address of p.
+static grpo_status host_range(const void* p, size_t bytes, void** dev_ptr) {
+  cudaPointerAttributes first, last;
+  if (cudaPointerGetAttributes(&first, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GRPO_ERR_INVALID_ARG;
+  }
+  if (first.type != cudaMemoryTypeHost || first.devicePointer == nullptr)
+    return GRPO_ERR_INVALID_ARG;
+  const char* end = static_cast<const char*>(p) + (bytes - 1);
+  if (cudaPointerGetAttributes(&last, end) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GRPO_ERR_INVALID_ARG;
+  }
+  if (last.type != cudaMemoryTypeHost ||
+      static_cast<const char*>(last.devicePointer) !=
+          static_cast<const char*>(first.devicePointer) + (bytes - 1))
+    return GRPO_ERR_INVALID_ARG;
+  *dev_ptr = first.devicePointer;
+  return GRPO_OK;
+}
+
 grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, int64_t N,
                                    int64_t P, int64_t C, int64_t V, const int64_t* input_ids,
                                    const int32_t* len, const float* adv, const float* old_logp,
@@ -601,20 +626,18 @@ grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, in
       !aligned(workspace, 256))
     return GRPO_ERR_MISALIGNED;
   if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
-  // the logits must be page-locked host memory the device can address
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, host_logits) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return GRPO_ERR_INVALID_ARG;
-  }
-  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return GRPO_ERR_INVALID_ARG;
+  // the logits must be page-locked host memory the device can address, all
+  // of it: the kernels read any scored row, up to the last byte
   const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
+  void* host_dev = nullptr;
+  s = host_range(host_logits, bytes, &host_dev);
+  if (s != GRPO_OK) return s;
   const char* sg = static_cast<const char*>(staging);
   const char* dl = static_cast<const char*>(dlogits);
   if (dlogits != nullptr && dl < sg + bytes && sg < dl + bytes) return GRPO_ERR_INVALID_ARG;
   return fwd_bwd_impl(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
                       beta, norm, GRPO_AGG_TOKEN_SUM, grad_loss, logp, lse, w, loss, dlogits,
-                      workspace, workspace_bytes, stream, attr.devicePointer);
+                      workspace, workspace_bytes, stream, host_dev);
 }
 
 grpo_status grpo_loss_fwd_bwd(const void* logits, grpo_dtype dtype, int64_t N, int64_t P,
