@@ -3,18 +3,24 @@
 
 One step = grpo_mask -> grpo_advantage -> grpo_loss_fwd -> grpo_loss_bwd on
 one stream, over one batch of synthetic inputs already resident in HBM.  The
-default workload is the Qwen2.5-0.5B-shaped single group (B=1, G=8, P=128,
-C=256, V=151936, bf16 logits ~N(0, 3^2)); the logits (0.93 GB) are larger
-than L2, so no flush is needed between steps.
+default workload is the largest one that fits one GPU: the long-completion
+batch (B=4 prompts x G=8, P=512, C=3584, V=151936, bf16 logits ~N(0, 3^2),
+k3 KL with beta=0.04): 39.8 GB of logits and a separate 39.8 GB dlogits
+buffer, far larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0):
   value        completion tokens/s (valid tokens / device step time), all ranks
   roofline     the dominant kernel (dlogits_kernel, one launch per step):
                algorithmic bytes / its CUDA-event duration vs measured HBM peak
+  paths        the same workload on each logits path (the two calls, the two
+               calls skipping zero-weight rows, the single-pass call), each
+               against its own byte count, with useful groups per second
+  per_config   the same summary for the other Qwen2.5-shaped workloads
   e2e          the same metric through the public API with host buffers:
                the logits in pinned host memory (grpo_loss_fwd_bwd_host moves
-               only the scored rows to the device), host -> device copies of
-               the other inputs and a device -> host read of the loss, all
+               only the scored rows to the device and writes the whole dlogits
+               into pinned host memory), host -> device copies of the other
+               inputs and device -> host copies of logp, w and the loss, all
                inside the timed region
   cpu_baseline the float64 CPU oracle, timed on a bounded sample
 ``--impl reference`` times the oracle alone (host cores) as the reference arm.
@@ -50,11 +56,16 @@ NOMINAL_HBM_GBS = 7900.0  # GB300's nominal HBM3e bandwidth, for context only
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=wl.QWEN_G8.name, choices=sorted(wl.BY_NAME))
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--workload", default=wl.LONG.name, choices=sorted(wl.BY_NAME))
+    p.add_argument("--per-config", default="auto",
+                   help="other workloads timed after the main one (comma-separated names); "
+                        "auto: every Qwen2.5-shaped workload but the main one; none: skip")
+    p.add_argument("--e2e-steps", type=int, default=20,
+                   help="end-to-end steps per timed loop (fewer when a loop would pass 1.5 s)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--reference-seconds", type=float, default=90.0,
                    help="--impl reference: host seconds the whole run (warm-up + timed) aims at")
@@ -72,7 +83,7 @@ def parse_args():
                         "lmhead_fwd_bwd: the loss from hidden states and its gradients with "
                         "respect to the hidden states and the LM head, on the tensor cores")
     p.add_argument("--no-other-path", dest="also_other_path", action="store_false",
-                   help="skip timing the other forward+backward path for the record")
+                   help="skip timing every logits path of the main workload for the record")
     p.add_argument("--hidden", type=int, default=896,
                    help="hidden size of the LM-head paths (Qwen2.5-0.5B: 896)")
     return p.parse_args()
@@ -236,6 +247,14 @@ def copy_ceiling(g, dev, nbytes: int = 4 << 30, reps: int = 10) -> float:
     del src, dst
     torch.cuda.empty_cache()
     return 2 * nbytes / best / 1e9
+
+
+def config_record(w: wl.Workload, world: int) -> dict:
+    """The workload's configuration, the same in both arms."""
+    return {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
+            "logits_dtype": w.dtype, "beta": w.beta, "eps": w.eps,
+            "l2": f"inputs larger than L2 ({w.logits_bytes / 1e9:.2f} GB logits); no flush",
+            "parallelism": f"dp{world} (independent groups)"}
 
 
 # --------------------------------------------------------------------------
@@ -444,8 +463,8 @@ def run_reference(args, w: wl.Workload):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
-                   "logits_dtype": w.dtype, "rows_per_step": rows},
+        "config": config_record(w, args.gpus),
+        "workload_stats": {"rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": f"{rows} rows of the [N, P+C] row space per step, cycling"},
@@ -457,6 +476,238 @@ def run_reference(args, w: wl.Workload):
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
+
+class Batch:
+    """One workload's inputs on the device and the buffers of its step."""
+
+    def __init__(self, g, w: wl.Workload, dev):
+        import torch
+        self.w = w
+        self.ids_np = wl.make_ids(w)
+        self.R_np = wl.make_rewards(w)
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.logits = torch.empty((w.N, w.T, w.V), dtype=tdt, device=dev)
+        wl.fill_logits_cuda(w, self.logits)
+        self.ids = torch.from_numpy(self.ids_np).to(dev)
+        self.R = torch.from_numpy(self.R_np).to(dev)
+        # old/ref log-probs: the current ones (computed by the library) + noise
+        self.mask, self.lens = g.grpo_mask(self.ids, w.P, w.C, w.eos_id)
+        self.adv = g.grpo_advantage(self.R, w.G)
+        cur = g.grpo_loss_fwd(self.logits, w.P, self.ids, self.lens, self.adv)
+        n_old, n_ref = wl.make_noise(w)
+        self.old = None if n_old is None else (
+            cur["logp"] + torch.from_numpy(n_old).float().to(dev)).contiguous()
+        self.ref = None if n_ref is None else (
+            cur["logp"] + torch.from_numpy(n_ref).float().to(dev)).contiguous()
+        self.t_valid = int(self.lens.sum().item())
+        _, n_contrast = g.grpo_advantage_ex(self.R, w.G, count_contrast=True)
+        self.contrast_groups = int(n_contrast.item())
+        # scored rows with a nonzero gradient weight (the only ones a backward
+        # that skips zero-weight rows reads)
+        wfull = g.grpo_loss_fwd(self.logits, w.P, self.ids, self.lens, self.adv, self.old,
+                                self.ref, w.eps, w.beta)["w"]
+        self.t_nonzero = int((wfull != 0).sum().item())
+        self.dlogits = torch.empty_like(self.logits)
+        self.ws = cur["workspace"]
+        self.out = None
+        self.fout = None
+
+    def step(self, g, path="two_pass", flags=None, record=None, stream=None):
+        """One step: grpo_mask -> grpo_advantage -> grpo_loss_fwd ->
+        grpo_loss_bwd (path "two_pass"), or the forward and backward in one
+        call (path "fused").  record: 4 events around the calls."""
+        w = self.w
+        if record is not None:
+            record[0].record(stream)
+        _, ln = g.grpo_mask(self.ids, w.P, w.C, w.eos_id, self.mask, self.lens)
+        a = g.grpo_advantage(self.R, w.G, self.adv)
+        if record is not None:
+            record[1].record(stream)
+        if path == "fused":
+            self.fout = g.grpo_loss_fwd_bwd(self.logits, w.P, self.ids, ln, a, self.old, self.ref,
+                                            w.eps, w.beta, 0.0, None, self.fout, self.ws,
+                                            self.dlogits)
+            if record is not None:
+                record[2].record(stream)
+                record[3].record(stream)
+            return
+        self.out = g.grpo_loss_fwd(self.logits, w.P, self.ids, ln, a, self.old, self.ref, w.eps,
+                                   w.beta, 0.0, self.out, self.ws)
+        if record is not None:
+            record[2].record(stream)
+        g.grpo_loss_bwd(self.logits, w.P, self.ids, ln, self.out["lse"], self.out["w"], None,
+                        self.dlogits, flags=flags)
+        if record is not None:
+            record[3].record(stream)
+
+    def free(self):
+        import torch
+        for k in ("logits", "dlogits", "ids", "R", "mask", "lens", "adv", "old", "ref", "ws",
+                  "out", "fout"):
+            setattr(self, k, None)
+        torch.cuda.empty_cache()
+
+
+def time_loop(fn, steps: int, stream) -> float:
+    """Seconds per call of fn over `steps` back-to-back calls, CUDA events at
+    the two ends only (an event between two launches would keep the second
+    from starting early)."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / steps
+
+
+def steps_for(ms_estimate: float, steps: int, seconds: float = 1.0) -> int:
+    """Timed steps for a secondary measurement: `steps`, fewer when they would
+    take longer than `seconds`, at least 5."""
+    return max(5, min(steps, int(seconds * 1e3 / max(ms_estimate, 1e-3))))
+
+
+def path_summary(g, b: Batch, peak: float, steps: int, warmup: int, stream) -> dict:
+    """Step time, throughput and roofline fraction of one workload on every
+    logits path: the two calls (the method's 2 reads + 1 write), the two calls
+    with the zero-weight skip (the skipped reads left out of the byte count),
+    and the single-pass call (1 read + 1 write)."""
+    w = b.w
+    out = {"workload": w.name, "valid_tokens": b.t_valid,
+           "nonzero_weight_tokens": b.t_nonzero,
+           "groups_with_reward_contrast": b.contrast_groups, "groups": w.B}
+    for name, path, flags, t_read in (("two_pass", "two_pass", None, None),
+                                      ("skip_zero_weight", "two_pass", 1, b.t_nonzero),
+                                      ("fused", "fused", None, None)):
+        fn = lambda: b.step(g, path, flags)  # noqa: E731
+        for _ in range(max(warmup, 3)):
+            fn()
+        est = time_loop(fn, 1, stream) * 1e3
+        n = steps_for(est, steps)
+        t = time_loop(fn, n, stream)
+        bb = algorithmic_bytes(w, b.t_valid, t_read)
+        nbytes = bb["step_logits_fused"] if path == "fused" else bb["step_logits"]
+        out[name] = {"ms_per_step": t * 1e3, "steps": n,
+                     "completion_tokens_per_s": b.t_valid / t,
+                     "useful_groups_per_s": b.contrast_groups / t,
+                     "logits_bytes_per_step": nbytes, "logits_gbs": nbytes / t / 1e9,
+                     "logits_roofline_frac": nbytes / t / 1e9 / peak}
+    return out
+
+
+def run_e2e(args, g, b: Batch, stream, world: int, dist) -> dict:
+    """The headline metric end to end through the public API, with the
+    step's inputs and results in pinned host memory: every step copies the
+    ids, rewards and old/reference log-probs in, runs grpo_mask,
+    grpo_advantage and grpo_loss_fwd_bwd_host (the single-pass call for
+    logits in host memory: only the scored rows cross the host link, into
+    the device logits buffer, which serves as its staging buffer, and the
+    kernels write the whole dlogits straight into pinned host memory, so the
+    gradient crosses the link the other way while the rows arrive), then
+    copies logp, w and the loss back."""
+    import torch
+    w = b.w
+
+    def pinned_like(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    h_logits = pinned_like(b.logits)
+    h_ids = pinned_like(b.ids)
+    h_R = pinned_like(b.R)
+    h_old = None if b.old is None else pinned_like(b.old)
+    h_ref = None if b.ref is None else pinned_like(b.ref)
+    h_dlogits = torch.empty(b.logits.shape, dtype=b.logits.dtype, pin_memory=True)
+    h_logp = torch.empty((w.N, w.C), dtype=torch.float32, pin_memory=True)
+    h_w = torch.empty((w.N, w.C), dtype=torch.float32, pin_memory=True)
+    h_loss = torch.empty((1,), dtype=torch.float32, pin_memory=True)
+    e = b.logits.element_size()
+    h2d = b.t_valid * w.V * e + sum(t.numel() * t.element_size()
+                                    for t in (h_ids, h_R, h_old, h_ref) if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in (h_dlogits, h_logp, h_w, h_loss))
+    state = {}
+
+    def enqueue():
+        b.ids.copy_(h_ids, non_blocking=True)
+        b.R.copy_(h_R, non_blocking=True)
+        if h_old is not None:
+            b.old.copy_(h_old, non_blocking=True)
+        if h_ref is not None:
+            b.ref.copy_(h_ref, non_blocking=True)
+        _, ln = g.grpo_mask(b.ids, w.P, w.C, w.eos_id, b.mask, b.lens)
+        a = g.grpo_advantage(b.R, w.G, b.adv)
+        o = g.grpo_loss_fwd_bwd_host(h_logits, w.P, b.ids, ln, a, b.old, b.ref, w.eps, w.beta,
+                                     0.0, None, state.get("o"), b.ws, h_dlogits,
+                                     staging=b.logits)
+        state["o"] = o
+        h_logp.copy_(o["logp"], non_blocking=True)
+        h_w.copy_(o["w"], non_blocking=True)
+        h_loss.copy_(o["loss"], non_blocking=True)
+
+    def eager_step():
+        enqueue()
+        stream.synchronize()
+
+    for _ in range(2):
+        eager_step()
+    n = steps_for(time_loop(eager_step, 1, stream) * 1e3, args.e2e_steps, 1.5)
+
+    def timed(step_fn):
+        # three timed loops of n steps; the median loop (one host stall would
+        # otherwise move a short loop noticeably)
+        for _ in range(2):
+            step_fn()
+        loops = []
+        for _ in range(3):
+            if world > 1:
+                dist.barrier()
+            loops.append(time_loop(step_fn, n, stream))
+        return sorted(loops)[1]
+
+    eager = timed(eager_step)
+    # The same calls captured once into a CUDA graph and replayed each step
+    # (one launch instead of the copies and kernels one by one; the host
+    # still waits for the results every step).
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            enqueue()
+    except Exception as ex:  # capture refused: keep the eager number
+        print(f"e2e graph capture failed: {ex!r}", file=sys.stderr)
+        graph = None
+        torch.cuda.synchronize()
+
+    def graph_step():
+        graph.replay()
+        stream.synchronize()
+
+    # every rank times a second pass (eager again where capture failed), so
+    # all ranks meet the same barriers
+    second = timed(graph_step if graph is not None else eager_step)
+    graph_used = graph is not None and second <= eager
+    best = second if graph_used else eager
+    if world > 1:
+        t = torch.tensor([best, eager], device=b.logits.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        best, eager = float(t[0]), float(t[1])
+    # the results that came back are the device path's: the loss, and the
+    # gradient rows around each completion's first scored row (its last
+    # prompt row is zero, the next two score tokens) have the bits of the
+    # last device-memory step's dlogits
+    ok = bool(torch.equal(h_loss, state["o"]["loss"].cpu()))
+    for i in range(w.N):
+        rows = slice(max(w.P - 2, 0), w.P + 1)
+        ok = ok and bool(torch.equal(h_dlogits[i, rows].to(b.dlogits.device), b.dlogits[i, rows]))
+    del graph
+    return {"s_per_step": best, "eager_s_per_step": eager, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "cuda_graph": graph_used, "results_match": ok}
+
 
 def run_ours(args, w0: wl.Workload):
     import torch
@@ -474,56 +725,18 @@ def run_ours(args, w0: wl.Workload):
     dev = torch.device("cuda", local)
     # weak scaling: each rank holds its own prompt groups (different seeds)
     w = wl.variant(w0, seed=w0.seed + 1000 * rank)
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
 
-    ids_np = wl.make_ids(w)
-    R_np = wl.make_rewards(w)
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    logits = torch.empty((w.N, w.T, w.V), dtype=tdt, device=dev)
-    wl.fill_logits_cuda(w, logits)
-    ids = torch.from_numpy(ids_np).to(dev)
-    R = torch.from_numpy(R_np).to(dev)
-    # old/ref log-probs: the current ones (computed by the library) + noise
-    mask, lens = g.grpo_mask(ids, w.P, w.C, w.eos_id)
-    adv = g.grpo_advantage(R, w.G)
-    cur = g.grpo_loss_fwd(logits, w.P, ids, lens, adv)
-    n_old, n_ref = wl.make_noise(w)
-    old = None if n_old is None else (cur["logp"] + torch.from_numpy(n_old).float().to(dev))
-    ref = None if n_ref is None else (cur["logp"] + torch.from_numpy(n_ref).float().to(dev))
-    t_valid = int(lens.sum().item())
-    adv_ex, n_contrast = g.grpo_advantage_ex(R, w.G, count_contrast=True)
-    contrast_groups = int(n_contrast.item())
-    # scored rows with a nonzero gradient weight (the only ones a backward
-    # that skips zero-weight rows reads)
-    wfull = g.grpo_loss_fwd(logits, w.P, ids, lens, adv, old, ref, w.eps, w.beta)["w"]
-    t_nonzero = int((wfull != 0).sum().item())
-    dlogits = torch.empty_like(logits)
-    out = None
-    ws = cur["workspace"]
+    b = Batch(g, w, dev)
     stream = torch.cuda.current_stream()
     fused = args.path == "fused"
+    flags = 1 if args.skip_zero_weight else None
 
     def step(record=None):
-        nonlocal out
-        if record is not None:
-            record[0].record(stream)
-        m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
-        a = g.grpo_advantage(R, w.G, adv)
-        if record is not None:
-            record[1].record(stream)
-        if fused:
-            out = g.grpo_loss_fwd_bwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, None,
-                                      out, ws, dlogits)
-            if record is not None:
-                record[2].record(stream)
-                record[3].record(stream)
-            return
-        out = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0, out, ws)
-        if record is not None:
-            record[2].record(stream)
-        g.grpo_loss_bwd(logits, w.P, ids, ln, out["lse"], out["w"], None, dlogits,
-                        flags=1 if args.skip_zero_weight else None)
-        if record is not None:
-            record[3].record(stream)
+        b.step(g, args.path, flags, record, stream)
 
     gpu_id = None
     try:
@@ -535,7 +748,7 @@ def run_ours(args, w0: wl.Workload):
         time.sleep(1.0)  # nvidia-smi needs a moment before its first sample
     for _ in range(max(args.warmup, 3)):
         step()
-    assert g.grpo_check_error(ws) == 0
+    assert g.grpo_check_error(b.ws) == 0
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -551,39 +764,6 @@ def run_ours(args, w0: wl.Workload):
     clocks = sampler.stop() if sampler is not None else None
     elapsed = start.elapsed_time(end) / 1e3
 
-    # the other path on the same inputs, for the record (its own byte count)
-    alt = None
-    if args.also_other_path and world == 1:
-        alt_fused = not fused
-        alt_out = {}
-        def alt_step():
-            m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
-            a = g.grpo_advantage(R, w.G, adv)
-            if alt_fused:
-                alt_out["o"] = g.grpo_loss_fwd_bwd(logits, w.P, ids, ln, a, old, ref, w.eps,
-                                                   w.beta, 0.0, None, alt_out.get("o"), ws, dlogits)
-            else:
-                o = g.grpo_loss_fwd(logits, w.P, ids, ln, a, old, ref, w.eps, w.beta, 0.0,
-                                    alt_out.get("o"), ws)
-                alt_out["o"] = o
-                g.grpo_loss_bwd(logits, w.P, ids, ln, o["lse"], o["w"], None, dlogits)
-        for _ in range(max(args.warmup, 3)):
-            alt_step()
-        torch.cuda.synchronize()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(args.steps):
-            alt_step()
-        s1.record(stream)
-        torch.cuda.synchronize()
-        alt_ms = s0.elapsed_time(s1) / args.steps
-        bb = algorithmic_bytes(w, t_valid)
-        alt_bytes = bb["step_logits_fused"] if alt_fused else bb["step_logits"]
-        alt = {"path": "fused" if alt_fused else "two_pass", "ms_per_step": alt_ms,
-               "value": t_valid / (alt_ms * 1e-3), "unit": UNIT,
-               "logits_bytes_per_step": alt_bytes,
-               "logits_gbs": alt_bytes / (alt_ms * 1e-3) / 1e9}
     # Per-call times, from a separate run with an event between the calls
     # (outside the timed region: an event between two launches keeps the
     # second from starting early, so these calls run one after the other).
@@ -595,92 +775,39 @@ def run_ours(args, w0: wl.Workload):
     t_mask = statistics.mean(e[0].elapsed_time(e[1]) for e in events) / 1e3
     t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in events) / 1e3
     t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in events) / 1e3
-    loss_val = float(out["loss"].item())
+    res = b.fout if fused else b.out
+    loss_val = float(res["loss"].item())
+    t_valid, t_nonzero, contrast = b.t_valid, b.t_nonzero, b.contrast_groups
 
-    # end to end through the public API: host inputs in, loss out.  The logits
-    # stay in pinned host memory and grpo_loss_fwd_bwd_host moves only the
-    # scored rows across the host link (into the device logits buffer, which
-    # serves as its staging buffer); ids, rewards and old/ref log-probs are
-    # copied in whole; the loss comes back.
-    h_logits = logits.cpu().pin_memory()
-    h_ids = ids.cpu().pin_memory()
-    h_R = R.cpu().pin_memory()
-    h_old = None if old is None else old.cpu().pin_memory()
-    h_ref = None if ref is None else ref.cpu().pin_memory()
-    h_loss = torch.empty((1,), dtype=torch.float32).pin_memory()
-    h2d = t_valid * w.V * logits.element_size() + sum(
-        t.numel() * t.element_size() for t in (h_ids, h_R, h_old, h_ref) if t is not None)
-    e2e_out = {}
+    # every logits path on the same inputs, for the record (each against its
+    # own byte count)
+    paths = None
+    if args.also_other_path and world == 1:
+        paths = path_summary(g, b, peak, args.steps, args.warmup, stream)
 
-    def e2e_enqueue():
-        ids.copy_(h_ids, non_blocking=True)
-        R.copy_(h_R, non_blocking=True)
-        if old is not None:
-            old.copy_(h_old, non_blocking=True)
-        if ref is not None:
-            ref.copy_(h_ref, non_blocking=True)
-        m, ln = g.grpo_mask(ids, w.P, w.C, w.eos_id, mask, lens)
-        a = g.grpo_advantage(R, w.G, adv)
-        e2e_out["o"] = g.grpo_loss_fwd_bwd_host(h_logits, w.P, ids, ln, a, old, ref, w.eps,
-                                                w.beta, 0.0, None, e2e_out.get("o"), ws,
-                                                dlogits, staging=logits)
-        h_loss.copy_(e2e_out["o"]["loss"], non_blocking=True)
+    e2e = None if args.no_e2e else run_e2e(args, g, b, stream, world, dist)
+    inputs = input_record(w, b.ids_np, b.R_np, b.logits)
 
-    def e2e_step():
-        e2e_enqueue()
-        stream.synchronize()
-
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
-
-    def time_e2e(step_fn):
-        # three timed loops of n_e2e steps; the median loop (one host stall of
-        # a few ms would otherwise move a 30 ms loop by a tenth)
-        for _ in range(2):
-            step_fn()
-        loops = []
-        for _ in range(3):
-            if world > 1:
-                dist.barrier()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(n_e2e):
-                step_fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            loops.append(e0.elapsed_time(e1) / 1e3)
-        return sorted(loops)[1]
-
-    e2e_eager_el = time_e2e(e2e_step)
-    # The same calls captured once into a CUDA graph and replayed each step
-    # (one launch instead of the copies and kernels one by one; the host
-    # still reads the loss back every step).
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            e2e_enqueue()
-    except Exception as ex:  # capture refused: keep the eager number
-        print(f"e2e graph capture failed: {ex!r}", file=sys.stderr)
-        graph = None
-        torch.cuda.synchronize()
-
-    def e2e_graph_step():
-        graph.replay()
-        stream.synchronize()
-
-    # every rank times a second pass (eager again where capture failed), so
-    # all ranks meet the same barriers
-    e2e_second = time_e2e(e2e_graph_step if graph is not None else e2e_step)
-    e2e_graph = e2e_second if graph is not None else None
-    e2e_el = e2e_eager_el if e2e_graph is None else e2e_graph
+    # the other workloads of the benchmark plan, one at a time, after this
+    # workload's buffers are released
+    per_config = None
+    if world == 1 and args.per_config != "none":
+        names = ([c.name for c in wl.CONFIGS[1:] if c.name != w0.name]
+                 if args.per_config == "auto" else args.per_config.split(","))
+        b.free()
+        per_config = {}
+        for name in names:
+            bc = Batch(g, wl.BY_NAME[name], dev)
+            per_config[name] = path_summary(g, bc, peak, args.steps, args.warmup, stream)
+            per_config[name]["inputs"] = input_record(bc.w, bc.ids_np, bc.R_np, bc.logits)
+            bc.free()
+    b = None
 
     # aggregate over ranks: units of all ranks / max time
     if world > 1:
-        t = torch.tensor([elapsed, e2e_el, e2e_eager_el], device=dev)
+        t = torch.tensor([elapsed], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed, e2e_el, e2e_eager_el = float(t[0]), float(t[1]), float(t[2])
+        elapsed = float(t[0])
         tv = torch.tensor([t_valid], device=dev, dtype=torch.int64)
         dist.all_reduce(tv)
         t_valid_all = int(tv.item())
@@ -704,19 +831,15 @@ def run_ours(args, w0: wl.Workload):
         cpu["cpu_model"] = cpu_model()
 
     if rank == 0:
-        peaks = measured_peaks()
-        peak = peaks.get("hbm_gbs")
-        peak_src = "measured" if peak else "fallback"
-        peak = peak or FALLBACK_HBM_GBS
-        b = algorithmic_bytes(w, t_valid, t_nonzero if args.skip_zero_weight else None)
+        bb = algorithmic_bytes(w, t_valid, t_nonzero if args.skip_zero_weight else None)
         ms = elapsed / args.steps
         if fused:
             # the fused call: prep + zero-row writer + lse_grad_kernel, timed together
-            step_bytes = b["step_logits_fused"]
-            kernel, kbytes, kt = "grpo_loss_fwd_bwd", b["fused"], t_fwd
+            step_bytes = bb["step_logits_fused"]
+            kernel, kbytes, kt = "grpo_loss_fwd_bwd", bb["fused"], t_fwd
         else:
-            step_bytes = b["step_logits"]
-            kernel, kbytes, kt = "dlogits_kernel", b["bwd"], t_bwd
+            step_bytes = bb["step_logits"]
+            kernel, kbytes, kt = "dlogits_kernel", bb["bwd"], t_bwd
         achieved = kbytes / kt / 1e9
         traffic = recorded_traffic(kernel, w)
         line = {
@@ -724,14 +847,14 @@ def run_ours(args, w0: wl.Workload):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "G": w.G, "P": w.P, "C": w.C, "V": w.V,
-                       "logits_dtype": w.dtype, "valid_tokens_per_rank": t_valid,
-                       "nonzero_weight_tokens_per_rank": t_nonzero,
-                       "groups_with_reward_contrast_per_rank": f"{contrast_groups}/{w.B}",
-                       "skip_zero_weight": bool(args.skip_zero_weight),
-                       "l2": f"inputs larger than L2 ({w.logits_bytes / 1e9:.2f} GB logits); "
-                             "no flush", "parallelism": f"dp{world} (independent groups)"},
+            "config": config_record(w0, world),
             "path": args.path,
+            "workload_stats": {"valid_tokens_per_rank": t_valid,
+                               "nonzero_weight_tokens_per_rank": t_nonzero,
+                               "groups_with_reward_contrast_per_rank": contrast,
+                               "groups_per_rank": w.B,
+                               "skip_zero_weight": bool(args.skip_zero_weight)},
+            "useful_groups_per_s": contrast * world / ms,
             "logits_gbs": step_bytes / ms / 1e9,
             "logits_roofline_frac": step_bytes / ms / 1e9 / peak,
             "logits_bytes_per_step": step_bytes,
@@ -739,26 +862,32 @@ def run_ours(args, w0: wl.Workload):
                           "bwd": t_bwd * 1e3},
             "kernel_timing": f"CUDA events between the calls over {n_inst} further steps on the "
                              "launching stream (the headline loop has events only at its ends)",
-            "fwd_gbs": (b["fused"] if fused else b["fwd"]) / t_fwd / 1e9,
+            "fwd_gbs": (bb["fused"] if fused else bb["fwd"]) / t_fwd / 1e9,
             "roofline": {"kernel": kernel, "bound": "hbm", "achieved": achieved,
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": kbytes},
-            "e2e": {"value": t_valid_all * n_e2e / e2e_el, "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
-                    "path": "grpo_mask + grpo_advantage + grpo_loss_fwd_bwd_host (logits in "
-                            "pinned host memory; only the scored rows cross the link)",
-                    "cuda_graph": e2e_graph is not None,
-                    "eager_value": t_valid_all * n_e2e / e2e_eager_el},
+            "e2e": None if e2e is None else {
+                "value": t_valid_all / e2e["s_per_step"], "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "path": "the single-pass call for host buffers: grpo_mask + grpo_advantage + "
+                        "grpo_loss_fwd_bwd_host (logits in pinned host memory, only the scored "
+                        "rows cross the host link; the kernels write the whole dlogits into "
+                        "pinned host memory across the link), then logp, w and the loss copied "
+                        "back",
+                "cuda_graph": e2e["cuda_graph"], "steps": e2e["steps"],
+                "eager_value": t_valid_all / e2e["eager_s_per_step"],
+                "results_match": e2e["results_match"]},
             "copy_ceiling_gbs": copy_gbs,
-            "other_path": None if alt is None else dict(
-                alt, logits_roofline_frac=alt["logits_gbs"] / peak),
+            "paths": paths,
+            "per_config": per_config,
             "gpu_launches": (KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP) * args.steps,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "loss": loss_val,
             "logits_nominal_frac": step_bytes / ms / 1e9 / NOMINAL_HBM_GBS,
-            "inputs": input_record(w, ids_np, R_np, logits),
+            "inputs": inputs,
             "env": run_env(dev),
         }
         print(json.dumps(line), flush=True)

@@ -321,9 +321,17 @@ grpo_status grpo_loss_fwd_bwd(const void *logits, grpo_dtype dtype, int64_t N, i
  *
  * Arguments: those of grpo_loss_fwd_bwd with host_logits for logits, plus
  * staging (device, logits' size, element-aligned, not overlapping dlogits).
- * The other pointers are device memory as for grpo_loss_fwd_bwd.  Returns
- * GRPO_ERR_INVALID_ARG when host_logits is not page-locked host memory the
- * device can address.
+ * dlogits may be device memory or, like host_logits, page-locked host memory
+ * mapped into the device's address space: the kernels then write every row
+ * of the gradient (zero rows included) straight into it across the host link,
+ * while the scored rows of the logits come the other way (the results are
+ * the same bits; completion of the stream work means the host buffer holds
+ * them).  The other pointers are device memory as for grpo_loss_fwd_bwd.
+ * Returns GRPO_ERR_INVALID_ARG when host_logits (or a host dlogits) is not
+ * page-locked host memory the device can address over its whole size
+ * (N*(P+C)*V elements: the first and the last byte are checked), when
+ * dlogits is pageable host memory, or when a host dlogits overlaps
+ * host_logits.
  */
 grpo_status grpo_loss_fwd_bwd_host(const void *host_logits, grpo_dtype dtype, int64_t N,
                                    int64_t P, int64_t C, int64_t V, const int64_t *input_ids,

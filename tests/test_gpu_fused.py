@@ -147,11 +147,12 @@ def test_fused_full_size_same_bits(w):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("host_dl", [False, True], ids=["dev_dlogits", "host_dlogits"])
 @pytest.mark.parametrize("dtype,V,shift", [("bf16", 1024, 0), ("bf16", 1001, 0), ("f32", 1001, 0),
                                            ("bf16", 1024, 1), ("f32", 1001, 1)],
                          ids=["bf16_vec16", "bf16_odd_V", "f32_odd_V", "bf16_host_phase_shift",
                               "f32_host_phase_shift"])
-def test_host_logits_match_device_path(dtype, V, shift):
+def test_host_logits_match_device_path(dtype, V, shift, host_dl):
     """grpo_loss_fwd_bwd_host on pinned host logits gives the bits of
     grpo_loss_fwd_bwd on the same logits in device memory, and only the
     scored rows of the staging buffer are written.  With the host buffer in
@@ -177,13 +178,17 @@ def test_host_logits_match_device_path(dtype, V, shift):
         host = buf[shift:].view(logits.shape)
         host.copy_(logits)
         assert host.is_pinned() and host.data_ptr() % 16 != 0
+    dl_out = None
+    if host_dl:  # the gradient written straight into pinned host memory
+        dl_out = torch.full(logits.shape, 5.0, dtype=logits.dtype).pin_memory()
     b = n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, old, None, 0.2, 0.0,
-                                 staging=staging)
+                                 staging=staging, dlogits=dl_out)
     assert n.grpo_check_error(b["workspace"]) == 0
+    assert b["dlogits"].is_cuda != host_dl
     for k in ("logp", "lse", "w", "loss"):
         assert torch.equal(a[k], b[k]), k
-    assert torch.equal(a["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32),
-                       b["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32))
+    assert torch.equal(a["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32).cpu(),
+                       b["dlogits"].view(torch.int16 if dtype == "bf16" else torch.int32).cpu())
     L = lens.cpu().numpy()
     scored = np.zeros((w.N, w.T), bool)
     for i in range(w.N):
@@ -268,6 +273,51 @@ def test_host_logits_registered_too_short():
     assert torch.equal(_bits(ref["dlogits"]), _bits(dl))
 
 
+def test_host_dlogits_refused_when_short_or_pageable():
+    """A host dlogits buffer must be page-locked over the whole gradient:
+    pageable memory, a buffer page-locked over only its first part, and one
+    overlapping the host logits are refused before anything is enqueued."""
+    n = H.g()
+    w = H.with_contrast(wl.variant(wl.QWEN_G8, name="short_dl", B=2, G=4, P=6, C=26, V=1024,
+                                   eos_id=1023, seed=93))
+    host = wl.make_logits_cpu(w).pin_memory()
+    t_ids = H.dev(wl.make_ids(w))
+    _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(wl.make_rewards(w)), w.G)
+    nbytes = host.numel() * 2
+    raw = np.zeros(nbytes + 4096, np.uint8)
+    off = (-raw.ctypes.data) % 4096
+    buf = raw[off:off + nbytes]
+    dl_view = torch.from_numpy(buf).view(torch.bfloat16).view(host.shape)
+    # pageable: the binding refuses it, and so does the library
+    with pytest.raises(ValueError):
+        n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, dlogits=dl_view)
+    import ctypes
+    lib = n.library()
+    ws = torch.zeros((n.grpo_workspace_size(w.N, w.C, w.V),), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((w.N, w.C), device="cuda") for _ in range(3)] + \
+        [torch.empty((1,), device="cuda")]
+    st = torch.empty(host.shape, dtype=host.dtype, device="cuda")
+    p = ctypes.c_void_p
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call(dl_ptr):
+        return lib.grpo_loss_fwd_bwd_host(
+            p(host.data_ptr()), 1, w.N, w.P, w.C, w.V, p(t_ids.data_ptr()), p(lens.data_ptr()),
+            p(adv.data_ptr()), None, None, 0.2, 0.0, 0.0, None, *[p(t.data_ptr()) for t in outs],
+            p(dl_ptr), p(st.data_ptr()), p(ws.data_ptr()), ws.numel(), p(stream))
+
+    assert call(buf.ctypes.data) == 1
+    cudart = torch.cuda.cudart()
+    assert int(cudart.cudaHostRegister(buf.ctypes.data, nbytes // 2, 3)) == 0
+    try:
+        assert call(buf.ctypes.data) == 1   # page-locked over half its size only
+    finally:
+        assert int(cudart.cudaHostUnregister(buf.ctypes.data)) == 0
+    assert call(host.data_ptr() + 4096) == 1  # overlaps the host logits
+    torch.cuda.synchronize()
+
+
 def test_host_logits_full_size_same_bits():
     """The benchmark workload (V = 151,936, whole rows per CTA) with the logits
     in pinned host memory: the gradient kernel reads the scored rows from host
@@ -280,7 +330,8 @@ def test_host_logits_full_size_same_bits():
     _, lens = n.grpo_mask(t_ids, w.P, w.C, w.eos_id)
     adv = n.grpo_advantage(torch.from_numpy(wl.make_rewards(w)).cuda(), w.G)
     a = n.grpo_loss_fwd_bwd(logits, w.P, t_ids, lens, adv, None, None, 0.2, 0.0)
-    host = logits.cpu().pin_memory()
+    host = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    host.copy_(logits)
     staging = torch.empty_like(logits)
     b = n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, None, None, 0.2, 0.0,
                                  staging=staging)
@@ -289,5 +340,13 @@ def test_host_logits_full_size_same_bits():
     for k in ("logp", "lse", "w", "loss"):
         assert torch.equal(_bits(a[k]), _bits(b[k])), k
     assert torch.equal(_bits(a["dlogits"]), _bits(b["dlogits"]))
-    del logits, staging, host, a, b
+    # the gradient written straight into pinned host memory: the same bits
+    h_dl = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    c = n.grpo_loss_fwd_bwd_host(host, w.P, t_ids, lens, adv, None, None, 0.2, 0.0,
+                                 staging=staging, dlogits=h_dl)
+    torch.cuda.synchronize()
+    assert n.grpo_check_error(c["workspace"]) == 0
+    assert torch.equal(_bits(a["loss"]), _bits(c["loss"]))
+    assert torch.equal(_bits(a["dlogits"]).cpu(), _bits(h_dl))
+    del logits, staging, host, a, b, c, h_dl
     torch.cuda.empty_cache()

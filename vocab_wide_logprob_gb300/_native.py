@@ -346,8 +346,10 @@ def grpo_loss_fwd_bwd_host(host_logits, P, input_ids, lens, adv, old_logp=None, 
     """:func:`grpo_loss_fwd_bwd` for logits in page-locked host memory
     (``host_logits`` a pinned CPU tensor): only the scored rows cross the
     host link, into the same rows of ``staging`` (a device tensor of the
-    logits' shape, allocated when None).  Returns the dict of
-    :func:`grpo_loss_fwd_bwd` plus ``staging``."""
+    logits' shape, allocated when None).  ``dlogits`` may be a device tensor
+    or a pinned CPU tensor (the kernels then write the gradient across the
+    host link).  Returns the dict of :func:`grpo_loss_fwd_bwd` plus
+    ``staging``."""
     if host_logits.is_cuda or not host_logits.is_pinned() or not host_logits.is_contiguous():
         raise ValueError("host_logits must be a contiguous pinned CPU tensor")
     N, T, V = host_logits.shape
@@ -370,7 +372,12 @@ def grpo_loss_fwd_bwd_host(host_logits, P, input_ids, lens, adv, old_logp=None, 
         dlogits = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
     if staging is None:
         staging = torch.empty(host_logits.shape, dtype=host_logits.dtype, device=dev)
-    _dev(dlogits, "dlogits", host_logits.dtype)
+    if dlogits.is_cuda:
+        _dev(dlogits, "dlogits", host_logits.dtype)
+    elif (not dlogits.is_pinned() or not dlogits.is_contiguous()
+          or dlogits.dtype != host_logits.dtype or dlogits.shape != host_logits.shape):
+        raise ValueError("dlogits must be a CUDA tensor or a contiguous pinned CPU tensor of "
+                         "the logits' shape and dtype")
     _dev(staging, "staging", host_logits.dtype)
     out.update(workspace=workspace, dlogits=dlogits, staging=staging)
     _check(_lib.grpo_loss_fwd_bwd_host(

@@ -615,28 +615,47 @@ grpo_status grpo_loss_fwd_bwd_host(const void* host_logits, grpo_dtype dtype, in
                                    size_t workspace_bytes, grpo_stream_t stream) {
   grpo_status s = check_shapes(dtype, N, P, C, V);
   if (s != GRPO_OK) return s;
+  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
+  const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
+  // dlogits: device memory, or page-locked host memory (all of it) that the
+  // kernels write through its device mapping, across the host link
+  void* dl_dev = dlogits;
+  bool dl_host = false;
+  if (dlogits != nullptr && bytes > 0) {
+    cudaPointerAttributes da;
+    if (cudaPointerGetAttributes(&da, dlogits) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GRPO_ERR_INVALID_ARG;
+    }
+    if (da.type == cudaMemoryTypeUnregistered) return GRPO_ERR_INVALID_ARG;  // pageable
+    if (da.type == cudaMemoryTypeHost) {
+      s = host_range(dlogits, bytes, &dl_dev);
+      if (s != GRPO_OK) return s;
+      dl_host = true;
+    }
+  }
   if (N == 0 || C == 0)
     return grpo_loss_fwd_bwd(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp,
-                             eps, beta, norm, grad_loss, logp, lse, w, loss, dlogits, workspace,
+                             eps, beta, norm, grad_loss, logp, lse, w, loss, dl_dev, workspace,
                              workspace_bytes, stream);
   if (host_logits == nullptr || staging == nullptr || len == nullptr || workspace == nullptr)
     return GRPO_ERR_INVALID_ARG;
-  const size_t esize = dtype == GRPO_F32 ? 4 : 2;
   if (!aligned(host_logits, esize) || !aligned(staging, esize) || !aligned(len, 4) ||
       !aligned(workspace, 256))
     return GRPO_ERR_MISALIGNED;
   if (workspace_bytes < ws_layout(N).total) return GRPO_ERR_WORKSPACE;
   // the logits must be page-locked host memory the device can address, all
   // of it: the kernels read any scored row, up to the last byte
-  const size_t bytes = (size_t)mul3(N, P + C, V) * esize;
   void* host_dev = nullptr;
   s = host_range(host_logits, bytes, &host_dev);
   if (s != GRPO_OK) return s;
-  const char* sg = static_cast<const char*>(staging);
+  // dlogits overlaps neither the logits nor the staging buffer
   const char* dl = static_cast<const char*>(dlogits);
-  if (dlogits != nullptr && dl < sg + bytes && sg < dl + bytes) return GRPO_ERR_INVALID_ARG;
+  const char* other = dl_host ? static_cast<const char*>(host_logits)
+                              : static_cast<const char*>(staging);
+  if (dlogits != nullptr && dl < other + bytes && other < dl + bytes) return GRPO_ERR_INVALID_ARG;
   return fwd_bwd_impl(staging, dtype, N, P, C, V, input_ids, len, adv, old_logp, ref_logp, eps,
-                      beta, norm, GRPO_AGG_TOKEN_SUM, grad_loss, logp, lse, w, loss, dlogits,
+                      beta, norm, GRPO_AGG_TOKEN_SUM, grad_loss, logp, lse, w, loss, dl_dev,
                       workspace, workspace_bytes, stream, host_dev);
 }
 
