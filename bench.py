@@ -86,6 +86,9 @@ def parse_args():
                    help="skip timing every logits path of the main workload for the record")
     p.add_argument("--hidden", type=int, default=896,
                    help="hidden size of the LM-head paths (Qwen2.5-0.5B: 896)")
+    p.add_argument("--lmhead-rows-per-pass", type=int, default=-1,
+                   help="LM-head backward: rows per pass of its workspace (-1: the scored "
+                        "rows present, one pass over them; 0: every possible row)")
     return p.parse_args()
 
 
@@ -931,8 +934,14 @@ def run_lmhead(args, w: wl.Workload):
         adv = g.grpo_advantage(R, w.G)
         fwd = g.grpo_lmhead_loss_fwd(hidden, weight, w.P, ids, lens, adv, old, ref, w.eps, w.beta)
         bflags = 1 if args.skip_zero_weight else None
+        # the backward's workspace sized by the scored rows actually present
+        # (one pass over them), not by every possible row
         dh, dw, bws = g.grpo_lmhead_loss_bwd(hidden, weight, w.P, ids, lens, fwd["lse"], fwd["w"],
-                                             flags=bflags)
+                                             flags=bflags,
+                                             rows_per_pass=(t_valid if args.lmhead_rows_per_pass < 0
+                                                            else args.lmhead_rows_per_pass))
+        bwd_ws_bytes = bws.numel()
+        bwd_ws_full = g.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, d)
         t_nonzero = int((fwd["w"] != 0).sum().item())
 
     def step_fwd():
@@ -1018,6 +1027,8 @@ def run_lmhead(args, w: wl.Workload):
         line["bwd_tflops"] = 3 * 2.0 * bwd_rows * w.V * d / (ms_bwd * 1e-3) / 1e12
         line["config"]["nonzero_weight_tokens"] = t_nonzero
         line["config"]["skip_zero_weight"] = bool(args.skip_zero_weight)
+        line["bwd_workspace_bytes"] = bwd_ws_bytes
+        line["bwd_workspace_bytes_every_possible_row"] = bwd_ws_full
     print(json.dumps(line), flush=True)
 
 

@@ -409,14 +409,29 @@ grpo_status grpo_lmhead_loss_fwd_ex(const void *hidden, const void *weight, int6
  * hidden, weight, N, P, C, V, d, input_ids, len as for grpo_lmhead_logprobs;
  * lse, w [N, C] float32 from the forward; grad_loss: device scalar (NULL: 1).
  * dhidden [N, P+C, d] float32 and dweight [V, d] float32, 16-byte aligned,
- * fully written (accumulate into your own buffers yourself).  workspace: at
- * least grpo_lmhead_bwd_workspace_size bytes; it holds the dense scored
- * hidden rows, the bfloat16 logits gradient of every possible scored row
- * (2 * N * C * V bytes, V rounded up to 256) and the split partials of
- * dhidden.  Results are deterministic (fixed summation orders).
+ * fully written (accumulate into your own buffers yourself).
+ *
+ * Workspace and passes: the scored rows are processed in passes of up to R
+ * rows (R a multiple of 256): each pass recomputes its rows' logits, forms
+ * their bfloat16 gradient in the workspace (2 * R * V bytes, V rounded up to
+ * 256) and runs both contractions over it; dweight is written by the first
+ * pass and added to by the others (a tensor-memory-accelerator reduction, in
+ * pass order).  The call takes R as large as `workspace_bytes` allows, so
+ * grpo_lmhead_bwd_workspace_size (R covering all N*C possible rows: one pass)
+ * and grpo_lmhead_bwd_workspace_size_rows(..., rows_per_pass) (R =
+ * rows_per_pass rounded up to 256; 0 means all N*C) both give valid sizes;
+ * the smallest accepted workspace is the one for R = 256.  A caller that
+ * knows the number of scored tokens T (the sum of len) can pass
+ * rows_per_pass = T for one pass over a workspace sized by the rows that are
+ * actually scored; more scored rows than that only add passes.  Results are
+ * deterministic for a given workspace size (fixed summation orders); a
+ * different R changes the order of dweight's (and dhidden's) float sums, so
+ * results agree to float rounding.
  */
 grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
                                            size_t *bytes);
+grpo_status grpo_lmhead_bwd_workspace_size_rows(int64_t N, int64_t C, int64_t V, int64_t d,
+                                                int64_t rows_per_pass, size_t *bytes);
 grpo_status grpo_lmhead_loss_bwd(const void *hidden, const void *weight, int64_t N, int64_t P,
                                  int64_t C, int64_t V, int64_t d, const int64_t *input_ids,
                                  const int32_t *len, const float *lse, const float *w,

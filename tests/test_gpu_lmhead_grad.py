@@ -286,3 +286,71 @@ def test_lmhead_loss_seq_mean_and_its_gradients():
     gr = oracle.lmhead_grads(Hn, Wn, w.P, w.C, ids, len_o, lse_o, w_o, 1.0, magnitudes=True)
     assert_grad(dh.cpu().numpy(), gr["dhidden"], gr["dhidden_mag"], "dhidden")
     assert_grad(dw.cpu().numpy(), gr["dweight"], gr["dweight_mag"], "dweight")
+
+
+PASSES = wl.variant(wl.QWEN_G16_KL, name="lmg_passes", B=2, G=8, P=5, C=100, V=4099,
+                    eos_id=4000, seed=84)
+# beta = 0 and a second group without reward contrast: with the skip flag its
+# rows (every weight 0) take no part, so the passes hold only group 0's rows
+PASSES_SKIP = wl.variant(PASSES, name="lmg_passes_skip", beta=0.0, ref_sigma=None,
+                         forced={"rewards": [1.0, 0.0, 0.0, 1.0, 0.0, 1.0, 0.0, 0.0] + [0.0] * 8})
+
+
+@pytest.mark.parametrize("rows_per_pass,flags,wk", [(256, None, PASSES), (512, None, PASSES),
+                                                    (256, 1, PASSES_SKIP), (0, 1, PASSES_SKIP)],
+                         ids=["R256", "R512", "R256_skip", "one_pass_skip"])
+def test_lmhead_grads_in_passes(rows_per_pass, flags, wk):
+    """The backward in passes of 256 or 512 rows (several passes with rows,
+    a ragged last one, and passes with none) against the oracle element by
+    element: each pass stores or adds its part of dweight and writes its rows
+    of dhidden."""
+    n = H.g()
+    w = H.with_contrast(wk)
+    hidden, weight, t_ids, lens, out, h = _setup(w, 384)
+    T_valid = int(h["len"].sum())
+    assert T_valid > 2 * 256 + 1 and T_valid % 256 != 0
+    g = 2.5
+    gt = torch.tensor([g], dtype=torch.float32, device="cuda")
+    need = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384, rows_per_pass)
+    full = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384)
+    assert (need < full) == (rows_per_pass > 0)
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    dh, dw, _ = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                                       gt, workspace=ws, flags=flags)
+    assert n.grpo_check_error(ws) == 0
+    gr = oracle.lmhead_grads(h["Hn"], h["Wn"], w.P, w.C, h["ids"], h["len"], h["lse"], h["w"], g,
+                             magnitudes=True)
+    assert_grad(dh.cpu().numpy(), gr["dhidden"], gr["dhidden_mag"], "dhidden")
+    assert_grad(dw.cpu().numpy(), gr["dweight"], gr["dweight_mag"], "dweight")
+    # a second call on the same workspace gives the same bits (dweight is
+    # stored again by the first pass, not added to the last call's)
+    dh2, dw2, _ = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                                         gt, workspace=ws, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(dh.view(torch.int32), dh2.view(torch.int32))
+    assert torch.equal(dw.view(torch.int32), dw2.view(torch.int32))
+
+
+def test_lmhead_grads_workspace_by_scored_rows():
+    """A workspace sized for the scored rows actually present (their count
+    rounded up to 256) runs one pass with rows; one smaller than a single
+    256-row pass is refused."""
+    n = H.g()
+    w = H.with_contrast(PASSES)
+    hidden, weight, t_ids, lens, out, h = _setup(w, 384)
+    T_valid = int(h["len"].sum())
+    ws = torch.empty((n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384, T_valid),),
+                     dtype=torch.uint8, device="cuda")
+    a = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                               workspace=ws)
+    b = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"])
+    torch.cuda.synchronize()
+    # the same single pass over the scored rows: the same bits as the
+    # workspace for every possible row
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    small = torch.empty((n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384, 256) - 1,),
+                        dtype=torch.uint8, device="cuda")
+    with pytest.raises(n.GrpoError):
+        n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
+                               workspace=small)

@@ -76,6 +76,8 @@ def _load():
         "grpo_lmhead_loss_fwd_ex": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, F, F, F, INT, P,
                                      P, P, P, P, SZ, P], INT),
         "grpo_lmhead_bwd_workspace_size": ([I64, I64, I64, I64, ctypes.POINTER(SZ)], INT),
+        "grpo_lmhead_bwd_workspace_size_rows": ([I64, I64, I64, I64, I64, ctypes.POINTER(SZ)],
+                                                INT),
         "grpo_lmhead_loss_bwd_ex": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P,
                                      ctypes.c_uint32, P, SZ, P], INT),
         "grpo_lmhead_loss_bwd": ([P, P, I64, I64, I64, I64, I64, P, P, P, P, P, P, P, P, SZ, P],
@@ -465,11 +467,24 @@ def grpo_lmhead_loss_fwd(hidden, weight, P, input_ids, lens, adv, old_logp=None,
     return out
 
 
+def grpo_lmhead_bwd_workspace_size(N: int, C: int, V: int, d: int, rows_per_pass: int = 0) -> int:
+    """Bytes of the LM-head backward's workspace for passes of
+    ``rows_per_pass`` backward rows (0: one pass over all N*C)."""
+    out = ctypes.c_size_t(0)
+    _check(_lib.grpo_lmhead_bwd_workspace_size_rows(N, C, V, d, int(rows_per_pass),
+                                                    ctypes.byref(out)),
+           "grpo_lmhead_bwd_workspace_size_rows")
+    return int(out.value)
+
+
 def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=None, out=None,
-                         workspace=None, stream=None, flags=None):
+                         workspace=None, stream=None, flags=None, rows_per_pass=0):
     """Gradients of ``grad_loss * loss`` with respect to the hidden states and
     the LM head.  Returns ``(dhidden [N, P+C, d], dweight [V, d], workspace)``,
-    float32; ``out`` = (dhidden, dweight) to reuse buffers."""
+    float32; ``out`` = (dhidden, dweight) to reuse buffers.  Without a
+    ``workspace`` one is allocated for passes of ``rows_per_pass`` rows (0:
+    one pass over every possible row); a given workspace sets the passes by
+    its size."""
     _dev(hidden, "hidden", torch.bfloat16)
     _dev(weight, "weight", torch.bfloat16)
     for name, t, dt in (("input_ids", input_ids, torch.int64), ("lens", lens, torch.int32),
@@ -483,11 +498,9 @@ def grpo_lmhead_loss_bwd(hidden, weight, P, input_ids, lens, lse, w, grad_loss=N
     if out is None:
         out = (torch.empty((N, T, d), dtype=torch.float32, device=dev),
                torch.empty((V, d), dtype=torch.float32, device=dev))
-    need = ctypes.c_size_t(0)
-    _check(_lib.grpo_lmhead_bwd_workspace_size(N, C, V, d, ctypes.byref(need)),
-           "grpo_lmhead_bwd_workspace_size")
-    if workspace is None or workspace.numel() < need.value:
-        workspace = torch.empty((need.value,), dtype=torch.uint8, device=dev)
+    if workspace is None:
+        need = grpo_lmhead_bwd_workspace_size(N, C, V, d, rows_per_pass)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     head = (_ptr(hidden), _ptr(weight), N, P, C, V, d, _ptr(input_ids), _ptr(lens), _ptr(lse),
             _ptr(w), _ptr(grad_loss), _ptr(out[0]), _ptr(out[1]))
     tail = (_ptr(workspace), workspace.numel(), _stream(stream))

@@ -793,16 +793,22 @@ grpo_status grpo_lmhead_loss_fwd_ex(const void* hidden, const void* weight, int6
                          stream, 1);
 }
 
-grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
-                                           size_t* bytes) {
-  if (bytes == nullptr || N < 0 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+grpo_status grpo_lmhead_bwd_workspace_size_rows(int64_t N, int64_t C, int64_t V, int64_t d,
+                                                int64_t rows_per_pass, size_t* bytes) {
+  if (bytes == nullptr || N < 0 || C < 0 || V < 1 || rows_per_pass < 0)
+    return GRPO_ERR_INVALID_ARG;
   if (d < 128 || d % 128 != 0) return GRPO_ERR_UNSUPPORTED;
   if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;
   if (V > (int64_t)INT32_MAX - 256) return GRPO_ERR_UNSUPPORTED;
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
-  *bytes = lm_bwd_layout(N, C, V, d, dev.sms).total;
+  *bytes = lm_bwd_layout(N, C, V, d, dev.sms, rows_per_pass).total;
   return GRPO_OK;
+}
+
+grpo_status grpo_lmhead_bwd_workspace_size(int64_t N, int64_t C, int64_t V, int64_t d,
+                                           size_t* bytes) {
+  return grpo_lmhead_bwd_workspace_size_rows(N, C, V, d, 0, bytes);
 }
 
 grpo_status grpo_lmhead_loss_bwd(const void* hidden, const void* weight, int64_t N, int64_t P,
@@ -830,7 +836,19 @@ grpo_status grpo_lmhead_loss_bwd_ex(const void* hidden, const void* weight, int6
     return GRPO_ERR_MISALIGNED;
   DeviceInfo dev;
   if (current_device(&dev) != cudaSuccess) return GRPO_ERR_CUDA;
-  if (workspace_bytes < lm_bwd_layout(N, C, V, d, dev.sms).total) return GRPO_ERR_WORKSPACE;
+  // rows per pass: as many as the workspace holds (every possible row when it
+  // is grpo_lmhead_bwd_workspace_size bytes), at least one block of 256
+  const int64_t blocks = (N * C + 255) / 256;
+  int64_t lo = 1, hi = blocks > 0 ? blocks : 1;
+  if (workspace_bytes < lm_bwd_layout(N, C, V, d, dev.sms, 256).total) return GRPO_ERR_WORKSPACE;
+  while (lo < hi) {  // the layout grows with the rows per pass
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (lm_bwd_layout(N, C, V, d, dev.sms, mid * 256).total <= workspace_bytes)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const LmBwdLayout bl = lm_bwd_layout(N, C, V, d, dev.sms, lo * 256);
   stream_take_after_fwd(stream);
   FwdArgs f = {};
   f.N = N;
@@ -862,10 +880,15 @@ grpo_status grpo_lmhead_loss_bwd_ex(const void* hidden, const void* weight, int6
   a.dhidden = dhidden;
   a.dweight = dweight;
   a.ws = workspace;
+  a.rows_pass = bl.rows_pass;
   a.skip_zero_weight = (flags & GRPO_BWD_SKIP_ZERO_WEIGHT) != 0;
-  cudaError_t e = launch_lmhead_dz(a, dev, st);
-  if (e != cudaSuccess) return GRPO_ERR_CUDA;
-  return from_cuda(launch_lmhead_grads(a, dev, st));
+  if (launch_lmhead_bwd_rows(a, dev, st) != cudaSuccess) return GRPO_ERR_CUDA;
+  for (int64_t pass = 0; pass < bl.npass; ++pass) {
+    if (launch_lmhead_dz(a, pass, dev, st) != cudaSuccess) return GRPO_ERR_CUDA;
+    cudaError_t e = launch_lmhead_grads(a, pass, dev, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return GRPO_OK;
 }
 
 grpo_status grpo_check_error(const void* workspace, grpo_stream_t stream) {

@@ -45,7 +45,10 @@ constexpr int kDzSmem = kLmSmem + 8 * 4096;  // + two 2 KiB TMA-store boxes per 
 struct LmParams {
   int64_t N, P, C, V, d;
   const int32_t* offsets;  // prefix sums of the clamped lengths ([N+1])
-  int4* geometry;          // [0] (row blocks, splits, tiles per split): written by the gather
+  int4* geometry;          // [geo_index] (row blocks, splits, tiles per split): by the gather
+  int geo_index;           // forward: 0; backward pass p: 3 + 2p
+  int64_t row0;            // backward: the pass's first row (forward: 0)
+  int64_t rows_pass;       // backward: rows per pass
   float4* partials;        // forward: [items][256] (max, sum, target logit, has target)
   uint32_t* counters;      // forward: partials written per row (zeroed by the gather)
   float* logp_out;         // forward: [N, C]
@@ -57,6 +60,11 @@ struct LmParams {
   const float* grad;       // upstream scalar gradient (nullable: 1)
   const int32_t* rowmap;   // the token i*C + t of each backward row (geometry[2].x rows)
 };
+
+// Backward rows of pass `pass` out of `rows` in passes of `rows_pass`.
+__device__ __forceinline__ int64_t pass_rows(int64_t rows, int64_t row0, int64_t rows_pass) {
+  return rows <= row0 ? 0 : (rows - row0 < rows_pass ? rows - row0 : rows_pass);
+}
 
 // Split `ksteps` steps of work for each of `units` independent tiles into
 // `splits` ranges so that the items (unit, range) fill the grid's rounds,
@@ -217,27 +225,32 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 // Dense copy of the backward rows' hidden states (zero rows up to the next
-// multiple of 256), geometry[0] for the projection pass and geometry[1] for
-// the hidden-state gradient contraction (256-row blocks, 512-wide d tiles,
-// vocabulary splits, 64-wide k-steps per split).
+// multiple of 256) and, for every pass of rows_pass rows, the geometries of
+// the projection pass (geometry[3 + 2p]: 256-row blocks, vocabulary splits,
+// tiles per split) and of the hidden-state gradient contraction
+// (geometry[4 + 2p]: 256-row blocks, 512-wide d tiles, vocabulary splits,
+// 64-wide k-steps per split).
 __global__ void __launch_bounds__(kThreads)
     gather_active_rows_kernel(const uint16_t* __restrict__ hidden, uint16_t* __restrict__ dense,
                               const int32_t* __restrict__ rowmap, int64_t C, int64_t T, int64_t P,
-                              int64_t d, int64_t V, int pairs, int4* __restrict__ geometry) {
+                              int64_t d, int64_t V, int pairs, int64_t rows_pass, int64_t npass,
+                              int4* __restrict__ geometry) {
   pdl_wait();
   pdl_trigger();
   const int64_t rows = geometry[2].x;
   const int32_t mb = (int32_t)((rows + kRows - 1) / kRows);
-  if (blockIdx.x == 0) {
+  for (int64_t pass = blockIdx.x; pass < npass; pass += gridDim.x) {  // uniform per CTA
+    const int64_t rp = pass_rows(rows, pass * rows_pass, rows_pass);
+    const int32_t mbp = (int32_t)((rp + kRows - 1) / kRows);
     const int32_t ntiles = (int32_t)((V + kVTile - 1) / kVTile);
-    const int2 s = choose_split_block(mb, ntiles, pairs, 4 * pairs + 2 * mb);
-    if (threadIdx.x == 0) geometry[0] = make_int4(mb, s.x, s.y, 0);
-  }
-  if (blockIdx.x == (gridDim.x > 1 ? 1u : 0u)) {
+    const int2 s0 = choose_split_block(mbp, ntiles, pairs, 4 * pairs + 2 * mbp);
     const int32_t nb = (int32_t)((d + 511) / 512);
-    const int32_t ksteps = (int32_t)((V + kVTile - 1) / kVTile) * (kVTile / kK);
-    const int2 s = choose_split_block(mb * nb, ksteps, pairs, 2 * pairs + mb * nb);
-    if (threadIdx.x == 0) geometry[1] = make_int4(mb, nb, s.x, s.y);
+    const int32_t ksteps = ntiles * (kVTile / kK);
+    const int2 s1 = choose_split_block(mbp * nb, ksteps, pairs, 2 * pairs + mbp * nb);
+    if (threadIdx.x == 0) {
+      geometry[3 + 2 * pass] = make_int4(mbp, s0.x, s0.y, 0);
+      geometry[4 + 2 * pass] = make_int4(mbp, nb, s1.x, s1.y);
+    }
   }
   const int64_t vec_per_row = d / 8;  // 16-byte vectors
   const int64_t rows_pad = (int64_t)mb * kRows;
@@ -298,8 +311,9 @@ struct LmOp {
   uint32_t chunk;
 
   __device__ void setup() {
-    tv = kMode == 1 ? (int64_t)p.geometry[2].x : (int64_t)p.offsets[p.N];  // rows of the pass
-    const int4 geo = p.geometry[0];
+    tv = kMode == 1 ? pass_rows(p.geometry[2].x, p.row0, p.rows_pass)  // rows of the pass
+                    : (int64_t)p.offsets[p.N];
+    const int4 geo = p.geometry[p.geo_index];
     mb = geo.x;
     splits = geo.y;
     tps = geo.z;
@@ -322,7 +336,7 @@ struct LmOp {
   __device__ void load(uint32_t sa, int64_t it, int t, int64_t ks, uint32_t rk,
                        uint32_t mbar) const {
     const int64_t rb = it / splits, n = first_tile(it) + t;
-    tma_load_2d_pair(sa, map_h, (int)(ks * kK), (int)(rb * kRows + rk * 128), mbar);
+    tma_load_2d_pair(sa, map_h, (int)(ks * kK), (int)(p.row0 + rb * kRows + rk * 128), mbar);
     tma_load_2d_pair(sa + kPairBOffset, map_w, (int)(ks * kK), (int)(n * kVTile + rk * 128),
                      mbar);
   }
@@ -343,7 +357,7 @@ struct LmOp {
     if (r < tv) {
       int64_t i, t;
       if (kMode == 1) {  // the backward's rows: the row map
-        const int64_t tok = p.rowmap[r];
+        const int64_t tok = p.rowmap[p.row0 + r];
         i = tok / p.C;
         t = tok - i * p.C;
       } else {           // every scored token, in order
@@ -570,6 +584,9 @@ LmParams lm_params(const int32_t* off, int4* geometry, WsHeader* hdr, int64_t N,
   p.d = d;
   p.offsets = off;
   p.geometry = geometry;
+  p.geo_index = 0;
+  p.row0 = 0;
+  p.rows_pass = INT64_MAX;
   p.hdr = hdr;
   return p;
 }
@@ -648,21 +665,26 @@ LmLayout lm_layout(int64_t N, int64_t C, int64_t d, int sms) {
   return l;
 }
 
-LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms) {
+LmBwdLayout lm_bwd_layout(int64_t N, int64_t C, int64_t V, int64_t d, int sms,
+                          int64_t rows_pass) {
   LmBwdLayout l;
   const WsLayout base = ws_layout(N);
   const int64_t mb_max = (N * C + kRows - 1) / kRows;
   const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
   l.rows_cap = mb_max * kRows;
+  l.rows_pass = rows_pass <= 0 ? l.rows_cap : (rows_pass + kRows - 1) / kRows * kRows;
+  if (l.rows_pass > l.rows_cap) l.rows_pass = l.rows_cap;
+  l.npass = l.rows_pass > 0 ? (l.rows_cap + l.rows_pass - 1) / l.rows_pass : 1;
+  if (l.npass < 1) l.npass = 1;
   l.ldz = (V + kVTile - 1) / kVTile * kVTile;
   const int64_t nb = (d + 511) / 512;  // d tiles of the hidden-state gradient
-  l.items_max = 2 * pairs + mb_max * nb;
+  l.items_max = 2 * pairs + (l.rows_pass / kRows) * nb;
   l.geometry = base.total;
-  l.rowmap = align_up(base.total + 48, 256);
+  l.rowmap = align_up(base.total + sizeof(int4) * (size_t)(3 + 2 * l.npass), 256);
   l.tokrow = align_up(l.rowmap + sizeof(int32_t) * (size_t)(N * C), 256);
   l.dense = align_up(l.tokrow + sizeof(int32_t) * (size_t)(N * C), 1024);
   l.dz = align_up(l.dense + (size_t)l.rows_cap * (size_t)d * 2, 1024);
-  l.dh_partials = align_up(l.dz + (size_t)l.rows_cap * (size_t)l.ldz * 2, 1024);
+  l.dh_partials = align_up(l.dz + (size_t)l.rows_pass * (size_t)l.ldz * 2, 1024);
   l.total = align_up(l.dh_partials + (size_t)l.items_max * kRows * 512 * sizeof(float), 256);
   return l;
 }
@@ -698,11 +720,10 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
                     (size_t)kLmSmem, st, 2, map_h, map_w, a.ids, p);
 }
 
-cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {
+cudaError_t launch_lmhead_bwd_rows(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {
   const WsLayout wl = ws_layout(a.N);
-  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms);
+  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms, a.rows_pass);
   char* ws = static_cast<char*>(a.ws);
-  const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
   const int32_t* lens = reinterpret_cast<const int32_t*>(ws + wl.lens);
   int32_t* rowmap = reinterpret_cast<int32_t*>(ws + bl.rowmap);
   int32_t* tokrow = reinterpret_cast<int32_t*>(ws + bl.tokrow);
@@ -713,20 +734,35 @@ cudaError_t launch_lmhead_dz(const LmBwdArgs& a, const DeviceInfo& dev, cudaStre
                              a.grad, a.N, a.C, a.skip_zero_weight ? 1 : 0, rowmap, tokrow,
                              geometry);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(gather_active_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0, st,
-                 1, static_cast<const uint16_t*>(a.hidden), dense, (const int32_t*)rowmap, a.C,
-                 a.P + a.C, a.P, a.d, a.V, pairs, geometry);
-  if (e != cudaSuccess) return e;
+  return launch_pdl(gather_active_rows_kernel, dim3((unsigned)(dev.sms * 8)), dim3(kThreads), 0,
+                    st, 1, static_cast<const uint16_t*>(a.hidden), dense, (const int32_t*)rowmap,
+                    a.C, a.P + a.C, a.P, a.d, a.V, pairs, bl.rows_pass, bl.npass, geometry);
+}
+
+cudaError_t launch_lmhead_dz(const LmBwdArgs& a, int64_t pass, const DeviceInfo& dev,
+                             cudaStream_t st) {
+  const WsLayout wl = ws_layout(a.N);
+  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms, a.rows_pass);
+  char* ws = static_cast<char*>(a.ws);
+  const int32_t* off = reinterpret_cast<const int32_t*>(ws + wl.offsets);
+  const int32_t* rowmap = reinterpret_cast<const int32_t*>(ws + bl.rowmap);
+  uint16_t* dense = reinterpret_cast<uint16_t*>(ws + bl.dense);
+  int4* geometry = reinterpret_cast<int4*>(ws + bl.geometry);
+  const int pairs = lm_pairs(dev);
   LmParams p = lm_params(off, geometry, reinterpret_cast<WsHeader*>(ws), a.N, a.P, a.C, a.V, a.d);
+  p.geo_index = lm_geo_proj(pass);
+  p.row0 = pass * bl.rows_pass;
+  p.rows_pass = bl.rows_pass;
   p.lse = a.lse;
   p.w = a.w;
   p.grad = a.grad;
   p.rowmap = rowmap;
   uint16_t* dz = reinterpret_cast<uint16_t*>(ws + bl.dz);
   CUtensorMap map_h, map_w, map_dz;
+  cudaError_t e;
   if ((e = encode_bf16_2d(&map_h, dense, a.d, bl.rows_cap, a.d, 128)) != cudaSuccess) return e;
   if ((e = encode_bf16_2d(&map_w, a.weight, a.d, a.V, a.d, 128)) != cudaSuccess) return e;
-  if ((e = encode_dz_slabs(&map_dz, dz, bl.rows_cap, bl.ldz, 32, true)) != cudaSuccess) return e;
+  if ((e = encode_dz_slabs(&map_dz, dz, bl.rows_pass, bl.ldz, 32, true)) != cudaSuccess) return e;
   static bool attr_done = false;
   if ((e = set_smem((const void*)lmhead_dz_kernel, kDzSmem, &attr_done)) != cudaSuccess) return e;
   return launch_pdl(lmhead_dz_kernel, dim3((unsigned)(2 * pairs)),

@@ -18,10 +18,15 @@
 //     vocabulary k-steps, 256 rows, up to 512 columns of d), fp32 tiles in the
 //     workspace
 // lmhead_grad_gemm_kernel<DwOp>   dweight: items (256 vocabulary rows, 512
-//     columns of d), K = every scored row, fp32 straight to dweight [V, d]
+//     columns of d), K = every row of the pass, fp32 straight to dweight
+//     [V, d]: stored by the first pass, added by TMA reductions in the others
 // lmhead_dh_reduce_kernel         sums a row's partials in split order
 //     (deterministic) into dhidden [N, P+C, d]; rows that score nothing get 0;
 //     runs beside the dweight kernel
+//
+// The backward rows run in passes (lmhead.cuh, LmBwdLayout): each pass runs
+// the logits-gradient kernel and these three over its rows, in stream order,
+// so one pass's dz buffer serves them all.
 //
 // The epilogue warps drain TMEM into 32 x 32 shared-memory boxes (128-byte
 // swizzle, two per warp) that TMA stores write out while the next box fills.
@@ -43,18 +48,39 @@ constexpr int64_t kDhTileFloats = (int64_t)kRows * kDhN;
 
 struct GradParams {
   int64_t N, V, d;
-  const int4* geometry;    // [1]: (row blocks, d tiles of 512, splits, k-steps per split);
+  const int4* geometry;    // [geo_dh]: (row blocks, d tiles of 512, splits, k-steps per split);
                            // [2].x: the backward's rows
+  int geo_dh;              // this pass's hidden-gradient geometry
+  int64_t row0, rows_pass;  // this pass's first backward row, rows per pass
+  int pass;
   int64_t ksteps_v;        // vocabulary k-steps of the hidden-state gradient (ldz / 64)
   WsHeader* hdr;
 };
 
+__device__ __forceinline__ int64_t rows_of_pass(const GradParams& p) {
+  const int64_t rows = p.geometry[2].x;
+  return rows <= p.row0 ? 0 : (rows - p.row0 < p.rows_pass ? rows - p.row0 : p.rows_pass);
+}
+
+// 2-D TMA reduction of a shared-memory box into global memory: each element
+// of the box is added to the one it lands on (bulk async group of the
+// calling thread).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t ssrc, int x,
+                                                  int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], "
+      "[%3];" ::"l"(map),
+      "r"(x), "r"(y), "r"(ssrc)
+      : "memory");
+}
+
 // Drains accumulator columns [c0, c1) of this warp's 32 TMEM lanes through
-// kBoxes 32 x 32 fp32 boxes (128-byte swizzle) into TMA stores at (x0 + c, y).
+// kBoxes 32 x 32 fp32 boxes (128-byte swizzle) into TMA stores at (x0 + c, y),
+// or with `add` TMA reductions that add the box to what is there.
 template <int kBoxes>
 __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t stg,
                                            uint32_t& chunk, uint32_t tbase, int c0, int c1,
-                                           bool empty, int x0, int y) {
+                                           bool empty, int x0, int y, bool add = false) {
   const int lane = threadIdx.x & 31;
   for (int c = c0; c < c1; c += 32) {
     float v[32];
@@ -76,7 +102,10 @@ __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t 
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(map_out, box, x0 + c, y);
+      if (add)
+        tma_reduce_add_2d(map_out, box, x0 + c, y);
+      else
+        tma_store_2d(map_out, box, x0 + c, y);
       bulk_commit();
     }
     ++chunk;
@@ -106,7 +135,7 @@ struct DhOp {
 
   __device__ void setup() {
     nb = (p.d + kDhN - 1) / kDhN;
-    const int4 g = p.geometry[1];
+    const int4 g = p.geometry[p.geo_dh];
     mb = g.x;
     sps = g.w;
     ksteps = p.ksteps_v;
@@ -193,8 +222,11 @@ struct DwOp {
 
   __device__ void setup() {
     nb = (p.d + kN - 1) / kN;
-    ksteps = (p.geometry[2].x + kGK - 1) / kGK;  // rows past the last one are zero
-    n_items = (p.V + kRows - 1) / kRows * nb;
+    const int64_t rows = rows_of_pass(p);
+    ksteps = (rows + kGK - 1) / kGK;  // rows past the pass's last one are zero
+    // the first pass stores dweight (zeros when there is no row at all); the
+    // others add to it, and one without rows has nothing to add
+    n_items = (p.pass > 0 && rows == 0) ? 0 : (p.V + kRows - 1) / kRows * nb;
     chunk = 0;
   }
   __device__ int64_t m_tile(int64_t it) const { return it / nb; }
@@ -217,12 +249,13 @@ struct DwOp {
       tma_load_3d_pair(sa + j * kMnAtomStride, map_a, 0, (int)(ks * kGK),
                        (int)(mt * (kRows / 64) + rk * 2 + j), mbar);
     const uint32_t sb = sa + kGABytes;
+    const int hrow = (int)(p.row0 + ks * kGK);  // the pass's rows of the dense hidden states
     for (int j = 0; j < n0 / 128; ++j)
-      tma_load_2d_pair(sb + j * kMnAtomStride, map_b, (int)(d0 + rk * (n0 / 2) + 64 * j),
-                       (int)(ks * kGK), mbar);
+      tma_load_2d_pair(sb + j * kMnAtomStride, map_b, (int)(d0 + rk * (n0 / 2) + 64 * j), hrow,
+                       mbar);
     for (int j = 0; j < n1 / 128; ++j)
       tma_load_2d_pair(sb + 16384 + j * kMnAtomStride, map_b,
-                       (int)(d0 + 256 + rk * (n1 / 2) + 64 * j), (int)(ks * kGK), mbar);
+                       (int)(d0 + 256 + rk * (n1 / 2) + 64 * j), hrow, mbar);
   }
   __device__ void mma(uint32_t dacc, uint32_t sa, int64_t it, int, bool first) const {
     const int w = width(it), n0 = min(w, 256), n1 = w - n0;
@@ -245,7 +278,8 @@ struct DwOp {
     const int quarter = (threadIdx.x >> 5) & 3;
     const int half = width(it) / 2;
     drain_fp32<kBoxes>(map_out, stg, chunk, tbase, slice * half, (slice + 1) * half, empty,
-                       (int)(n_tile(it) * kN), (int)(m_tile(it) * kRows + rank * 128 + quarter * 32));
+                       (int)(n_tile(it) * kN), (int)(m_tile(it) * kRows + rank * 128 + quarter * 32),
+                       p.pass > 0);
   }
   __device__ void epi_end(int64_t) {}
   __device__ void epi_finish() {
@@ -271,8 +305,10 @@ __global__ void __launch_bounds__(64 + 32 * Op::kEpiWarps, 1)
 
 // dhidden [N, P+C, d]: row (i, P-1+t) is backward row r = tokrow[i*C + t]
 // (-1: the token is not scored, or its weight is 0 and was skipped; then the
-// row is 0); its value is the sum of its split partials in order.
-// A CTA per output row (index arithmetic once per row), 16-byte accesses.
+// row is 0).  The pass that holds backward row r writes that row: the sum of
+// its split partials in split order; the first pass also writes every row of
+// no backward row (zeros).  A CTA per output row (index arithmetic once per
+// row), 16-byte accesses.
 // Launched after the dweight kernel (programmatic dependent launch), it runs
 // beside it: it starts once every dweight CTA has begun, which is after the
 // dhidden kernel it reads from has completed, and it waits for the dweight
@@ -281,29 +317,28 @@ constexpr int kReduceThreads = 128;
 
 __global__ void __launch_bounds__(kReduceThreads)
     lmhead_dh_reduce_kernel(const float* __restrict__ partials, const int4* __restrict__ geometry,
+                            int geo_dh, const int32_t* __restrict__ rowmap,
                             const int32_t* __restrict__ tokrow, int64_t N, int64_t P, int64_t C,
-                            int64_t d, float* __restrict__ dh) {
+                            int64_t d, int64_t row0, int64_t rows_pass, int pass,
+                            float* __restrict__ dh) {
   pdl_trigger();
-  const int4 g = geometry[1];
+  const int4 g = geometry[geo_dh];
   const int64_t mb = g.x, nb = g.y;
   const int splits = g.z;
-  const int64_t T = P + C, rows = N * T;
+  const int64_t T = P + C;
   const int d4 = (int)(d / 4);
   const int64_t split_stride = mb * nb * kDhTileFloats;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int64_t i = row / T, t = row - i * T - (P - 1);
-    float4* dst = reinterpret_cast<float4*>(dh + row * d);
-    const int64_t r = (t >= 0 && t < C) ? tokrow[i * C + t] : -1;
-    if (r < 0) {
-      for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads)
-        dst[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
-      continue;
-    }
-    const int64_t rb = r / kRows, rr = r - rb * kRows;
+  const int64_t all = geometry[2].x;
+  const int64_t rows = all <= row0 ? 0 : (all - row0 < rows_pass ? all - row0 : rows_pass);
+  // this pass's backward rows
+  for (int64_t rr = blockIdx.x; rr < rows; rr += gridDim.x) {
+    const int64_t tok = rowmap[row0 + rr], i = tok / C, t = tok - i * C;
+    float4* dst = reinterpret_cast<float4*>(dh + (i * T + P - 1 + t) * d);
+    const int64_t rb = rr / kRows, rl = rr - rb * kRows;
     for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads) {
       const int k = 4 * k4, nt = k / kDhN, kk = k - nt * kDhN;
       // partial tile of split s: item (s * mb + rb) * nb + nt
-      const float* src = partials + (rb * nb + nt) * kDhTileFloats + rr * kDhN + kk;
+      const float* src = partials + (rb * nb + nt) * kDhTileFloats + rl * kDhN + kk;
       // L2 loads (not L1): the partials were written by a kernel this one does not wait for
       float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
 #pragma unroll 4
@@ -315,6 +350,17 @@ __global__ void __launch_bounds__(kReduceThreads)
         acc.w += x.w;
       }
       dst[k4] = acc;
+    }
+  }
+  // the rows of no backward row: prompt rows, the last row, rows past each
+  // length and skipped tokens
+  if (pass == 0) {
+    for (int64_t row = blockIdx.x; row < N * T; row += gridDim.x) {
+      const int64_t i = row / T, t = row - i * T - (P - 1);
+      if (t >= 0 && t < C && tokrow[i * C + t] >= 0) continue;
+      float4* dst = reinterpret_cast<float4*>(dh + row * d);
+      for (int k4 = threadIdx.x; k4 < d4; k4 += kReduceThreads)
+        dst[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   pdl_wait();  // the dweight kernel launched before this one has completed
@@ -340,9 +386,11 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 
 }  // namespace
 
-cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaStream_t st) {
-  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms);
+cudaError_t launch_lmhead_grads(const LmBwdArgs& a, int64_t pass, const DeviceInfo& dev,
+                                cudaStream_t st) {
+  const LmBwdLayout bl = lm_bwd_layout(a.N, a.C, a.V, a.d, dev.sms, a.rows_pass);
   char* ws = static_cast<char*>(a.ws);
+  const int32_t* rowmap = reinterpret_cast<const int32_t*>(ws + bl.rowmap);
   const int32_t* tokrow = reinterpret_cast<const int32_t*>(ws + bl.tokrow);
   const uint16_t* dz = reinterpret_cast<const uint16_t*>(ws + bl.dz);
   const uint16_t* dense = reinterpret_cast<const uint16_t*>(ws + bl.dense);
@@ -354,14 +402,18 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
   p.V = a.V;
   p.d = a.d;
   p.geometry = geometry;
+  p.geo_dh = lm_geo_dh(pass);
+  p.row0 = pass * bl.rows_pass;
+  p.rows_pass = bl.rows_pass;
+  p.pass = (int)pass;
   p.ksteps_v = bl.ldz / kGK;
   p.hdr = reinterpret_cast<WsHeader*>(ws);
 
   // dhidden = dz W: A = dz (K-major, K = vocabulary), B = W (MN-major)
   CUtensorMap a_dh, b_dh, o_dh, a_dw, b_dw, o_dw;
   cudaError_t e;
-  if ((e = encode_dz_slabs(&a_dh, const_cast<uint16_t*>(dz), bl.rows_cap, bl.ldz, 128, false)) !=
-      cudaSuccess)
+  if ((e = encode_dz_slabs(&a_dh, const_cast<uint16_t*>(dz), bl.rows_pass, bl.ldz, 128,
+                           false)) != cudaSuccess)
     return e;
   if ((e = encode_bf16_2d(&b_dh, a.weight, a.d, a.V, a.d, kGK)) != cudaSuccess) return e;
   if ((e = encode_store_32x32(&o_dh, partials, true, kDhN, bl.items_max * kRows, kDhN)) !=
@@ -369,9 +421,9 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
     return e;
   if ((e = launch_gemm<DhOp>(a_dh, b_dh, o_dh, p, dev, st)) != cudaSuccess) return e;
 
-  // dweight = dz^T H: A = dz (MN-major, K = scored rows), B = H (MN-major)
-  if ((e = encode_dz_slabs(&a_dw, const_cast<uint16_t*>(dz), bl.rows_cap, bl.ldz, 64, false)) !=
-      cudaSuccess)
+  // dweight (+)= dz^T H: A = dz (MN-major, K = the pass's rows), B = H (MN-major)
+  if ((e = encode_dz_slabs(&a_dw, const_cast<uint16_t*>(dz), bl.rows_pass, bl.ldz, 64,
+                           false)) != cudaSuccess)
     return e;
   if ((e = encode_bf16_2d(&b_dw, dense, a.d, bl.rows_cap, a.d, kGK)) != cudaSuccess) return e;
   if ((e = encode_store_32x32(&o_dw, a.dweight, true, a.d, a.V, a.d)) != cudaSuccess) return e;
@@ -382,7 +434,8 @@ cudaError_t launch_lmhead_grads(const LmBwdArgs& a, const DeviceInfo& dev, cudaS
   if (blocks > 16 * (int64_t)dev.sms) blocks = 16 * (int64_t)dev.sms;
   if (blocks < 1) blocks = 1;
   return launch_pdl(lmhead_dh_reduce_kernel, dim3((unsigned)blocks), dim3(kReduceThreads), 0, st,
-                    1, (const float*)partials, geometry, tokrow, a.N, a.P, a.C, a.d, a.dhidden);
+                    1, (const float*)partials, geometry, lm_geo_dh(pass), rowmap, tokrow, a.N, a.P,
+                    a.C, a.d, p.row0, bl.rows_pass, (int)pass, a.dhidden);
 }
 
 }  // namespace grpo
