@@ -152,9 +152,11 @@ def recorded_traffic(kernel: str, w: wl.Workload, hidden: int | None = None):
     this workload or when the kernel's sources changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f).get(kernel)
+            recs = json.load(f)
     except (OSError, ValueError):
         return None
+    # a capture of this workload ("kernel@workload"), else the kernel's default one
+    rec = recs.get(f"{kernel}@{w.name}") or recs.get(kernel)
     if (not rec or rec.get("sources_sha") != sources_sha(kernel) or rec.get("workload") != w.name
             or rec.get("hidden") != hidden):
         return None
