@@ -82,13 +82,16 @@ __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t 
                                            uint32_t& chunk, uint32_t tbase, int c0, int c1,
                                            bool empty, int x0, int y, bool add = false) {
   const int lane = threadIdx.x & 31;
+  // The next 32 columns' TMEM load is issued as soon as this chunk's values
+  // sit in shared memory, so it runs while the TMA reads the box.
+  uint32_t v[32];
+  if (!empty && c0 < c1) tmem_ld32_issue(tbase + (uint32_t)c0, v);
   for (int c = c0; c < c1; c += 32) {
-    float v[32];
     if (!empty) {
-      tmem_ld32(tbase + (uint32_t)c, v);
+      tmem_ld_wait(v);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      for (int j = 0; j < 32; ++j) v[j] = 0u;
     }
     // row `lane` of the box; 16-byte chunk q sits at q ^ (lane & 7)
     const uint32_t box = stg + (chunk % kBoxes) * (uint32_t)kEpiBoxBytes;
@@ -96,11 +99,11 @@ __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t 
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      st_shared_v4(box + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4),
-                   __float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                   __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3]));
+      st_shared_v4(box + (uint32_t)lane * 128u + ((uint32_t)(q ^ (lane & 7)) << 4), v[4 * q],
+                   v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     fence_async_smem();
     __syncwarp();
+    if (!empty && c + 32 < c1) tmem_ld32_issue(tbase + (uint32_t)(c + 32), v);
     if (lane == 0) {
       if (add)
         tma_reduce_add_2d(map_out, box, x0 + c, y);
