@@ -813,11 +813,11 @@ def run_ours(args, w0: wl.Workload):
         t = torch.tensor([elapsed], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed = float(t[0])
-        tv = torch.tensor([t_valid], device=dev, dtype=torch.int64)
+        tv = torch.tensor([t_valid, contrast], device=dev, dtype=torch.int64)
         dist.all_reduce(tv)
-        t_valid_all = int(tv.item())
+        t_valid_all, contrast_all = int(tv[0].item()), int(tv[1].item())
     else:
-        t_valid_all = t_valid
+        t_valid_all, contrast_all = t_valid, contrast
 
     copy_gbs = None if args.no_copy_ceiling else copy_ceiling(g, dev)
 
@@ -859,7 +859,7 @@ def run_ours(args, w0: wl.Workload):
                                "groups_with_reward_contrast_per_rank": contrast,
                                "groups_per_rank": w.B,
                                "skip_zero_weight": bool(args.skip_zero_weight)},
-            "useful_groups_per_s": contrast * world / ms,
+            "useful_groups_per_s": contrast_all / ms,
             "logits_gbs": step_bytes / ms / 1e9,
             "logits_roofline_frac": step_bytes / ms / 1e9 / peak,
             "logits_bytes_per_step": step_bytes,
