@@ -75,7 +75,10 @@ def test_step_replays_in_a_cuda_graph(fused):
     assert not torch.equal(_bits(eager2["dl"]), _bits(eager["dl"]))
 
 
-def test_host_logits_step_replays_in_a_cuda_graph():
+@pytest.mark.parametrize("host_dl", [False, True], ids=["dev_dlogits", "host_dlogits"])
+def test_host_logits_step_replays_in_a_cuda_graph(host_dl):
+    """The host-logits call captured into a CUDA graph and replayed, with the
+    gradient in device memory or written straight into pinned host memory."""
     n = H.g()
     w = _case(410)
     logits = wl.make_logits_cpu(w)
@@ -87,9 +90,11 @@ def test_host_logits_step_replays_in_a_cuda_graph():
     adv = n.grpo_advantage(R, w.G)
     ref = n.grpo_loss_fwd_bwd(logits.cuda(), w.P, ids, lens, adv, None, None, 0.2, 0.0)
     torch.cuda.synchronize()
+    dl0 = torch.empty(logits.shape, dtype=logits.dtype).pin_memory() if host_dl else None
     out = n.grpo_loss_fwd_bwd_host(host, w.P, ids, lens, adv, None, None, 0.2, 0.0,
-                                   staging=staging)
+                                   staging=staging, dlogits=dl0)
     dl = out["dlogits"]
+    assert dl.is_cuda != host_dl
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         n.grpo_loss_fwd_bwd_host(host, w.P, ids, lens, adv, None, None, 0.2, 0.0, 0.0, None,
@@ -100,4 +105,4 @@ def test_host_logits_step_replays_in_a_cuda_graph():
     assert n.grpo_check_error(out["workspace"]) == 0
     for k in ("logp", "lse", "w", "loss"):
         assert torch.equal(_bits(ref[k]), _bits(out[k])), k
-    assert torch.equal(_bits(ref["dlogits"]), _bits(dl))
+    assert torch.equal(_bits(ref["dlogits"]).cpu(), _bits(dl).cpu())
