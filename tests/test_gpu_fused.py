@@ -67,11 +67,11 @@ def test_fused_same_bits_as_two_calls(w):
 
 @pytest.mark.parametrize("B,C,V,dtype", [(50, 4, 50001, "bf16"), (1025, 1, 50000, "bf16"),
                                          (50, 4, 20001, "f32")],
-                         ids=["N200_three_head_slots", "N4100_offsets_in_memory", "N200_f32"])
+                         ids=["N200_two_head_slots", "N4100_offsets_in_memory", "N200_f32"])
 def test_fused_head_slots_same_bits(B, C, V, dtype):
     """The fused kernel holds each row's first chunks in shared-memory slots,
     as many as fit beside its ring and offsets table with two CTAs per SM:
-    three at 200 completions, four again at 4,100 (the offsets table then
+    two at 200 completions, three again at 4,100 (the offsets table then
     stays in global memory).  Whole rows per CTA (N*C above four rows per
     SM), five to seven 16 KiB chunks a row, so the ring carries the rest;
     the outputs have the bits of the two calls."""

@@ -41,7 +41,11 @@
 namespace grpo {
 namespace {
 
-constexpr int kStages = 3;
+// A 4-stage ring and 3 head slots (7 x 16 KiB, two CTAs per SM): measured
+// against 3 + 4, 2 + 5, 5 + 2 and 6 + 1 at the long-completion workload
+// (10.28 ms against 10.31, 10.76, 10.39 and 10.57) and at 6,043 scored rows
+// (0.857 ms against 0.863, 0.889, 0.866 and 0.874).
+constexpr int kStages = 4;
 constexpr int kStageBytes = 16384;
 constexpr int kConsumers = kThreads;
 constexpr int kFusedThreads = kConsumers + 32;
@@ -51,9 +55,10 @@ constexpr int kSmemOffsets = 4096;
 // Chunks at the head of each row (slice) that pass 1 loads into slots of
 // their own and pass 2 reads from there, not from L2: with whole rows per CTA
 // the head of a row is the part likeliest to have left L2 by pass 2.  As many
-// slots as leave two CTAs per SM (keep_slots): four with a small offsets
-// table (N < 128), three up to the largest one.
-constexpr int kKeepMax = 4;
+// slots as leave two CTAs per SM beside the ring and the offsets table
+// (keep_slots): three up to 191 completions, two above that, three again
+// from 4,096 (the offsets table then stays in global memory).
+constexpr int kKeepMax = 3;
 
 template <typename T>
 struct FusedParams {
