@@ -603,6 +603,17 @@ def path_summary(g, b: Batch, peak: float, steps: int, warmup: int, stream) -> d
     return out
 
 
+def rank_aggregate(dist, dev, elapsed: float, t_valid: int, contrast: int):
+    """Whole-job figures of a weak-scaling run: the slowest rank's time and the
+    scored tokens and contrasted groups of all ranks."""
+    import torch
+    t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([t_valid, contrast], device=dev, dtype=torch.int64)
+    dist.all_reduce(n)
+    return float(t[0]), int(n[0].item()), int(n[1].item())
+
+
 def run_e2e(args, g, b: Batch, stream, world: int, dist) -> dict:
     """The headline metric end to end through the public API, with the
     step's inputs and results in pinned host memory: every step copies the
@@ -810,12 +821,7 @@ def run_ours(args, w0: wl.Workload):
 
     # aggregate over ranks: units of all ranks / max time
     if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t[0])
-        tv = torch.tensor([t_valid, contrast], device=dev, dtype=torch.int64)
-        dist.all_reduce(tv)
-        t_valid_all, contrast_all = int(tv[0].item()), int(tv[1].item())
+        elapsed, t_valid_all, contrast_all = rank_aggregate(dist, dev, elapsed, t_valid, contrast)
     else:
         t_valid_all, contrast_all = t_valid, contrast
 

@@ -81,3 +81,37 @@ def test_two_rank_partials_add_up():
     for rank, total, a, b, d_rank in got:
         assert abs(total - loss) <= 1e-12 * max(1.0, abs(loss)), (total, loss)
         assert np.array_equal(d_rank, d[a:b])
+
+
+def _agg_rank(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        out = bench.rank_aggregate(dist, torch.device("cpu"), 0.5 + rank, 100 * (rank + 1),
+                                   rank)
+        q.put((rank, out))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_rank_aggregate_two_ranks():
+    """bench.py's whole-job figures over 2 gloo ranks: the slowest rank's time,
+    the sum of scored tokens and of contrasted groups."""
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_agg_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(2):
+        assert res[r] == (1.5, 300, 1)
