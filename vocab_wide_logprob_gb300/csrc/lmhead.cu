@@ -322,8 +322,22 @@ struct LmOp {
     g = (kMode == 1 && p.grad != nullptr) ? __ldg(p.grad) : 1.f;
     chunk = 0;
   }
+  // item it = (row block, vocabulary split), decoded once per item by each
+  // role's thread (the producer asks at every k-step, where 64-bit divisions
+  // on every call would hold up the issue)
+  mutable int64_t c_it = -1, c_rb = 0, c_n0 = 0;
+  __device__ void decode(int64_t it) const {
+    if (it != c_it) {
+      c_it = it;
+      c_rb = it / splits;
+      c_n0 = (it - c_rb * splits) * tps;
+    }
+  }
   __device__ int64_t items() const { return mb * splits; }
-  __device__ int64_t first_tile(int64_t it) const { return (it % splits) * tps; }
+  __device__ int64_t first_tile(int64_t it) const {
+    decode(it);
+    return c_n0;
+  }
   __device__ int tiles(int64_t it) const {
     const int64_t n0 = first_tile(it);
     return (int)(min(ntiles, n0 + tps) - n0);
@@ -335,7 +349,8 @@ struct LmOp {
   __device__ uint32_t bytes(int64_t, int) const { return kPairStageBytes; }
   __device__ void load(uint32_t sa, int64_t it, int t, int64_t ks, uint32_t rk,
                        uint32_t mbar) const {
-    const int64_t rb = it / splits, n = first_tile(it) + t;
+    decode(it);
+    const int64_t rb = c_rb, n = c_n0 + t;
     tma_load_2d_pair(sa, map_h, (int)(ks * kK), (int)(p.row0 + rb * kRows + rk * 128), mbar);
     tma_load_2d_pair(sa + kPairBOffset, map_w, (int)(ks * kK), (int)(n * kVTile + rk * 128),
                      mbar);

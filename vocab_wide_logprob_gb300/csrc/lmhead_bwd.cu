@@ -29,7 +29,8 @@
 // so one pass's dz buffer serves them all.
 //
 // The epilogue warps drain TMEM into 32 x 32 shared-memory boxes (128-byte
-// swizzle, two per warp) that TMA stores write out while the next box fills.
+// swizzle, one or two per warp) that TMA stores write out while the next box
+// fills.
 // d must be a multiple of 128: each CTA of a pair holds half of every MMA's
 // N columns (256 or 128) as whole 64-column MN-major atoms.
 #include "pair_pipeline.cuh"
@@ -115,6 +116,28 @@ __device__ __forceinline__ void drain_fp32(const CUtensorMap* map_out, uint32_t 
   }
 }
 
+// The d tile item `it` of the persistent loop works on.  Items come in
+// aligned groups of nb (one unit: the same operand rows, its nb d tiles, the
+// last one narrower when d is not a multiple of 512), and a pair takes every
+// npairs-th item: with the tile fixed by `it % nb` the same pairs would always
+// get the narrow tile (npairs even, nb = 2: even pairs 512 columns per item,
+// odd pairs 384).  Rotating the tiles of each group by the round, it / npairs,
+// gives every pair the tiles in turn; a group still runs in one round on
+// neighbouring pairs (npairs a multiple of nb), sharing its operand in L2.
+__device__ __forceinline__ int64_t rotated_tile(int64_t it, int64_t nb) {
+  const int64_t npairs = gridDim.x >> 1;
+  if (nb <= 1 || npairs % nb != 0) return it % nb;
+  return (it % nb + it / npairs) % nb;
+}
+
+// An item's unit (it / nb), d tile and width, decoded once per item by each
+// role's thread: the producer and the MMA issuer consult them at every
+// k-step, where 64-bit divisions on every call would hold up the issue.
+struct ItemTile {
+  int64_t it = -1, unit = 0, n = 0;
+  int w = 0;
+};
+
 // dhidden = dz W.  Items (vocabulary split, 256-row block, d tile of up to
 // 512): A = dz (K-major, one {64 vocabulary, 128 rows} slab box per CTA), B =
 // W (MN-major): the d tile is two MMAs of N0 <= 256 and N1 = width - N0
@@ -145,15 +168,26 @@ struct DhOp {
     n_items = (int64_t)g.x * g.y * g.z;
     chunk = 0;
   }
-  // it = (split * mb + row block) * nb + d tile: the items running at the same
-  // time share their vocabulary range in L2.
-  __device__ int64_t m_tile(int64_t it) const { return (it / nb) % mb; }
-  __device__ int64_t n_tile(int64_t it) const { return it % nb; }
-  __device__ int width(int64_t it) const { return (int)min((int64_t)kDhN, p.d - n_tile(it) * kDhN); }
+  // it / nb = split * mb + row block, its d tile rotated by the round
+  // (rotated_tile): the items running at the same time share their vocabulary
+  // range in L2.
+  mutable ItemTile cur;
+  __device__ const ItemTile& tile_of(int64_t it) const {
+    if (it != cur.it) {
+      cur.it = it;
+      cur.unit = it / nb;
+      cur.n = rotated_tile(it, nb);
+      cur.w = (int)min((int64_t)kDhN, p.d - cur.n * kDhN);
+    }
+    return cur;
+  }
+  __device__ int64_t m_tile(int64_t it) const { return tile_of(it).unit % mb; }
+  __device__ int64_t n_tile(int64_t it) const { return tile_of(it).n; }
+  __device__ int width(int64_t it) const { return tile_of(it).w; }
   __device__ int64_t items() const { return n_items; }
   __device__ int tiles(int64_t) const { return 1; }
   __device__ void krange(int64_t it, int, int64_t* k0, int64_t* k1) const {
-    *k0 = (it / nb / mb) * sps;
+    *k0 = (tile_of(it).unit / mb) * sps;
     *k1 = min(ksteps, *k0 + sps);
   }
   __device__ uint32_t bytes(int64_t it, int) const {
@@ -189,10 +223,12 @@ struct DhOp {
   }
   __device__ void epi_begin(int64_t) {}
   __device__ void epi_tile(int64_t it, int, uint32_t tbase, bool empty, int) {
-    // partial tile `it`: rows it*256 .. of an [items*256, 512] matrix
+    // partial tile (split * mb + row block) * nb + d tile: rows .. * 256 of an
+    // [items * 256, 512] matrix
     const int quarter = (threadIdx.x >> 5) & 3;
+    const int64_t tile = tile_of(it).unit * nb + n_tile(it);
     drain_fp32<kBoxes>(map_out, stg, chunk, tbase, 0, width(it), empty, 0,
-                       (int)(it * kRows + rank * 128 + quarter * 32));
+                       (int)(tile * kRows + rank * 128 + quarter * 32));
   }
   __device__ void epi_end(int64_t) {}
   __device__ void epi_finish() {
@@ -232,9 +268,19 @@ struct DwOp {
     n_items = (p.pass > 0 && rows == 0) ? 0 : (p.V + kRows - 1) / kRows * nb;
     chunk = 0;
   }
-  __device__ int64_t m_tile(int64_t it) const { return it / nb; }
-  __device__ int64_t n_tile(int64_t it) const { return it % nb; }
-  __device__ int width(int64_t it) const { return (int)min((int64_t)kN, p.d - n_tile(it) * kN); }
+  mutable ItemTile cur;
+  __device__ const ItemTile& tile_of(int64_t it) const {
+    if (it != cur.it) {
+      cur.it = it;
+      cur.unit = it / nb;
+      cur.n = rotated_tile(it, nb);
+      cur.w = (int)min((int64_t)kN, p.d - cur.n * kN);
+    }
+    return cur;
+  }
+  __device__ int64_t m_tile(int64_t it) const { return tile_of(it).unit; }
+  __device__ int64_t n_tile(int64_t it) const { return tile_of(it).n; }
+  __device__ int width(int64_t it) const { return tile_of(it).w; }
   __device__ int64_t items() const { return n_items; }
   __device__ int tiles(int64_t) const { return 1; }
   __device__ void krange(int64_t, int, int64_t* k0, int64_t* k1) const {
