@@ -146,6 +146,16 @@ def sources_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def lmhead_bwd_passes(w, rows_per_pass: int) -> int:
+    """Passes of the LM-head backward over a workspace sized for
+    ``rows_per_pass`` rows, by the library's layout rule: every possible row
+    (N*C rounded up to 256) in passes of rows_per_pass rounded up to 256 (0:
+    one pass).  Passes past the scored rows find no row and return at once."""
+    cap = -(-w.N * w.C // 256) * 256
+    r = cap if rows_per_pass <= 0 else min(cap, -(-rows_per_pass // 256) * 256)
+    return -(-cap // r)
+
+
 def recorded_traffic(kernel: str, w: wl.Workload, hidden: int | None = None):
     """DRAM bytes (read + write) per launch of `kernel` on workload `w` from a
     committed ncu capture (profiles/traffic.json); None when there is none for
@@ -949,6 +959,8 @@ def run_lmhead(args, w: wl.Workload):
                                              rows_per_pass=(t_valid if args.lmhead_rows_per_pass < 0
                                                             else args.lmhead_rows_per_pass))
         bwd_ws_bytes = bws.numel()
+        bwd_passes = lmhead_bwd_passes(w, t_valid if args.lmhead_rows_per_pass < 0
+                                       else args.lmhead_rows_per_pass)
         bwd_ws_full = g.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, d)
         t_nonzero = int((fwd["w"] != 0).sum().item())
 
@@ -1022,9 +1034,9 @@ def run_lmhead(args, w: wl.Workload):
                      "traffic": recorded_traffic("lmhead_fwd_bwd" if train else
                                                  "lmhead_lse_kernel", w, d)},
         # per step: mask, prep, gather, log-sum-exp (+ advantage, surrogate, and
-        # the backward's prep, row scan, gather, logits-gradient, dhidden,
-        # dweight and reduce kernels)
-        "gpu_launches": (13 if train else 4) * args.steps, "clocks": clocks,
+        # the backward's prep, row scan and gather, then per pass its
+        # logits-gradient, dhidden, dweight and reduce kernels)
+        "gpu_launches": ((9 + 4 * bwd_passes) if train else 4) * args.steps, "clocks": clocks,
         "cpu_baseline": None if args.no_cpu_baseline else
         time_oracle_lmhead(w, d, args.cpu_seconds, train),
     }
@@ -1037,6 +1049,7 @@ def run_lmhead(args, w: wl.Workload):
         line["config"]["skip_zero_weight"] = bool(args.skip_zero_weight)
         line["bwd_workspace_bytes"] = bwd_ws_bytes
         line["bwd_workspace_bytes_every_possible_row"] = bwd_ws_full
+        line["bwd_passes"] = bwd_passes
     print(json.dumps(line), flush=True)
 
 

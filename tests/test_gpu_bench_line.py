@@ -47,3 +47,24 @@ def test_our_arm_line():
         assert pr["ms_per_step"] > 0 and pr["logits_bytes_per_step"] > 0
     assert wl.TINY.name in d["per_config"]
     assert d["gpu_launches"] == 6 * d["steps"]
+
+
+@pytest.mark.parametrize("rows_per_pass,passes", [(-1, 2), (2048, 1)])
+def test_lmhead_line_counts_every_pass(rows_per_pass, passes):
+    """The LM-head loss line: a tensor-core roofline, and a launch count with
+    the backward's four kernels once per pass (passes of the scored rows
+    present leave an empty second pass over the 2,048 possible rows; passes
+    of 2,048 rows one pass)."""
+    w = wl.QWEN_G8
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--path",
+                        "lmhead_fwd_bwd", "--workload", w.name, "--steps", "3", "--warmup", "3",
+                        "--lmhead-rows-per-pass", str(rows_per_pass), "--no-cpu-baseline",
+                        "--no-clocks"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["roofline"]["bound"] == "tensor" and d["roofline"]["frac"] > 0
+    assert d["bwd_passes"] == passes
+    assert d["gpu_launches"] == (9 + 4 * passes) * d["steps"]

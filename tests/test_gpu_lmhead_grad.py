@@ -98,6 +98,15 @@ SMALL = [
                                  V=4099, eos_id=4000, seed=82), 384, 2.5),
     ("V300_d128_short", wl.variant(wl.QWEN_G8, name="lmg_300_128", B=1, G=2, P=3, C=6, V=300,
                                    eos_id=299, seed=83), 128, None),
+    # several 512-column d tiles, the last one narrow, and more items than one
+    # round of CTA pairs (dweight: 24 vocabulary blocks x 4 tiles; dhidden: 2
+    # row blocks x 4 tiles x its vocabulary splits): four tiles rotate over
+    # the rounds, three keep their order (a 152-SM grid's 76 pairs are not a
+    # multiple of 3)
+    ("V6001_d1664_four_tiles", wl.variant(wl.QWEN_G8, name="lmg_6001_1664", B=1, G=4, P=5,
+                                          C=120, V=6001, eos_id=6000, seed=86), 1664, None),
+    ("V6001_d1152_three_tiles", wl.variant(wl.QWEN_G8, name="lmg_6001_1152", B=1, G=4, P=5,
+                                           C=120, V=6001, eos_id=6000, seed=87), 1152, 0.5),
 ]
 
 
