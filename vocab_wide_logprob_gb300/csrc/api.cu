@@ -10,6 +10,7 @@
 #include <utility>
 
 #include "common.cuh"
+#include "host_ctx.cuh"
 #include "lmhead.cuh"
 #include "host_rows.cuh"
 #include "selftest.cuh"
@@ -45,21 +46,21 @@ int grid_mult(const char* env, int def) {
 
 namespace {
 
-int g_sms[64] = {};  // SM count per device ordinal; benign race (same value)
+// SM count per device ordinal (ordinals below 64; others are asked each time)
+std::atomic<int> g_sms[64] = {};
 
 cudaError_t current_device(DeviceInfo* d) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   d->device = dev;
-  int& sms = g_sms[dev & 63];
-  if (sms == 0) {
-    int n = 0;
+  int n = dev >= 0 && dev < 64 ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    sms = n;
+    if (dev >= 0 && dev < 64) g_sms[dev].store(n, std::memory_order_relaxed);
   }
-  d->sms = sms;
+  d->sms = n;
   return cudaSuccess;
 }
 
@@ -105,12 +106,14 @@ bool disjoint_from(const CallRecord& c, Span w, Span r) {
 }
 
 std::mutex g_order_mutex;
-std::map<std::pair<int, cudaStream_t>, CallRecord> g_last_call;
+std::map<std::pair<unsigned long long, cudaStream_t>, CallRecord> g_last_call;
 
-std::pair<int, cudaStream_t> order_key(cudaStream_t st) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) (void)cudaGetLastError();
-  return {dev, st};
+// A stream handle names a stream of the current context (the legacy default
+// stream 0 is a different stream in each), so records are kept per context.
+std::pair<unsigned long long, cudaStream_t> order_key(cudaStream_t st) {
+  unsigned long long ctx = 0;
+  if (current_context_id(&ctx) != cudaSuccess) (void)cudaGetLastError();
+  return {ctx, st};
 }
 
 // grpo_set_early_start(0) turns the two early starts off process-wide.

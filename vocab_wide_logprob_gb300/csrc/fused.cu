@@ -36,6 +36,7 @@
 #include <tuple>
 
 #include "common.cuh"
+#include "host_ctx.cuh"
 #include "host_rows.cuh"
 
 namespace grpo {
@@ -652,17 +653,12 @@ cudaError_t launch_k(const FwdArgs& a, const BwdArgs& bw, const DeviceInfo& d, c
   // kernel in both modes
   auto kern = lse_grad_kernel<T, K, false>;
   auto kern_launch = staging != nullptr ? lse_grad_kernel<T, K, true> : kern;
-  static bool attr_set[2][2][4] = {};
-  bool& done = attr_set[staging != nullptr ? 1 : 0][sizeof(T) == 4 ? 0 : 1]
-                       [K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
-  if (!done) {
+  {
     const int max_smem =
         (kStages + kKeepMax) * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaError_t e = ensure_dynamic_smem((const void*)kern, max_smem);
+    if (e == cudaSuccess) e = ensure_dynamic_smem((const void*)kern_launch, max_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern_launch, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e != cudaSuccess) return e;
-    done = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

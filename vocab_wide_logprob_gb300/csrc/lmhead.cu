@@ -28,6 +28,7 @@
 // gradient contractions (lmhead_bwd.cu).
 #include <mutex>
 
+#include "host_ctx.cuh"
 #include "pair_pipeline.cuh"
 #include "lmhead.cuh"
 
@@ -606,13 +607,6 @@ LmParams lm_params(const int32_t* off, int4* geometry, WsHeader* hdr, int64_t N,
   return p;
 }
 
-cudaError_t set_smem(const void* kern, int bytes, bool* done) {
-  if (*done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) *done = true;
-  return e;
-}
-
 }  // namespace
 
 int lm_pairs(const DeviceInfo& dev) { return dev.sms / 2 > 0 ? dev.sms / 2 : 1; }
@@ -729,8 +723,7 @@ cudaError_t launch_lmhead(const void* hidden, const void* weight, const FwdArgs&
   CUtensorMap map_h, map_w;
   if ((e = encode_bf16_2d(&map_h, dense, d, rows, d, 128)) != cudaSuccess) return e;
   if ((e = encode_bf16_2d(&map_w, weight, d, a.V, d, 128)) != cudaSuccess) return e;
-  static bool attr_done = false;
-  if ((e = set_smem((const void*)lmhead_lse_kernel, kLmSmem, &attr_done)) != cudaSuccess) return e;
+  if ((e = ensure_dynamic_smem((const void*)lmhead_lse_kernel, kLmSmem)) != cudaSuccess) return e;
   return launch_pdl(lmhead_lse_kernel, dim3((unsigned)(2 * pairs)), dim3(kPairThreads),
                     (size_t)kLmSmem, st, 2, map_h, map_w, a.ids, p);
 }
@@ -778,8 +771,7 @@ cudaError_t launch_lmhead_dz(const LmBwdArgs& a, int64_t pass, const DeviceInfo&
   if ((e = encode_bf16_2d(&map_h, dense, a.d, bl.rows_cap, a.d, 128)) != cudaSuccess) return e;
   if ((e = encode_bf16_2d(&map_w, a.weight, a.d, a.V, a.d, 128)) != cudaSuccess) return e;
   if ((e = encode_dz_slabs(&map_dz, dz, bl.rows_pass, bl.ldz, 32, true)) != cudaSuccess) return e;
-  static bool attr_done = false;
-  if ((e = set_smem((const void*)lmhead_dz_kernel, kDzSmem, &attr_done)) != cudaSuccess) return e;
+  if ((e = ensure_dynamic_smem((const void*)lmhead_dz_kernel, kDzSmem)) != cudaSuccess) return e;
   return launch_pdl(lmhead_dz_kernel, dim3((unsigned)(2 * pairs)),
                     dim3(64 + 32 * LmOp<1>::kEpiWarps), (size_t)kDzSmem, st, 2, map_h, map_w,
                     map_dz, a.ids, p);

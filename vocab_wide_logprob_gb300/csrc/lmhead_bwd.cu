@@ -33,6 +33,7 @@
 // fills.
 // d must be a multiple of 128: each CTA of a pair holds half of every MMA's
 // N columns (256 or 128) as whole 64-column MN-major atoms.
+#include "host_ctx.cuh"
 #include "pair_pipeline.cuh"
 #include "lmhead.cuh"
 
@@ -420,15 +421,8 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
                         const GradParams& p, const DeviceInfo& dev, cudaStream_t st) {
   constexpr int smem = Op::kStages * Op::kStageBytes + Op::kEpiWarps * Op::kBoxes * kEpiBoxBytes +
                        1024;
-  static bool attr_done = false;
-  cudaError_t e;
-  if (!attr_done) {
-    if ((e = cudaFuncSetAttribute(lmhead_grad_gemm_kernel<Op>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-        cudaSuccess)
-      return e;
-    attr_done = true;
-  }
+  cudaError_t e = ensure_dynamic_smem((const void*)lmhead_grad_gemm_kernel<Op>, smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(lmhead_grad_gemm_kernel<Op>, dim3((unsigned)(2 * lm_pairs(dev))),
                     dim3(64 + 32 * Op::kEpiWarps), (size_t)smem, st, 2, a, b, out, p);
 }

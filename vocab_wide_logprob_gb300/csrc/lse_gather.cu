@@ -26,6 +26,7 @@
 #include <tuple>
 
 #include "common.cuh"
+#include "host_ctx.cuh"
 
 namespace grpo {
 
@@ -523,13 +524,10 @@ cudaError_t launch_k(const FwdArgs& a, const DeviceInfo& d, cudaStream_t st, boo
   const size_t smem = (size_t)kStages * kStageBytes +
                       (a.N + 1 <= kSmemOffsets ? sizeof(int32_t) * (size_t)(a.N + 1) : 0);
   auto kern = lse_gather_kernel<T, K>;
-  static bool attr_set[2][4] = {};  // (dtype, log2 K); benign race: same value
-  bool& done = attr_set[sizeof(T) == 4 ? 0 : 1][K == 1 ? 0 : (K == 2 ? 1 : (K == 4 ? 2 : 3))];
-  if (!done) {
+  {
     const int max_smem = kStages * kStageBytes + (int)sizeof(int32_t) * kSmemOffsets;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaError_t e = ensure_dynamic_smem((const void*)kern, max_smem);
     if (e != cudaSuccess) return e;
-    done = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];

@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "grpo.h"
+#include "host_ctx.cuh"
 
 namespace grpo {
 namespace {
@@ -29,62 +30,26 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 // The array's device address belongs to a CUDA context: a device reset or a
 // non-primary context on the same device gives the same symbol another
-// address.  The cache is therefore keyed on the current context's unique id
-// (cuCtxGetId: ids are never reused within a process), resolved through the
-// runtime's driver entry points so the library needs no link to libcuda.
-using CtxGetCurrentFn = int (*)(void** ctx);
-using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
-
+// address.  The cache is therefore keyed on the current context's unique id.
 struct CachedAddress {
   unsigned long long ctx_id;
   void* addr;
 };
 
 std::mutex g_mutex;
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
 constexpr int kCacheSlots = 64;
 CachedAddress g_cache[kCacheSlots] = {};
 int g_cache_used = 0;
 int g_cache_next = 0;  // slot replaced next once every slot is taken
 
-cudaError_t resolve_driver_calls() {
-  if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return cudaSuccess;
-  void* a = nullptr;
-  void* b = nullptr;
-  cudaDriverEntryPointQueryResult qa, qb;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000,
-                                                   cudaEnableDefault, &qa);
-  if (e != cudaSuccess) return e;
-  e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb);
-  if (e != cudaSuccess) return e;
-  if (qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !a || !b)
-    return cudaErrorNotSupported;
-  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
-  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
-  return cudaSuccess;
-}
-
 // Device address of g_static_scratch in the calling thread's current context
 // (the current device's primary context unless the caller made another one
 // current).  The first call in a context looks it up with cudaGetSymbolAddress.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  unsigned long long id = 0;
+  cudaError_t e = current_context_id(&id);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> g(g_mutex);
-  e = resolve_driver_calls();
-  if (e != cudaSuccess) return e;
-  void* ctx = nullptr;
-  if (g_ctx_get_current(&ctx) != 0) return cudaErrorDeviceUninitialized;
-  if (ctx == nullptr) {
-    // no context current yet: make the device's primary context current
-    e = cudaSetDevice(dev);
-    if (e != cudaSuccess) return e;
-    if (g_ctx_get_current(&ctx) != 0 || ctx == nullptr) return cudaErrorDeviceUninitialized;
-  }
-  unsigned long long id = 0;
-  if (g_ctx_get_id(ctx, &id) != 0) return cudaErrorDeviceUninitialized;
   for (int k = 0; k < g_cache_used; ++k) {
     if (g_cache[k].ctx_id == id) {
       *out = g_cache[k].addr;
@@ -92,7 +57,7 @@ cudaError_t scratch_address(void** out) {
     }
   }
   void* p = nullptr;
-  e = cudaGetSymbolAddress(&p, g_static_scratch);  // `ctx` is current here
+  e = cudaGetSymbolAddress(&p, g_static_scratch);  // in the current context
   if (e != cudaSuccess) return e;
   int slot;
   if (g_cache_used < kCacheSlots) {
