@@ -118,12 +118,10 @@ def _child():
     d_ids, d_lens, d_adv, d_old = put(ids), put(lens), put(adv), put(old)
     ws_bytes = size(lib.grpo_workspace_size, N, C, V)
     nc = (N, C)
-    got = {}
 
     lp_, lse_, ws = alloc(4 * N * C), alloc(4 * N * C), alloc(ws_bytes)
     ok(lib.grpo_logprobs(d_logits, g.GRPO_BF16, N, P, C, V, d_ids, d_lens, lp_, lse_, ws,
                          ws_bytes, s0), "grpo_logprobs")
-    got["logprobs"] = (lp_, lse_)
 
     f_lp, f_lse, f_w, f_loss = alloc(4 * N * C), alloc(4 * N * C), alloc(4 * N * C), alloc(4)
     f_dl, ws2 = alloc(2 * N * T * V), alloc(ws_bytes)
