@@ -76,6 +76,8 @@ def test_mask_validation(lib):
     assert lib.grpo_mask(A(0x1004), 2, 4, 4, 2, None, A(0x2000), None) == MISALIGNED
     assert lib.grpo_mask(A(0x1000), 2, 4, 4, 2, None, A(0x2002), None) == MISALIGNED
     assert lib.grpo_mask(None, 0, 4, 4, 2, None, None, None) == OK  # nothing to do
+    big = (1 << 63) - 1  # P + C would not fit in int64
+    assert lib.grpo_mask(A(0x1000), 2, big, 4, 2, None, A(0x2000), None) == UNSUPPORTED
 
 
 def test_advantage_validation(lib):
@@ -123,6 +125,7 @@ def test_fwd_validation(lib):
     assert _fwd(lib, ids=A(0x20004)) == MISALIGNED
     assert _fwd(lib, ws_bytes=64) == WORKSPACE
     assert _fwd(lib, N=1 << 20, C=1 << 12) == UNSUPPORTED   # N*C >= 2^31
+    assert _fwd(lib, P=(1 << 63) - 1) == UNSUPPORTED         # P + C would not fit in int64
 
 
 def _bwd(lib, **kw):

@@ -154,6 +154,7 @@ grpo_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GRPO_OK : GRPO_
 grpo_status check_shapes(grpo_dtype dtype, int64_t N, int64_t P, int64_t C, int64_t V) {
   if (dtype != GRPO_F32 && dtype != GRPO_BF16) return GRPO_ERR_UNSUPPORTED;
   if (N < 0 || P < 1 || C < 0 || V < 1) return GRPO_ERR_INVALID_ARG;
+  if (P > INT64_MAX - C) return GRPO_ERR_UNSUPPORTED;  // P + C is formed below
   if (N > 0 && C > 0 && N > (int64_t)INT32_MAX / C) return GRPO_ERR_UNSUPPORTED;  // N*C < 2^31
   const int64_t elems = mul3(N, P + C, V);
   if (elems < 0 || elems > INT64_MAX / 4) return GRPO_ERR_UNSUPPORTED;
@@ -196,7 +197,7 @@ grpo_status grpo_mask(const int64_t* input_ids, int64_t N, int64_t P, int64_t C,
   if (N < 0 || P < 0 || C < 0) return GRPO_ERR_INVALID_ARG;
   if (N == 0) return GRPO_OK;
   if (len == nullptr || (C > 0 && input_ids == nullptr)) return GRPO_ERR_INVALID_ARG;
-  if (mul3(N, P + C, 8) < 0 || C > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
+  if (P > INT64_MAX - C || mul3(N, P + C, 8) < 0 || C > INT32_MAX) return GRPO_ERR_UNSUPPORTED;
   if (!aligned(input_ids, 8) || !aligned(len, 4)) return GRPO_ERR_MISALIGNED;
   stream_take_last(stream);
   const cudaError_t e = launch_mask(input_ids, N, P, C, eos_id, mask, len, (cudaStream_t)stream);
