@@ -624,6 +624,40 @@ def rank_aggregate(dist, dev, elapsed: float, t_valid: int, contrast: int):
     return float(t[0]), int(n[0].item()), int(n[1].item())
 
 
+def host_mem_available() -> int | None:
+    """MemAvailable of the host, in bytes (None where /proc/meminfo is not
+    readable)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
+def e2e_fits(b: "Batch", world: int, dist) -> tuple[bool, str]:
+    """Whether every rank on this host can pin its end-to-end buffers (a host
+    copy of the logits and one of the gradient per rank) within 60% of the
+    host's available memory; all ranks take the same decision, since the leg
+    has collectives inside."""
+    import torch
+    need = 2 * b.logits.numel() * b.logits.element_size()
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    unknown = 1 << 62
+    avail = host_mem_available()
+    avail = unknown if avail is None else avail
+    if world > 1:  # the smallest over the ranks: every rank decides alike
+        t = torch.tensor([avail], device=b.logits.device, dtype=torch.int64)
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        avail = int(t.item())
+    ok = avail == unknown or need * local <= 0.6 * avail
+    why = ("" if ok else f"{local} rank(s) on a host would pin {need * local / 1e9:.3g} GB of "
+           f"host memory, more than 60% of the {avail / 1e9:.3g} GB available there")
+    return ok, why
+
+
 def run_e2e(args, g, b: Batch, stream, world: int, dist) -> dict:
     """The headline metric end to end through the public API, with the
     step's inputs and results in pinned host memory: every step copies the
@@ -811,7 +845,13 @@ def run_ours(args, w0: wl.Workload):
     if args.also_other_path and world == 1:
         paths = path_summary(g, b, peak, args.steps, args.warmup, stream)
 
-    e2e = None if args.no_e2e else run_e2e(args, g, b, stream, world, dist)
+    e2e, e2e_skipped = None, None
+    if not args.no_e2e:
+        fits, why = e2e_fits(b, world, dist)
+        if fits:
+            e2e = run_e2e(args, g, b, stream, world, dist)
+        else:
+            e2e_skipped = why
     inputs = input_record(w, b.ids_np, b.R_np, b.logits)
 
     # the other workloads of the benchmark plan, one at a time, after this
@@ -888,7 +928,8 @@ def run_ours(args, w0: wl.Workload):
                          "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": kbytes},
-            "e2e": None if e2e is None else {
+            "e2e": ({"value": None, "unit": UNIT, "skipped": e2e_skipped}
+                    if e2e_skipped is not None else None) if e2e is None else {
                 "value": t_valid_all / e2e["s_per_step"], "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],

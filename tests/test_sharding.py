@@ -115,3 +115,42 @@ def test_bench_rank_aggregate_two_ranks():
         assert p.exitcode == 0
     for r in range(2):
         assert res[r] == (1.5, 300, 1)
+
+
+def _fits_rank(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    os.environ["LOCAL_WORLD_SIZE"] = str(world)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import types
+
+        import bench
+        # rank 1's host reports too little memory for both ranks' pinned buffers
+        bench.host_mem_available = lambda: (1 << 40) if rank == 0 else (1 << 10)
+        b = types.SimpleNamespace(logits=torch.zeros((4, 1024), dtype=torch.bfloat16))
+        q.put((rank, bench.e2e_fits(b, world, dist)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_e2e_skip_agrees_over_ranks():
+    """The end-to-end leg has collectives inside, so when one rank's host
+    cannot pin the buffers every rank skips it, with the reason."""
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 30500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_fits_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(2):
+        ok, why = res[r]
+        assert ok is False and "would pin" in why and "1.02e-06 GB available" in why
