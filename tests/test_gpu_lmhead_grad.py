@@ -305,23 +305,31 @@ PASSES_SKIP = wl.variant(PASSES, name="lmg_passes_skip", beta=0.0, ref_sigma=Non
                          forced={"rewards": [1.0, 0.0, 0.0, 1.0, 0.0, 1.0, 0.0, 0.0] + [0.0] * 8})
 
 
-@pytest.mark.parametrize("rows_per_pass,flags,wk", [(256, None, PASSES), (512, None, PASSES),
-                                                    (256, 1, PASSES_SKIP), (0, 1, PASSES_SKIP)],
-                         ids=["R256", "R512", "R256_skip", "one_pass_skip"])
-def test_lmhead_grads_in_passes(rows_per_pass, flags, wk):
+# two 512-column d tiles (896 = 512 + 384) and 40 vocabulary blocks: 80
+# dweight items per pass, more than one round of CTA pairs, so every pass adds
+# its items with the d tiles rotated over the rounds
+PASSES_WIDE = wl.variant(PASSES, name="lmg_passes_wide", V=10007, eos_id=10000)
+
+
+@pytest.mark.parametrize("rows_per_pass,flags,wk,d",
+                         [(256, None, PASSES, 384), (512, None, PASSES, 384),
+                          (256, 1, PASSES_SKIP, 384), (0, 1, PASSES_SKIP, 384),
+                          (256, None, PASSES_WIDE, 896)],
+                         ids=["R256", "R512", "R256_skip", "one_pass_skip", "R256_d896"])
+def test_lmhead_grads_in_passes(rows_per_pass, flags, wk, d):
     """The backward in passes of 256 or 512 rows (several passes with rows,
     a ragged last one, and passes with none) against the oracle element by
     element: each pass stores or adds its part of dweight and writes its rows
     of dhidden."""
     n = H.g()
     w = H.with_contrast(wk)
-    hidden, weight, t_ids, lens, out, h = _setup(w, 384)
+    hidden, weight, t_ids, lens, out, h = _setup(w, d)
     T_valid = int(h["len"].sum())
     assert T_valid > 2 * 256 + 1 and T_valid % 256 != 0
     g = 2.5
     gt = torch.tensor([g], dtype=torch.float32, device="cuda")
-    need = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384, rows_per_pass)
-    full = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, 384)
+    need = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, d, rows_per_pass)
+    full = n.grpo_lmhead_bwd_workspace_size(w.N, w.C, w.V, d)
     assert (need < full) == (rows_per_pass > 0)
     ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
     dh, dw, _ = n.grpo_lmhead_loss_bwd(hidden, weight, w.P, t_ids, lens, out["lse"], out["w"],
