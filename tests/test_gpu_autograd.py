@@ -67,3 +67,39 @@ def test_bf16_logits_grad_dtype_and_shape():
     dl = n.grpo_loss_bwd(logits.detach(), w.P, t_ids, lens, out["lse"], out["w"])
     torch.cuda.synchronize()
     assert torch.equal(dl.view(torch.int16), logits.grad.view(torch.int16))
+
+
+@pytest.mark.parametrize("rows_per_pass", [None, 0], ids=["scored_rows", "every_row"])
+def test_lmhead_backward_gives_the_c_abi_gradients(rows_per_pass):
+    """GRPOLMHeadLoss: the loss of grpo_lmhead_loss_fwd, and loss.backward()
+    stores grpo_lmhead_loss_bwd's dhidden and dweight (whose parity with the
+    oracle the LM-head gradient tests establish) in the parameters' bf16,
+    scaled by the upstream gradient."""
+    from vocab_wide_logprob_gb300.autograd import grpo_lmhead_loss
+    w = H.with_contrast(wl.variant(wl.QWEN_G8, name="autograd_lm", B=2, G=4, P=8, C=24, V=1000,
+                                   eos_id=999, seed=81))
+    d = 128
+    n = H.g()
+    ids = H.dev(wl.make_ids(w))
+    _, lens = n.grpo_mask(ids, w.P, w.C, w.eos_id)
+    adv = n.grpo_advantage(H.dev(wl.make_rewards(w)), w.G)
+    gen = torch.Generator().manual_seed(5)
+    hidden = torch.randn((w.N, w.T, d), generator=gen).to(torch.bfloat16).cuda()
+    weight = (torch.randn((w.V, d), generator=gen) * 0.05).to(torch.bfloat16).cuda()
+    hidden.requires_grad_(True)
+    weight.requires_grad_(True)
+    loss = grpo_lmhead_loss(hidden, weight, w.P, ids, lens, adv, rows_per_pass=rows_per_pass)
+    assert loss.shape == () and loss.requires_grad
+    (loss * 2.0).backward()
+
+    f = n.grpo_lmhead_loss_fwd(hidden.detach(), weight.detach(), w.P, ids, lens, adv)
+    gt = torch.tensor([2.0], dtype=torch.float32, device="cuda")
+    rpp = int(lens.sum().item()) if rows_per_pass is None else rows_per_pass
+    dh, dw, _ = n.grpo_lmhead_loss_bwd(hidden.detach(), weight.detach(), w.P, ids, lens,
+                                       f["lse"], f["w"], gt, rows_per_pass=rpp)
+    torch.cuda.synchronize()
+    assert torch.equal(loss.detach().reshape(1).view(torch.int32), f["loss"].view(torch.int32))
+    assert hidden.grad.dtype == torch.bfloat16 and weight.grad.dtype == torch.bfloat16
+    assert torch.equal(hidden.grad.view(torch.int16), dh.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(weight.grad.view(torch.int16), dw.to(torch.bfloat16).view(torch.int16))
+    assert float(dw.abs().sum()) > 0  # the group has reward contrast: a live gradient
