@@ -190,7 +190,7 @@ def cpu_model() -> str | None:
 
 def run_env(dev) -> dict:
     """What produced the numbers: GPU, driver, toolkit, torch, and a hash of
-    the library's sources (the GPU machine gets the tree without its git history)."""
+    the library's sources (a copy of the tree may come without its git history)."""
     import torch
     env = {"gpu": torch.cuda.get_device_name(dev), "torch": torch.__version__,
            "cuda_runtime": torch.version.cuda, "driver": None, "nvcc": None}
