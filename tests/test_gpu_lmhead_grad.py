@@ -107,6 +107,9 @@ SMALL = [
                                           C=120, V=6001, eos_id=6000, seed=86), 1664, None),
     ("V6001_d1152_three_tiles", wl.variant(wl.QWEN_G8, name="lmg_6001_1152", B=1, G=4, P=5,
                                            C=120, V=6001, eos_id=6000, seed=87), 1152, 0.5),
+    # a vocabulary smaller than one 256-column tile: the only tile runs past V
+    ("V100_d128_subtile", wl.variant(wl.QWEN_G8, name="lmg_100_128", B=1, G=4, P=4, C=20,
+                                     V=100, eos_id=99, seed=89), 128, 1.5),
     # Qwen2.5-7B's hidden size: seven 512-column d tiles, 56 k-steps per
     # projection tile
     ("V2000_d3584", wl.variant(wl.QWEN_G8, name="lmg_2000_3584", B=1, G=4, P=5, C=60, V=2000,
